@@ -1,0 +1,437 @@
+"""Benchmark: paged decode attention on GB300.
+
+Default workload: the LLaMA-13B-shaped full decode step — 40 layers x (kv_append of the
+new token of each of 48 sequences + paged_decode_attention over 48 sequences x 40 heads x
+2048 tokens, d 128, fp16 K/V, block size 16).  The pool is ~75 GiB, far larger than L2,
+so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 oracle on the
+host cores instead (the reference arm of this build).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak); seq-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- workloads
+def make_workload(name: str):
+    import workloads as W
+    if name == "llama13b":
+        w = W.llama13b()
+    elif name == "llama7b":
+        w = W.llama7b()
+        w.lens = [n + w.steps for n in w.lens]       # context after the last of the 64 steps
+    elif name.startswith("ragged"):
+        # ragged_f16_b16 | ragged_fp8_b8 ...
+        _, dt, b = name.split("_")
+        w = W.ragged(int(b[1:]))
+        w.kv = dt
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    if not hasattr(w, "kv"):
+        w.kv = w.dtype
+    return w
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes one paged_decode_attention call must move at minimum (one layer):
+    K+V of every cached token, q, out (fp32), the used block-table entries, context_lens,
+    and for FP8 pools the two per-block scales."""
+    kv_elem = 1 if w.kv == "fp8" else 2
+    H, d, B = w.num_heads, w.head_dim, w.block_size
+    kv = sum(w.lens) * H * d * kv_elem * 2
+    q = w.batch * H * d * 2
+    out = w.batch * H * d * 4
+    tables = sum(-(-n // B) for n in w.lens) * 4
+    lens = w.batch * 4
+    scales = sum(-(-n // B) for n in w.lens) * 8 if w.kv == "fp8" else 0
+    return kv + q + out + tables + lens + scales
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel_src: str):
+    """DRAM bytes per launch from the committed ncu summary, only if the kernel source
+    is unchanged since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "attention_llama13b_traffic.txt")
+    try:
+        rec = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                rec[k.strip()] = v.strip()
+        h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+        if rec.get("source_sha256_16") == h:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join("/tmp", f"kvpaged_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+def _oracle_worker(args):
+    """Time the oracle on `units` (sequence, head) decode problems of context n (float64)."""
+    units, n, d, seed = args
+    import numpy as np
+    from oracle import attention as OA
+    rng = np.random.default_rng(seed)
+    data = [(rng.standard_normal(d).astype(np.float16),
+             rng.standard_normal((n, d), dtype=np.float32).astype(np.float16),
+             rng.standard_normal((n, d), dtype=np.float32).astype(np.float16)) for _ in range(units)]
+    t0 = time.perf_counter()
+    for q, K, V in data:
+        OA.decode_attention_one(q, K, V, 1.0 / math.sqrt(d))
+    return time.perf_counter() - t0
+
+
+def oracle_rate(w, units_total: int):
+    """Oracle throughput on a bounded sample of the workload, in the metric's unit (GB/s of
+    algorithmic bytes), using every available host core (one single-threaded process each)."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    n = max(w.lens)
+    per = [units_total // cores + (1 if i < units_total % cores else 0) for i in range(cores)]
+    per = [p for p in per if p > 0]
+    env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    old = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(len(per)) as pool:
+            t0 = time.perf_counter()
+            times = pool.map(_oracle_worker, [(p, n, w.head_dim, 1000 + i) for i, p in enumerate(per)])
+            wall = time.perf_counter() - t0
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    busy = max(times)
+    bytes_per_unit = n * w.head_dim * 2 * 2 + w.head_dim * 2 + w.head_dim * 4
+    gbs = units_total * bytes_per_unit / busy / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": len(per), "kind": "oracle",
+            "sample": f"{units_total} (sequence, head) units of context {n}, d {w.head_dim}, "
+                      f"fp16 inputs widened to float64; numpy, one single-threaded process per core",
+            "seconds": busy, "wall_seconds": wall}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    w = make_workload(args.workload)
+    units = args.ref_units
+    for _ in range(args.warmup):
+        oracle_rate(w, max(1, units // 8))
+    t0 = time.perf_counter()
+    vals = [oracle_rate(w, units) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    value = sum(v["value"] for v in vals) / len(vals)
+    per_step_units = units
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "sample_units_per_step": per_step_units},
+        "cpu_baseline": {k: vals[-1][k] for k in ("kind", "cores", "sample")} | {"value": value, "unit": "GB/s"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import workloads as W
+    from paged_kv_cache_169_gb300 import build as B
+    from paged_kv_cache_169_gb300.cache import PagedKVCache
+
+    world, rank, local = dist_setup(args.gpus)
+    B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = make_workload(args.workload)
+    L, H, d, BS = w.num_layers, w.num_heads, w.head_dim, w.block_size
+    nbs = [-(-n // BS) for n in w.lens]
+    w.num_blocks = max(w.num_blocks, sum(nbs))
+    cache = PagedKVCache(L, w.num_blocks, BS, H, d, w.kv, device=dev)
+    for l in range(L):
+        if w.kv == "fp8":
+            for pool, sc, key in ((cache.k[l], cache.k_scale[l], 0), (cache.v[l], cache.v_scale[l], 1)):
+                g = torch.Generator(device=dev)
+                g.manual_seed(w.seed * 1000 + 2 * l + key)
+                for b0 in range(0, w.num_blocks, 4096):
+                    nb = min(4096, w.num_blocks - b0)
+                    x = torch.randn((nb, H, BS, d), generator=g, device=dev).half().float()
+                    s = (x.abs().amax(dim=(1, 2, 3)).clamp_min(2.0 ** -20 * 448) / 448.0).float()
+                    pool[b0:b0 + nb].copy_((x / s.view(-1, 1, 1, 1)).clamp(-448, 448)
+                                           .to(torch.float8_e4m3fn).view(torch.uint8))
+                    sc[b0:b0 + nb].copy_(s)
+        else:
+            W.device_fill_normal(cache.k[l], w.seed * 1000 + 2 * l)
+            W.device_fill_normal(cache.v[l], w.seed * 1000 + 2 * l + 1)
+    tables = W.shuffled_tables(w, nbs)
+    slots_h = np.array([int(tables[s, (n - 1) // BS]) * BS + (n - 1) % BS for s, n in enumerate(w.lens)],
+                       dtype=np.int64)
+    lens_h = np.array(w.lens, dtype=np.int32)
+    tdt = torch.float16
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed * 7 + 1)
+    q = torch.randn((L, w.batch, H, d), generator=g, device=dev).to(tdt)
+    k_new = torch.randn((L, w.batch, H, d), generator=g, device=dev).to(tdt)
+    v_new = torch.randn((L, w.batch, H, d), generator=g, device=dev).to(tdt)
+    bt = torch.from_numpy(tables).to(dev)
+    cl = torch.from_numpy(lens_h).to(dev)
+    slots = torch.from_numpy(slots_h).to(dev)
+    out = torch.empty((L, w.batch, H, d), dtype=torch.float32, device=dev)
+    max_ctx = max(w.lens)
+    ws = cache.workspace(w.batch, max_ctx, args.partition)
+    stream = torch.cuda.current_stream(dev)
+
+    from paged_kv_cache_169_gb300 import abi
+    plan_parts = ws.numel() > 256                                     # split-context partials in use
+    launches_per_layer = 2 + (1 if plan_parts else 0) + (w.batch - 1) // 1024
+
+    def step(ev=None):
+        for l in range(L):
+            cache.append(l, k_new[l], v_new[l], slots)
+            if ev is not None:
+                ev[l][0].record(stream)
+            cache.attention(l, q[l], bt, cl, max_ctx, w.scale, out=out[l], partition_tokens=args.partition,
+                            workspace=ws)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if cache.device_error() != 0:
+        raise SystemExit("device error during warm-up")
+
+    # ---- device-timed region
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(world, t_start.elapsed_time(t_end))
+    attn_ms = [e[0].elapsed_time(e[1]) for row in evs for e in row]
+    attn_ms_mean = sum(attn_ms) / len(attn_ms)
+
+    # ---- end-to-end through the public API with host buffers
+    pin = dict(q=torch.empty(q.shape, dtype=tdt).pin_memory(), k=torch.empty(q.shape, dtype=tdt).pin_memory(),
+               v=torch.empty(q.shape, dtype=tdt).pin_memory(), out=torch.empty(out.shape).pin_memory(),
+               slots=torch.from_numpy(slots_h).pin_memory(), bt=torch.from_numpy(tables).pin_memory(),
+               cl=torch.from_numpy(lens_h).pin_memory())
+    pin["q"].copy_(q.cpu())
+    pin["k"].copy_(k_new.cpu())
+    pin["v"].copy_(v_new.cpu())
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "slots", "bt", "cl"))
+    d2h = pin["out"].numel() * pin["out"].element_size()
+
+    def e2e_step():
+        q.copy_(pin["q"], non_blocking=True)
+        k_new.copy_(pin["k"], non_blocking=True)
+        v_new.copy_(pin["v"], non_blocking=True)
+        slots.copy_(pin["slots"], non_blocking=True)
+        bt.copy_(pin["bt"], non_blocking=True)
+        cl.copy_(pin["cl"], non_blocking=True)
+        step()
+        pin["out"].copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    err = cache.device_error()
+    if err != 0:
+        raise SystemExit(f"device error bits {err}")
+
+    # ---- numbers
+    alg = algorithmic_bytes(w)
+    step_bytes = alg * L
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
+    peak, peak_src = measured_peak()
+    achieved = alg / (attn_ms_mean / 1e3) / 1e9
+    src = os.path.join(ROOT, "paged_kv_cache_169_gb300", "csrc", "decode_attention.cu")
+    traffic = traffic_record(src) if args.workload == "llama13b" else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_rate(w, args.cpu_units)
+        cpu.pop("wall_seconds", None)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32-accum/" + w.kv, "data": "synthetic",
+        "config": {"workload": args.workload, "layers": L, "batch": w.batch, "heads": H, "head_dim": d,
+                   "block_size": BS, "kv_dtype": w.kv, "context_mean": sum(w.lens) / len(w.lens),
+                   "context_max": max_ctx, "pool_gib": round(2 * L * w.num_blocks * H * BS * d *
+                                                             (1 if w.kv == "fp8" else 2) / 2 ** 30, 2),
+                   "l2": "no flush: inputs (the KV pool) larger than L2",
+                   "partition_tokens": args.partition or "auto", "parallelism": f"replica x{world}"},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "seq_steps_per_s": world * w.batch * args.steps / (elapsed_ms / 1e3),
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (partition + reduce)",
+                     "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg, "mean_call_ms": attn_ms_mean},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * step_bytes * args.steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches_per_layer * L * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    cache.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    del abi
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama13b")
+    ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library choice)")
+    ap.add_argument("--cpu-units", type=int, default=3840, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--ref-units", type=int, default=768, help="oracle units per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,238 @@
+/*
+ * kvpaged — single-token decode attention over a block-paged KV cache (GB300, sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only.  Every device buffer is owned by the
+ * caller; the library never frees caller memory.  Every call returns 0 on
+ * success or a negative kv_status; no C++ exception crosses this boundary.
+ * Device calls are asynchronous on the given stream and never synchronise,
+ * except kv_get_device_error.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [KV Cache篇]      "大模型推理加速——KV Cache篇"
+ *   [KV缓存机制解析]  "KV缓存机制解析：优化大型语言模型推理性能"
+ *   [PagedAttention]  "KV Cache与PagedAttention：大模型推理显存优化方案"
+ *
+ * Pool layout (per layer, chosen for this library):
+ *   K, V: [num_blocks][num_heads][block_size][head_dim] elements of `dtype`.
+ *   One (block, head) tile is block_size*head_dim contiguous elements, so a
+ *   tile moves as one bulk copy.  Slot id = physical_block * block_size + offset.
+ *   FP8 pools add per-layer scale arrays k_scale[], v_scale[]: one float32 per
+ *   physical block (shared by all heads), capacity rounded up to a multiple of 4
+ *   floats, 16-byte aligned.  Stored value = e4m3 code * scale.
+ */
+#ifndef KVPAGED_H
+#define KVPAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported from libkvpaged.so (built with hidden default visibility). */
+#if defined(__GNUC__)
+#define KV_API __attribute__((visibility("default")))
+#else
+#define KV_API
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* kv_stream_t;
+
+typedef enum {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = -1,  /* bad pointer, size, alignment, layer, dtype or shape  */
+    KV_ERR_NO_BLOCKS = -2,    /* allocator: free list too short; state left unchanged */
+    KV_ERR_STATE = -3,        /* allocator: unknown/freed sequence, refcount misuse     */
+    KV_ERR_CUDA = -4,         /* a CUDA runtime call failed (launch, query, memcpy)     */
+    KV_ERR_DEVICE = -5,       /* kv_get_device_error found a device-side error bit      */
+    KV_ERR_UNSUPPORTED = -6   /* valid request this build does not implement            */
+} kv_status;
+
+typedef enum { KV_F32 = 0, KV_F16 = 1, KV_FP8_E4M3 = 2 } kv_dtype;
+
+/* Device-side error bits (kv_get_device_error).  Kernels never trap: they set a
+ * bit, skip or clamp the offending access, and finish. */
+enum {
+    KV_DEVERR_SLOT = 1,        /* slot_mapping entry >= num_blocks*block_size           */
+    KV_DEVERR_BLOCK_ID = 2,    /* block table / copy pair id outside [0, num_blocks)    */
+    KV_DEVERR_CONTEXT = 4,     /* context_len < 0, > max_blocks*block_size or > max_context */
+    KV_DEVERR_TIMEOUT = 8      /* a bounded mbarrier wait ran out (about one second)    */
+};
+
+typedef struct {
+    int num_layers;   /* >= 1, <= 4096                              */
+    int num_blocks;   /* physical blocks per layer, >= 1            */
+    int block_size;   /* B: 8, 16 or 32 tokens                      */
+    int num_heads;    /* H: 1 .. 256                                */
+    int head_dim;     /* d: 64 or 128                               */
+    kv_dtype dtype;   /* element type of the pool                   */
+} kv_pool_desc;
+
+typedef struct kv_pool kv_pool;    /* opaque; bound to the device current at creation */
+typedef struct kv_alloc kv_alloc;  /* opaque; host memory only                        */
+
+typedef struct {
+    int num_blocks;        /* pool size                                                 */
+    int free_blocks;       /* on the free list                                          */
+    int shared_blocks;     /* reference count > 1                                       */
+    int num_seqs;          /* live sequences                                            */
+    int64_t used_slots;    /* sum over live sequences of their length                   */
+    int64_t wasted_slots;  /* sum over live sequences of n_blocks*B - length (tail waste,
+                              counted per sequence; [PagedAttention] §2.2)              */
+} kv_alloc_stats_t;
+
+/* ---------------------------------------------------------------- misc */
+
+/* Static string for a kv_status value.  Never NULL. */
+KV_API const char* kv_status_str(int status);
+
+/* Library ABI version (major*100 + minor). */
+KV_API int kv_version(void);
+
+/* ---------------------------------------------------------------- pool */
+
+/* Wrap caller-owned device memory as a paged KV pool.
+ *   desc        shape and dtype (validated: see kv_pool_desc).
+ *   k_layers, v_layers  host arrays of desc->num_layers device pointers, each to
+ *               num_blocks*num_heads*block_size*head_dim elements, 16-byte aligned.
+ *   k_scales, v_scales  FP8 only: host arrays of num_layers device pointers to float32
+ *               [round_up(num_blocks, 4)], 16-byte aligned; must be NULL otherwise.
+ *   out         receives the handle.
+ * The pool keeps copies of the pointers, not the memory.  It allocates one small
+ * device word for device error bits (its only allocation).
+ * Paged storage of the cache: [PagedAttention] §2.1 and §3.1 (global block pool). */
+KV_API int kv_pool_create(const kv_pool_desc* desc, void* const* k_layers, void* const* v_layers,
+                   float* const* k_scales, float* const* v_scales, kv_pool** out);
+
+/* Release the handle (not the caller's memory).  Synchronises nothing; the caller
+ * must not destroy a pool with work still queued on it. */
+KV_API int kv_pool_destroy(kv_pool* pool);
+
+/* Copy of the descriptor the pool was created with. */
+KV_API int kv_pool_get_desc(const kv_pool* pool, kv_pool_desc* desc);
+
+/* Read (and if clear != 0, reset) the pool's device error bits.  Enqueues a copy on
+ * `stream` and synchronises that stream.  Returns KV_ERR_DEVICE if any bit is set
+ * (bits in *code), else KV_OK with *code = 0. */
+KV_API int kv_get_device_error(kv_pool* pool, kv_stream_t stream, int clear, int* code);
+
+/* ---------------------------------------------------------------- append */
+
+/* Write num_tokens new tokens' K and V into their slots for one layer.
+ *   k, v           device, [num_tokens][num_heads][head_dim] of in_dtype, 16-byte aligned.
+ *                  in_dtype must equal the pool dtype for F32/F16 pools; an FP8 pool
+ *                  takes F16 or F32 input and stores
+ *                  e4m3 = round-nearest-even-satfinite(fp32(x) / scale[block]), where
+ *                  scale[block] is the value already in the layer's scale array
+ *                  (the caller sets a fresh block's scale before appending into it).
+ *   slot_mapping   device int64 [num_tokens]; slot < 0 means "skip this token".
+ * Token i, head h lands at block slot/B, offset slot%B.  Out-of-range slots set
+ * KV_DEVERR_SLOT and are skipped.  Bit-exact copy for F32/F16.
+ * The cache write of [KV Cache篇] §3.1 (cache_k[:, start_pos] = xk) and
+ * write_KV_to_block of [PagedAttention] §3.3. */
+KV_API int kv_append(kv_pool* pool, int layer, const void* k, const void* v, kv_dtype in_dtype,
+              const int64_t* slot_mapping, int num_tokens, kv_stream_t stream);
+
+/* ---------------------------------------------------------------- copy-on-write */
+
+/* For each pair (src, dst) in pairs (device int32 [num_pairs][2]) copy the whole
+ * physical block src onto dst — K and V, every head, all B slots, and for FP8
+ * pools both scales — in every layer of [layer_begin, layer_end).  Bit-exact.
+ * dst blocks must be distinct and must not appear as a src (result undefined
+ * otherwise).  Ids outside [0, num_blocks) set KV_DEVERR_BLOCK_ID and are skipped.
+ * copy_block of [PagedAttention] §3.3 (batched, as its "批量处理多个块的CoW" asks). */
+KV_API int kv_copy_blocks(kv_pool* pool, const int32_t* pairs, int num_pairs, int layer_begin,
+                   int layer_end, kv_stream_t stream);
+
+/* ---------------------------------------------------------------- decode attention */
+
+/* Bytes of device workspace paged_decode_attention needs for these arguments
+ * (0 on invalid arguments).  partition_tokens as in paged_decode_attention. */
+KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int max_context,
+                                   int partition_tokens);
+
+/* out[s,h,:] = softmax(scale * q[s,h,:] . K_s^T) . V_s  over the first
+ * context_lens[s] tokens of sequence s, for every sequence s and head h, read
+ * through block_tables.  One query token per sequence (decode).
+ *   q             device [batch][num_heads][head_dim]: float32 for F32 pools, float16
+ *                 for F16 and FP8 pools; 16-byte aligned.
+ *   out           device float32 [batch][num_heads][head_dim] (written, not accumulated).
+ *   block_tables  device int32 [batch][max_blocks_per_seq]; entry j of row s is the
+ *                 physical block of tokens [j*B, (j+1)*B) of sequence s.
+ *   context_lens  device int32 [batch]; includes the token appended this step.
+ *                 0 gives out = 0.  Values above min(max_blocks_per_seq*B, max_context)
+ *                 are clamped and set KV_DEVERR_CONTEXT.
+ *   max_context   host upper bound of context_lens (sizes the split-context workspace).
+ *   scale         score multiplier, usually 1/sqrt(head_dim); finite and > 0.
+ *   partition_tokens  0 = library choice; else tokens per split-context partition,
+ *                 a multiple of 32 and at most 32*B.  Sequences longer than one
+ *                 partition are split, attended per partition and merged exactly
+ *                 (log-sum-exp) by a second kernel.
+ *   workspace     device, >= paged_decode_workspace_size(...) bytes, 256-byte aligned,
+ *                 contents need not be initialised; not shared between concurrent calls.
+ * Arithmetic: fp32 scores, fp32 online softmax, fp32 accumulation of V.
+ * The cached decode step of [KV Cache篇] §3.1 / [KV缓存机制解析] §5.1 over the
+ * block-table gather of [PagedAttention] §3.2, with [KV Cache篇] §6.3's tiling. */
+KV_API int paged_decode_attention(kv_pool* pool, int layer, const void* q, float* out,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int batch, int max_context,
+                           float scale, int partition_tokens, void* workspace,
+                           size_t workspace_bytes, kv_stream_t stream);
+
+/* ---------------------------------------------------------------- host block allocator */
+/* Host memory only; not thread-safe (the caller serialises).  Block ids are the
+ * physical ids of a kv_pool of the same num_blocks and block_size.
+ * Free list, first-fit allocation, per-block reference counts and copy-on-write:
+ * [PagedAttention] §3.1 and §3.3. */
+
+/* free_order: NULL for 0..num_blocks-1, else a permutation of the physical ids giving
+ * the initial free list, head first.  Allocation pops the head; a block whose count
+ * reaches 0 is pushed back on the head. */
+KV_API int kv_alloc_create(int num_blocks, int block_size, const int32_t* free_order, kv_alloc** out);
+KV_API int kv_alloc_destroy(kv_alloc* a);
+
+/* New empty sequence (length 0, no blocks). */
+KV_API int kv_alloc_seq_new(kv_alloc* a, int* seq_id);
+
+/* New sequence sharing every block of `parent` (each reference count + 1), same length. */
+KV_API int kv_alloc_seq_fork(kv_alloc* a, int parent, int* child);
+
+/* Reserve slots for the next `count` tokens of `seq` (count >= 1).  slots_out: host
+ * int64 [count].  A new block is taken whenever the length is a multiple of B.  If the
+ * first token lands in a block with reference count > 1, a copy is planned:
+ * cow_pair_out (host int32 [2]) receives (src, dst), the sequence's table points at dst
+ * and src's count drops by one; otherwise cow_pair_out = (-1, -1).  The caller copies
+ * (kv_copy_blocks) before writing.  Fails with KV_ERR_NO_BLOCKS, state unchanged, when
+ * the free list is too short for the whole request. */
+KV_API int kv_alloc_append_slots(kv_alloc* a, int seq, int count, int64_t* slots_out,
+                          int32_t* cow_pair_out);
+
+/* Drop the sequence: every block's count - 1, blocks reaching 0 return to the free list. */
+KV_API int kv_alloc_seq_free(kv_alloc* a, int seq);
+
+/* Length and block count of a live sequence. */
+KV_API int kv_alloc_seq_info(const kv_alloc* a, int seq, int* length, int* n_blocks);
+
+/* The sequence's block table (host int32, cap entries available); *n_blocks = its length. */
+KV_API int kv_alloc_block_table(const kv_alloc* a, int seq, int32_t* out, int cap, int* n_blocks);
+
+/* Padded tables for a batch: tables (host int32 [n][max_blocks], unused entries -1)
+ * and context_lens (host int32 [n]).  KV_ERR_INVALID_ARG if a table exceeds max_blocks. */
+KV_API int kv_alloc_build_tables(const kv_alloc* a, const int32_t* seqs, int n, int32_t* tables,
+                          int max_blocks, int32_t* context_lens);
+
+/* Reference count of one physical block. */
+KV_API int kv_alloc_ref_count(const kv_alloc* a, int block, int* ref);
+
+/* Current free list, head first (cap entries available); *n = its length. */
+KV_API int kv_alloc_free_list(const kv_alloc* a, int32_t* out, int cap, int* n);
+
+KV_API int kv_alloc_stats(const kv_alloc* a, kv_alloc_stats_t* stats);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVPAGED_H */

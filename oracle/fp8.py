@@ -91,10 +91,28 @@ def _round_half_even(v: float) -> int:
 
 
 def encode(x) -> np.ndarray:
-    """Vectorised (by a Python loop) encode of float values to uint8 codes."""
-    flat = np.asarray(x, dtype=np.float64).reshape(-1)
-    out = np.fromiter((encode_scalar(float(v)) for v in flat), dtype=np.uint8, count=flat.size)
-    return out.reshape(np.shape(x))
+    """Vectorised encode, same rule as ``encode_scalar``.
+
+    The non-negative codes 0x00..0x7E are increasing in value, so for a = |x| the
+    candidates are the two neighbouring table entries; the nearer wins, and on a tie
+    the even code (even mantissa) wins.  Beyond 448 the code saturates to 0x7E.
+    """
+    xf = np.asarray(x, dtype=np.float64)
+    flat = xf.reshape(-1)
+    mags = DECODE_TABLE[:0x7F]                         # values of codes 0x00..0x7E
+    a = np.abs(flat)
+    hi = np.clip(np.searchsorted(mags, a, side="left"), 1, 0x7E)
+    lo = hi - 1
+    d_lo = a - mags[lo]
+    d_hi = mags[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= MAX_FINITE, 0x7E, code)
+    code = np.where(a == 0.0, 0, code)
+    sign = np.signbit(flat).astype(np.int64) << 7
+    out = (code | sign).astype(np.uint8)
+    out = np.where(np.isnan(flat), NAN_CODE, out).astype(np.uint8)
+    return out.reshape(xf.shape)
 
 
 def quantize(x, scale) -> np.ndarray:

@@ -1,0 +1,180 @@
+// C ABI of kvpaged: argument validation and dispatch to the launchers.
+// Declarations and the contract of every entry point are in include/kvpaged.h.
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "kvp_internal.cuh"
+
+namespace {
+
+bool valid_desc(const kv_pool_desc* d) {
+    if (!d) return false;
+    if (d->num_layers < 1 || d->num_layers > 4096) return false;
+    if (d->num_blocks < 1) return false;
+    if (d->block_size != 8 && d->block_size != 16 && d->block_size != 32) return false;
+    if (d->num_heads < 1 || d->num_heads > 256) return false;
+    if (d->head_dim != 64 && d->head_dim != 128) return false;
+    if (d->dtype != KV_F32 && d->dtype != KV_F16 && d->dtype != KV_FP8_E4M3) return false;
+    // element offsets of a whole layer must fit the kernels' int64 arithmetic with room
+    const long long elems = 1ll * d->num_blocks * d->num_heads * d->block_size * d->head_dim;
+    return elems > 0 && elems < (1ll << 40);
+}
+
+void free_pool(kv_pool* p) {
+    if (!p) return;
+    std::free(p->k_layers);
+    std::free(p->v_layers);
+    std::free(p->k_scales);
+    std::free(p->v_scales);
+    delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kv_status_str(int status) {
+    switch (status) {
+        case KV_OK: return "ok";
+        case KV_ERR_INVALID_ARG: return "invalid argument";
+        case KV_ERR_NO_BLOCKS: return "no free blocks";
+        case KV_ERR_STATE: return "invalid allocator state";
+        case KV_ERR_CUDA: return "CUDA runtime error";
+        case KV_ERR_DEVICE: return "device-side error flag set";
+        case KV_ERR_UNSUPPORTED: return "unsupported";
+        default: return "unknown status";
+    }
+}
+
+int kv_version(void) { return 100; }
+
+int kv_pool_create(const kv_pool_desc* desc, void* const* k_layers, void* const* v_layers,
+                   float* const* k_scales, float* const* v_scales, kv_pool** out) {
+    if (!out) return KV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!valid_desc(desc) || !k_layers || !v_layers) return KV_ERR_INVALID_ARG;
+    const bool fp8 = desc->dtype == KV_FP8_E4M3;
+    if (fp8 != (k_scales != nullptr) || fp8 != (v_scales != nullptr)) return KV_ERR_INVALID_ARG;
+    const int L = desc->num_layers;
+    for (int l = 0; l < L; ++l) {
+        if (!k_layers[l] || !v_layers[l] || !kvp::aligned16(k_layers[l]) || !kvp::aligned16(v_layers[l]))
+            return KV_ERR_INVALID_ARG;
+        if (fp8 && (!k_scales[l] || !v_scales[l] || !kvp::aligned16(k_scales[l]) ||
+                    !kvp::aligned16(v_scales[l])))
+            return KV_ERR_INVALID_ARG;
+    }
+    kv_pool* p = new (std::nothrow) kv_pool{};
+    if (!p) return KV_ERR_INVALID_ARG;
+    p->desc = *desc;
+    p->k_layers = static_cast<void**>(std::calloc(L, sizeof(void*)));
+    p->v_layers = static_cast<void**>(std::calloc(L, sizeof(void*)));
+    if (fp8) {
+        p->k_scales = static_cast<float**>(std::calloc(L, sizeof(float*)));
+        p->v_scales = static_cast<float**>(std::calloc(L, sizeof(float*)));
+    }
+    if (!p->k_layers || !p->v_layers || (fp8 && (!p->k_scales || !p->v_scales))) {
+        free_pool(p);
+        return KV_ERR_INVALID_ARG;
+    }
+    std::memcpy(p->k_layers, k_layers, L * sizeof(void*));
+    std::memcpy(p->v_layers, v_layers, L * sizeof(void*));
+    if (fp8) {
+        std::memcpy(p->k_scales, k_scales, L * sizeof(float*));
+        std::memcpy(p->v_scales, v_scales, L * sizeof(float*));
+    }
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
+        cudaMalloc(&p->d_err, sizeof(int)) != cudaSuccess) {
+        free_pool(p);
+        return KV_ERR_CUDA;
+    }
+    if (cudaMemset(p->d_err, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(p->d_err);
+        free_pool(p);
+        return KV_ERR_CUDA;
+    }
+    *out = p;
+    return KV_OK;
+}
+
+int kv_pool_destroy(kv_pool* pool) {
+    if (!pool) return KV_ERR_INVALID_ARG;
+    int rc = cudaFree(pool->d_err) == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+    free_pool(pool);
+    return rc;
+}
+
+int kv_pool_get_desc(const kv_pool* pool, kv_pool_desc* desc) {
+    if (!pool || !desc) return KV_ERR_INVALID_ARG;
+    *desc = pool->desc;
+    return KV_OK;
+}
+
+int kv_get_device_error(kv_pool* pool, kv_stream_t stream, int clear, int* code) {
+    if (!pool || !code) return KV_ERR_INVALID_ARG;
+    int h = 0;
+    if (cudaMemcpyAsync(&h, pool->d_err, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return KV_ERR_CUDA;
+    if (clear && cudaMemsetAsync(pool->d_err, 0, sizeof(int), stream) != cudaSuccess) return KV_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return KV_ERR_CUDA;
+    *code = h;
+    return h ? KV_ERR_DEVICE : KV_OK;
+}
+
+int kv_append(kv_pool* pool, int layer, const void* k, const void* v, kv_dtype in_dtype,
+              const int64_t* slot_mapping, int num_tokens, kv_stream_t stream) {
+    if (!pool || layer < 0 || layer >= pool->desc.num_layers || num_tokens < 0) return KV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return KV_OK;
+    if (!k || !v || !slot_mapping || !kvp::aligned16(k) || !kvp::aligned16(v)) return KV_ERR_INVALID_ARG;
+    const kv_dtype pd = pool->desc.dtype;
+    if (pd == KV_FP8_E4M3) {
+        if (in_dtype != KV_F16 && in_dtype != KV_F32) return KV_ERR_INVALID_ARG;
+    } else if (in_dtype != pd) {
+        return KV_ERR_INVALID_ARG;
+    }
+    return kvp::launch_append(pool, layer, k, v, in_dtype, slot_mapping, num_tokens, stream);
+}
+
+int kv_copy_blocks(kv_pool* pool, const int32_t* pairs, int num_pairs, int layer_begin,
+                   int layer_end, kv_stream_t stream) {
+    if (!pool || num_pairs < 0 || layer_begin < 0 || layer_end < layer_begin ||
+        layer_end > pool->desc.num_layers)
+        return KV_ERR_INVALID_ARG;
+    if (num_pairs == 0 || layer_end == layer_begin) return KV_OK;
+    if (!pairs || num_pairs > 65535) return KV_ERR_INVALID_ARG;
+    return kvp::launch_copy_blocks(pool, pairs, num_pairs, layer_begin, layer_end, stream);
+}
+
+size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int max_context,
+                                   int partition_tokens) {
+    if (!pool) return 0;
+    kvp::AttnPlan plan;
+    if (kvp::plan_attention(pool, batch, max_context, partition_tokens, &plan) != KV_OK) return 0;
+    return plan.ws_bytes;
+}
+
+int paged_decode_attention(kv_pool* pool, int layer, const void* q, float* out,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int batch, int max_context,
+                           float scale, int partition_tokens, void* workspace,
+                           size_t workspace_bytes, kv_stream_t stream) {
+    if (!pool || layer < 0 || layer >= pool->desc.num_layers || batch < 0 || max_context < 0)
+        return KV_ERR_INVALID_ARG;
+    if (batch == 0) return KV_OK;
+    if (!q || !out || !block_tables || !context_lens || !workspace || max_blocks_per_seq < 1)
+        return KV_ERR_INVALID_ARG;
+    if (!kvp::aligned16(q) || !kvp::aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KV_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return KV_ERR_INVALID_ARG;
+    kvp::AttnPlan plan;
+    int rc = kvp::plan_attention(pool, batch, max_context, partition_tokens, &plan);
+    if (rc != KV_OK) return rc;
+    if (workspace_bytes < plan.ws_bytes) return KV_ERR_INVALID_ARG;
+    return kvp::launch_attention(pool, layer, q, out, block_tables, max_blocks_per_seq, context_lens,
+                                 batch, max_context, scale, plan, workspace, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// Internal declarations shared by the kvpaged CUDA translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvpaged.h"
+
+struct kv_pool {
+    kv_pool_desc desc;
+    int device;
+    int num_sms;
+    void** k_layers;     // host copies of the caller's per-layer device pointers
+    void** v_layers;
+    float** k_scales;    // FP8 pools only, else nullptr
+    float** v_scales;
+    int* d_err;          // device error bits (the library's only allocation)
+};
+
+namespace kvp {
+
+inline int elem_bytes(kv_dtype t) { return t == KV_F32 ? 4 : (t == KV_F16 ? 2 : 1); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- launchers
+int launch_append(const kv_pool* pool, int layer, const void* k, const void* v, kv_dtype in_dtype,
+                  const int64_t* slot_mapping, int num_tokens, cudaStream_t stream);
+int launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int num_pairs, int layer_begin,
+                       int layer_end, cudaStream_t stream);
+
+struct AttnPlan {
+    int partition;       // tokens per split-context partition
+    int max_parts;       // ceil(max_context / partition)
+    int consumers;       // consumer warps per CTA
+    size_t ws_bytes;     // workspace bytes
+};
+int plan_attention(const kv_pool* pool, int batch, int max_context, int partition_tokens,
+                   AttnPlan* plan);
+int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,
+                     const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                     int batch, int max_context, float scale, const AttnPlan& plan,
+                     void* workspace, cudaStream_t stream);
+
+// ---------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for completion of the phase with the given parity, for at most ~1 s.
+// On time-out: set KV_DEVERR_TIMEOUT in *err and return false (no trap, no hang).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err) {
+    #pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    #pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, KV_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// 1-D bulk copy global -> shared (the issuing CTA's own shared memory), completion
+// counted in bytes on the mbarrier.  dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Two E4M3 bytes (low byte = first element) -> two floats, exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    __half2 h = *reinterpret_cast<__half2*>(&h2);
+    return __half22float2(h);
+}
+
+// Two floats -> two E4M3 bytes (low byte = a), round to nearest even, saturating.
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace kvp

@@ -1,0 +1,173 @@
+"""C-ABI library: builds, loads, exports every declared symbol; host-only entry points
+(the block allocator, argument validation) checked on the CPU.
+
+The allocator is compared with the oracle's block manager on the same inputs (same
+initial free list, same operation sequence): block ids, slots, copy pairs, reference
+counts and free lists must be identical (integer work: bit-exact).
+"""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import cache as OC
+from paged_kv_cache_169_gb300 import abi, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kvpaged.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return abi.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    return re.findall(r"^KV_API\s+[\w\s\*]+?\b(\w+)\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(abi._SIGS), "binding and header must list the same entry points"
+
+
+def test_status_strings(lib):
+    assert abi.kv_status_str(0) == "ok"
+    assert abi.kv_status_str(abi.KV_ERR_NO_BLOCKS) == "no free blocks"
+    assert abi.kv_status_str(12345) == "unknown status"
+    assert abi.kv_version() >= 100
+
+
+def test_pool_create_rejects_bad_descriptors_without_a_gpu(lib):
+    bad = [dict(head_dim=96), dict(block_size=12), dict(num_heads=0), dict(num_layers=0),
+           dict(num_blocks=0), dict(dtype=7)]
+    base = dict(num_layers=1, num_blocks=4, block_size=16, num_heads=2, head_dim=64, dtype=abi.KV_F16)
+    for b in bad:
+        d = {**base, **b}
+        with pytest.raises(abi.KvError) as e:
+            abi.kv_pool_create(d["num_layers"], d["num_blocks"], d["block_size"], d["num_heads"],
+                               d["head_dim"], d["dtype"], [256] * max(d["num_layers"], 1),
+                               [256] * max(d["num_layers"], 1))
+        assert e.value.status == abi.KV_ERR_INVALID_ARG
+    # misaligned pointer, and FP8 without scales, are refused before any device call
+    with pytest.raises(abi.KvError):
+        abi.kv_pool_create(1, 4, 16, 2, 64, abi.KV_F16, [258], [256])
+    with pytest.raises(abi.KvError):
+        abi.kv_pool_create(1, 4, 16, 2, 64, abi.KV_FP8_E4M3, [256], [256])
+    with pytest.raises(abi.KvError):
+        abi.kv_pool_create(1, 4, 16, 2, 64, abi.KV_F16, [256], [256], [512], [512])
+
+
+def _run_both(num_blocks, B, order, ops):
+    """Apply the same operations to the C allocator and the oracle model."""
+    a = abi.kv_alloc_create(num_blocks, B, order)
+    m = OC.BlockManager(num_blocks, B, free_order=order)
+    ids = {}
+    try:
+        for op in ops:
+            kind = op[0]
+            if kind == "new":
+                ids[op[1]] = (abi.kv_alloc_seq_new(a), m.new_seq())
+            elif kind == "fork":
+                ids[op[2]] = (abi.kv_alloc_seq_fork(a, ids[op[1]][0]), m.fork(ids[op[1]][1]))
+            elif kind == "append":
+                ca, cm = ids[op[1]]
+                try:
+                    slots_m, cows_m = m.append_slots(cm, op[2])
+                    ok_m = True
+                except OC.OutOfBlocks:
+                    ok_m = False
+                try:
+                    slots_a, cow_a = abi.kv_alloc_append_slots(a, ca, op[2])
+                    ok_a = True
+                except abi.KvError as e:
+                    assert e.status == abi.KV_ERR_NO_BLOCKS
+                    ok_a = False
+                assert ok_a == ok_m
+                if ok_a:
+                    assert slots_a == slots_m
+                    assert ([cow_a] if cow_a else []) == [tuple(c) for c in cows_m]
+            elif kind == "free":
+                ca, cm = ids.pop(op[1])
+                abi.kv_alloc_seq_free(a, ca)
+                m.free_seq(cm)
+            # state comparison after every operation
+            assert abi.kv_alloc_free_list(a, num_blocks) == m.free
+            assert [abi.kv_alloc_ref_count(a, b) for b in range(num_blocks)] == m.ref
+            for name, (ca, cm) in ids.items():
+                assert abi.kv_alloc_block_table(a, ca) == m.table(cm)
+                assert abi.kv_alloc_seq_info(a, ca) == (m.lens[cm], len(m.table(cm)))
+        st = abi.kv_alloc_stats(a)
+        assert st.free_blocks == len(m.free) and st.shared_blocks == m.shared_blocks()
+        assert st.num_seqs == len(ids)
+        assert st.used_slots == sum(m.lens[cm] for _, cm in ids.values())
+        assert st.wasted_slots == sum(len(m.table(cm)) * B - m.lens[cm] for _, cm in ids.values())
+    finally:
+        abi.kv_alloc_destroy(a)
+
+
+def test_allocator_matches_oracle_parallel_sampling(lib):
+    ops = [("new", "p"), ("append", "p", 1030)]
+    ops += [("fork", "p", f"c{i}") for i in range(1, 8)]
+    names = ["p"] + [f"c{i}" for i in range(1, 8)]
+    for _ in range(128):
+        ops += [("append", n, 1) for n in names]
+    ops += [("free", n) for n in names]
+    _run_both(200, 16, np.random.default_rng(4).permutation(200).tolist(), ops)
+
+
+def test_allocator_matches_oracle_random_ops(lib):
+    rng = np.random.default_rng(11)
+    for B in (8, 16, 32):
+        nb = 120
+        ops, live, k = [("new", 0)], [0], 1
+        for _ in range(400):
+            r = rng.integers(10)
+            if r < 6:
+                ops.append(("append", live[int(rng.integers(len(live)))], int(rng.integers(1, 40))))
+            elif r < 7:
+                ops.append(("fork", live[int(rng.integers(len(live)))], k))
+                live.append(k)
+                k += 1
+            elif r < 8 and len(live) > 1:
+                ops.append(("free", live.pop(int(rng.integers(len(live))))))
+            else:
+                ops.append(("new", k))
+                live.append(k)
+                k += 1
+        _run_both(nb, B, rng.permutation(nb).tolist(), ops)
+
+
+def test_allocator_errors(lib):
+    a = abi.kv_alloc_create(4, 8)
+    try:
+        s = abi.kv_alloc_seq_new(a)
+        abi.kv_alloc_append_slots(a, s, 32)
+        with pytest.raises(abi.KvError) as e:
+            abi.kv_alloc_append_slots(a, s, 1)
+        assert e.value.status == abi.KV_ERR_NO_BLOCKS
+        assert abi.kv_alloc_seq_info(a, s) == (32, 4)        # unchanged
+        with pytest.raises(abi.KvError) as e:
+            abi.kv_alloc_seq_free(a, 999)
+        assert e.value.status == abi.KV_ERR_STATE
+        with pytest.raises(abi.KvError):
+            abi.kv_alloc_append_slots(a, s, 0)
+        with pytest.raises(abi.KvError):
+            abi.kv_alloc_build_tables(a, [s], 3)              # table longer than max_blocks
+        tabs, lens = abi.kv_alloc_build_tables(a, [s], 6)
+        assert lens == [32] and tabs[0][4:] == [-1, -1]
+        abi.kv_alloc_seq_free(a, s)
+        assert sorted(abi.kv_alloc_free_list(a, 4)) == [0, 1, 2, 3]
+        with pytest.raises(abi.KvError) as e:
+            abi.kv_alloc_seq_free(a, s)                       # double free
+        assert e.value.status == abi.KV_ERR_STATE
+    finally:
+        abi.kv_alloc_destroy(a)
+    with pytest.raises(abi.KvError):
+        abi.kv_alloc_create(4, 8, [0, 1, 1, 2])               # not a permutation

@@ -78,3 +78,16 @@ def test_quantize_divides_in_float32_then_rounds():
         ok = np.abs(xf) / float(scale) <= 448
         assert np.all(np.abs(deq[ok] - xf[ok]) <= np.maximum(np.abs(xf[ok]) * 2.0 ** -4,
                                                               float(scale) * 2.0 ** -10) * (1 + 1e-6))
+
+
+def test_vectorised_encode_equals_scalar_definition():
+    rng = np.random.default_rng(10)
+    finite = fp8.DECODE_TABLE[np.isfinite(fp8.DECODE_TABLE)]
+    mags = np.sort(np.unique(np.abs(finite)))
+    mids = (mags[:-1] + mags[1:]) / 2
+    xs = np.concatenate([finite, mids, -mids, mids * (1 + 1e-12), mids * (1 - 1e-12),
+                         rng.standard_normal(20000) * 60, rng.uniform(-3e-3, 3e-3, 5000),
+                         [448.0, 464.0, -464.0, 470.0, 1e9, -1e9, 0.0, -0.0, np.inf, -np.inf, np.nan]])
+    vec = fp8.encode(xs)
+    ref = np.array([fp8.encode_scalar(float(v)) for v in xs], dtype=np.uint8)
+    assert np.array_equal(vec, ref)
