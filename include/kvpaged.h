@@ -181,6 +181,33 @@ KV_API int paged_decode_attention(kv_pool* pool, int layer, const void* q, float
                            float scale, int partition_tokens, void* workspace,
                            size_t workspace_bytes, kv_stream_t stream);
 
+/* Size of the library's fixed device scratch array used by paged_decode_attention_static. */
+#define KV_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* paged_decode_attention without a workspace argument and without any allocation: for
+ * callers that cannot call cudaMalloc (a plugin whose host application owns all device
+ * memory and gives it no allocator; a serving loop that forbids device allocation once
+ * it runs, since cudaMalloc can synchronise the device or fail late).  The pages have no
+ * counterpart of this entry point: it only changes where the scratch memory comes from.
+ * Arguments and results are those of paged_decode_attention, minus workspace and
+ * workspace_bytes.  The scratch (work counters and split-context partials) is a
+ * file-scope device array of KV_STATIC_SCRATCH_BYTES that every GPU loading the library
+ * holds until the process exits.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - The pool's device must be the current device (else KV_ERR_INVALID_ARG).
+ *   - If the scratch these arguments need (paged_decode_workspace_size) exceeds
+ *     KV_STATIC_SCRATCH_BYTES the call is refused with KV_ERR_INVALID_ARG and nothing
+ *     is launched; a larger partition_tokens needs less scratch.
+ *   - All calls share the array and it keeps the last call's contents; the counters
+ *     that must start at zero are cleared by every call.  Calls whose kernels overlap on
+ *     the GPU (other streams, other host threads) race on it: serialise them.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine. */
+KV_API int paged_decode_attention_static(kv_pool* pool, int layer, const void* q, float* out,
+                                         const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* context_lens, int batch, int max_context,
+                                         float scale, int partition_tokens, kv_stream_t stream);
+
 /* ---------------------------------------------------------------- host block allocator */
 /* Host memory only; not thread-safe (the caller serialises).  Block ids are the
  * physical ids of a kv_pool of the same num_blocks and block_size.

@@ -48,6 +48,8 @@ _SIGS = {
     "paged_decode_workspace_size": (C.c_size_t, [_VP, C.c_int, C.c_int, C.c_int]),
     "paged_decode_attention": (C.c_int, [_VP, C.c_int, _VP, _VP, _VP, C.c_int, _VP, C.c_int,
                                          C.c_int, C.c_float, C.c_int, _VP, C.c_size_t, _VP]),
+    "paged_decode_attention_static": (C.c_int, [_VP, C.c_int, _VP, _VP, _VP, C.c_int, _VP, C.c_int,
+                                                C.c_int, C.c_float, C.c_int, _VP]),
     "kv_alloc_create": (C.c_int, [C.c_int, C.c_int, _I32P, C.POINTER(_VP)]),
     "kv_alloc_destroy": (C.c_int, [_VP]),
     "kv_alloc_seq_new": (C.c_int, [_VP, C.POINTER(C.c_int)]),
@@ -167,6 +169,22 @@ def paged_decode_attention(pool: int, layer: int, q: int, out: int, block_tables
     _check("paged_decode_attention", load().paged_decode_attention(
         pool, layer, q, out, block_tables, max_blocks_per_seq, context_lens, batch, max_context,
         scale, partition_tokens, workspace, workspace_bytes, stream))
+
+
+KV_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_decode_attention_static(pool: int, layer: int, q: int, out: int, block_tables: int,
+                                  max_blocks_per_seq: int, context_lens: int, batch: int,
+                                  max_context: int, scale: float, partition_tokens: int,
+                                  stream: int = 0) -> None:
+    """paged_decode_attention with the library's fixed device scratch instead of a caller
+    workspace: for callers that cannot allocate device memory.  The first call on a device
+    looks up the scratch address (make it before any stream capture); calls that overlap
+    on the GPU race on the shared scratch."""
+    _check("paged_decode_attention_static", load().paged_decode_attention_static(
+        pool, layer, q, out, block_tables, max_blocks_per_seq, context_lens, batch, max_context,
+        scale, partition_tokens, stream))
 
 
 # ---------------------------------------------------------------- allocator
