@@ -47,6 +47,12 @@ def make_workload(name: str):
     return w
 
 
+def apply_overrides(w, args):
+    if args.layers:
+        w.num_layers = args.layers
+    return w
+
+
 def algorithmic_bytes(w) -> int:
     """Bytes one paged_decode_attention call must move at minimum (one layer):
     K+V of every cached token, q, out (fp32), the used block-table entries, context_lens,
@@ -146,11 +152,13 @@ def _oracle_worker(args):
     import numpy as np
     from oracle import attention as OA
     rng = np.random.default_rng(seed)
-    data = [(rng.standard_normal(d).astype(np.float16),
+    distinct = min(units, 32)                  # bounded host memory; each unit still widens
+    data = [(rng.standard_normal(d).astype(np.float16),        # its own fp16 inputs to float64
              rng.standard_normal((n, d), dtype=np.float32).astype(np.float16),
-             rng.standard_normal((n, d), dtype=np.float32).astype(np.float16)) for _ in range(units)]
+             rng.standard_normal((n, d), dtype=np.float32).astype(np.float16)) for _ in range(distinct)]
     t0 = time.perf_counter()
-    for q, K, V in data:
+    for i in range(units):
+        q, K, V = data[i % distinct]
         OA.decode_attention_one(q, K, V, 1.0 / math.sqrt(d))
     return time.perf_counter() - t0
 
@@ -257,7 +265,7 @@ def run_ours(args):
     B.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = make_workload(args.workload)
+    w = apply_overrides(make_workload(args.workload), args)
     L, H, d, BS = w.num_layers, w.num_heads, w.head_dim, w.block_size
     nbs = [-(-n // BS) for n in w.lens]
     w.num_blocks = max(w.num_blocks, sum(nbs))
@@ -422,7 +430,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama13b")
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library choice)")
-    ap.add_argument("--cpu-units", type=int, default=3840, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a smaller case)")
+    ap.add_argument("--cpu-units", type=int, default=38400, help="oracle sample size for cpu_baseline")
     ap.add_argument("--ref-units", type=int, default=768, help="oracle units per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

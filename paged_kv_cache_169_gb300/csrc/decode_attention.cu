@@ -11,19 +11,23 @@
 // * Work items are (sequence, head, partition) triples; a partition is P tokens
 //   (split-context, flash-decoding style).  Items are handed out dynamically with one
 //   atomic counter, so ragged batches balance.
-// * Each CTA is persistent (one per SM): warp NC is a producer, warps 0..NC-1 are
-//   consumers.  The producer streams each item as chunks of CT = 32 tokens: for every
-//   physical block in the chunk it issues one 1-D bulk copy (cp.async.bulk, the TMA
-//   engine) of the contiguous (block, head) K tile and one of the V tile into the
-//   consumer's shared-memory ring, completing on an mbarrier.  The block-table entries
-//   of an item are loaded one item ahead by the 32 producer lanes.
-// * A consumer owns NSW ring stages.  Per chunk: each lane holds head_dim/32 dims of q;
-//   32 partial dot products are transpose-reduced across the warp so that lane t ends
-//   with token t's score; fp32 online softmax (log2 domain) with a running max; the
-//   V tile is accumulated in fp32 with p_t broadcast by shuffle.  ("KV Cache篇" §6.3:
-//   tiles in on-chip SRAM, softmax kept in on-chip state.)
+// * Each CTA is persistent (one per SM): warps 0..NC-1 are consumers, warp NC is the
+//   producer.  Producer lane w serves consumer w: it polls that consumer's ring without
+//   blocking, and for every physical block of the next CT-token chunk issues one 1-D
+//   bulk copy (cp.async.bulk, the TMA engine) of the contiguous (block, head) K tile
+//   and one of the V tile into the ring stage, completing on the stage's mbarrier.
+//   Block-table entries are fetched one chunk ahead, work items one item ahead.
+// * A consumer warp owns NSW ring stages.  Its two half-warps read two token rows per
+//   16-byte shared-memory load (lane: head_dim/16 dims of one row).  Each lane forms
+//   partial dot products for its CT/2 tokens; a transpose-reduce over the 16 lanes of
+//   a half leaves one token's score per lane.  Softmax runs in fp32 in the log2
+//   domain with a running maximum that is only raised (and the state rescaled) when
+//   some score exceeds it by more than 8; V is accumulated in fp32 with p_t broadcast
+//   by shuffle, and the two halves are summed once per item.  ("KV Cache篇" §6.3:
+//   tiles in on-chip SRAM, softmax state kept on chip.)
 // * A sequence that fits one partition is normalised and written directly; longer
-//   ones write (m, l, o) partials merged by reduce_kernel (exact log-sum-exp merge).
+//   ones write (m, l, o) partials merged by attention_reduce_kernel (exact
+//   log-sum-exp merge).
 //
 // No tensor cores: one query row per head is a matrix-vector product bound by HBM.
 
@@ -34,19 +38,37 @@
 namespace kvp {
 namespace {
 
-constexpr int CT = 32;             // tokens per chunk: lane t <-> token t after the reduce
 constexpr int kMaxBatch = 1024;    // sequences per launch (prefix table in shared memory)
 constexpr int kMaxSub = 64;        // launches per call -> batch <= 65536
+constexpr int kPartAlign = 32;     // partition sizes are multiples of this
 constexpr unsigned FULL = 0xffffffffu;
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_TERM = 4, F_SINGLE = 8 };
 
 struct __align__(16) Meta {
     int s, h, p, ntok;      // item (sequence, head, partition); valid tokens in the chunk
-    int flags, scidx, pad0, pad1;   // scidx: 2 bits per block = (id & 3) for FP8 scales
+    int flags, pad0, pad1, pad2;
+    int ids[4];             // physical block of each copy in the chunk (FP8: scale lookup)
 };
 
 constexpr int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+// Launch shape per storage type: tokens per chunk (CT), consumer warps (NC), ring stages
+// per consumer (NSW).  Compile-time overrides exist only for tuning sweeps
+// (KVP_F16_CT/NC/NSW, KVP_FP8_CT/NC/NSW).
+template <int ESZ> struct Tune { static constexpr int CT = 32, NC = 0, NSW = 0; };   // 0: by stage size
+#if !defined(KVP_F16_CT)
+template <> struct Tune<2> { static constexpr int CT = 16, NC = 12, NSW = 0; };
+#endif
+#if !defined(KVP_FP8_CT)
+template <> struct Tune<1> { static constexpr int CT = 32, NC = 12, NSW = 0; };
+#endif
+#if defined(KVP_F16_CT) && defined(KVP_F16_NC) && defined(KVP_F16_NSW)
+template <> struct Tune<2> { static constexpr int CT = KVP_F16_CT, NC = KVP_F16_NC, NSW = KVP_F16_NSW; };
+#endif
+#if defined(KVP_FP8_CT) && defined(KVP_FP8_NC) && defined(KVP_FP8_NSW)
+template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_NC, NSW = KVP_FP8_NSW; };
+#endif
 
 template <int D_, typename KV_, typename QT_>
 struct Cfg {
@@ -54,26 +76,33 @@ struct Cfg {
     using KV = KV_;
     using QT = QT_;
     static constexpr int ESZ = sizeof(KV);
-    static constexpr int DPL = D / 32;                    // dims per lane
     static constexpr bool FP8 = (ESZ == 1);
+    static constexpr int CT = Tune<ESZ>::CT;
+    static constexpr int TPL = CT / 2;                    // tokens per lane per chunk
+    static constexpr int DPL = D / 16;                    // dims per lane
+    static constexpr int CBMAX = CT / 8;                  // blocks per chunk at B = 8
     static constexpr int ROW = D * ESZ;                   // bytes of one token row of one head
     static constexpr int KV_BYTES = CT * ROW;             // bytes of K (or V) per chunk
     static constexpr int Q_BYTES = D * sizeof(QT);
-    static constexpr int SC_BYTES = FP8 ? 2 * 4 * 16 : 0; // <= 4 blocks per chunk, K and V
+    static constexpr int SC_BYTES = 0;
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = KV_BYTES;
     static constexpr int Q_OFF = 2 * KV_BYTES;
     static constexpr int SC_OFF = Q_OFF + Q_BYTES;
     static constexpr int META_OFF = SC_OFF + SC_BYTES;
     static constexpr int STAGE = round_up(META_OFF + (int)sizeof(Meta), 128);
-    static constexpr int NC = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
-    static constexpr int NSW = STAGE <= 17 * 1024 ? 3 : 2;
+    static constexpr int NC = Tune<ESZ>::NC ? Tune<ESZ>::NC
+                                            : (STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3));
+    // stages that fit beside the prefix table and the barriers
+    static constexpr int NSW_FIT = (227 * 1024 - 2 * kMaxBatch * 4 - 1024) / (NC * STAGE);
+    static constexpr int NSW = Tune<ESZ>::NSW ? Tune<ESZ>::NSW : (NSW_FIT > 4 ? 4 : NSW_FIT);
+    static_assert(NSW >= 2, "at least double buffering");
     static constexpr int THREADS = (NC + 1) * 32;
     static constexpr int BAR_OFF = NC * NSW * STAGE;
     static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
-    static constexpr int PSTATE_OFF = PREFIX_OFF + 2 * kMaxBatch * 4;
-    static constexpr int SMEM = PSTATE_OFF + 2 * NC * 32;
+    static constexpr int SMEM = PREFIX_OFF + 2 * kMaxBatch * 4;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(NC <= 32 && (CT == 16 || CT == 32), "launch shape");
     static_assert(Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && META_OFF % 16 == 0, "alignment");
 };
 
@@ -107,59 +136,82 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// lane's DPL elements of one row -> floats
+// d = a * b + c on two fp32 lanes at once (packed FFMA2, sm_100 family)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// The lane's DPL consecutive elements of one token row, as DPL/2 float pairs.
 template <typename C>
-__device__ __forceinline__ void load_row(const char* row, int lane, float (&x)[C::DPL]) {
-    using KV = typename C::KV;
-    const char* p = row + lane * C::DPL * C::ESZ;
+__device__ __forceinline__ void load_row(const char* row, int sub, float2 (&x)[C::DPL / 2]) {
+    const char* p = row + sub * C::DPL * C::ESZ;
     if constexpr (C::ESZ == 4) {
-        if constexpr (C::DPL == 4) {
-            float4 v = *reinterpret_cast<const float4*>(p);
-            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-        } else {
-            float2 v = *reinterpret_cast<const float2*>(p);
-            x[0] = v.x; x[1] = v.y;
+        #pragma unroll
+        for (int i = 0; i < C::DPL / 4; ++i) {
+            const float4 v = reinterpret_cast<const float4*>(p)[i];
+            x[2 * i] = make_float2(v.x, v.y);
+            x[2 * i + 1] = make_float2(v.z, v.w);
         }
     } else if constexpr (C::ESZ == 2) {
-        if constexpr (C::DPL == 4) {
-            uint2 v = *reinterpret_cast<const uint2*>(p);
-            float2 a = __half22float2(*reinterpret_cast<__half2*>(&v.x));
-            float2 b = __half22float2(*reinterpret_cast<__half2*>(&v.y));
-            x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+        if constexpr (C::DPL == 8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p);
+            x[0] = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+            x[1] = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+            x[2] = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
+            x[3] = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
         } else {
-            uint32_t v = *reinterpret_cast<const uint32_t*>(p);
-            float2 a = __half22float2(*reinterpret_cast<__half2*>(&v));
-            x[0] = a.x; x[1] = a.y;
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            x[0] = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+            x[1] = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
         }
     } else {
-        if constexpr (C::DPL == 4) {
-            uint32_t v = *reinterpret_cast<const uint32_t*>(p);
-            float2 a = e4m3x2_to_float2(static_cast<uint16_t>(v & 0xffffu));
-            float2 b = e4m3x2_to_float2(static_cast<uint16_t>(v >> 16));
-            x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+        if constexpr (C::DPL == 8) {
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            x[0] = e4m3x2_to_float2(static_cast<uint16_t>(v.x & 0xffffu));
+            x[1] = e4m3x2_to_float2(static_cast<uint16_t>(v.x >> 16));
+            x[2] = e4m3x2_to_float2(static_cast<uint16_t>(v.y & 0xffffu));
+            x[3] = e4m3x2_to_float2(static_cast<uint16_t>(v.y >> 16));
         } else {
-            uint16_t v = *reinterpret_cast<const uint16_t*>(p);
-            float2 a = e4m3x2_to_float2(v);
-            x[0] = a.x; x[1] = a.y;
+            const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+            x[0] = e4m3x2_to_float2(static_cast<uint16_t>(v & 0xffffu));
+            x[1] = e4m3x2_to_float2(static_cast<uint16_t>(v >> 16));
         }
     }
-    (void)sizeof(KV);
 }
 
 template <typename C>
-__device__ __forceinline__ void load_q(const char* qrow, int lane, float qs, float (&x)[C::DPL]) {
+__device__ __forceinline__ void load_q(const char* qrow, int sub, float qs, float2 (&x)[C::DPL / 2]) {
     using QT = typename C::QT;
-    const QT* p = reinterpret_cast<const QT*>(qrow) + lane * C::DPL;
+    const QT* p = reinterpret_cast<const QT*>(qrow) + sub * C::DPL;
     #pragma unroll
-    for (int i = 0; i < C::DPL; ++i) x[i] = static_cast<float>(p[i]) * qs;
+    for (int i = 0; i < C::DPL / 2; ++i)
+        x[i] = make_float2(static_cast<float>(p[2 * i]) * qs, static_cast<float>(p[2 * i + 1]) * qs);
 }
 
-// Item decode shared by the producer: (s, h, p) of compact item index `it`.
 struct __align__(16) Item {
     int s, h, p, tok0, ntok, nchunks, single, valid;
 };
-static_assert(sizeof(Item) == 32, "producer state slot");
 
+// (s, h, p) of compact item index `it` (items ordered by sequence, head, partition).
+template <int CT>
 __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ctx, const int* s_end,
                                             int batch, int H, int P) {
     Item r{};
@@ -187,7 +239,8 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
 
 template <typename C>
 __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(AttnArgs a) {
-    constexpr int NC = C::NC, NSW = C::NSW, D = C::D;
+    constexpr int NC = C::NC, NSW = C::NSW, D = C::D, CT = C::CT, TPL = C::TPL, DPL = C::DPL;
+    constexpr int CBMAX = C::CBMAX;
     extern __shared__ __align__(128) char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);   // full[NC*NSW], empty[NC*NSW]
     int* s_ctx = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
@@ -232,126 +285,116 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
 
     if (warp == NC) {
         // ================================================================ producer
-        // Per consumer stream: the item being streamed (cur) and the next one (nxt),
-        // kept in shared memory (warp-uniform values); each lane keeps the physical id
-        // of item block `lane` for cur and nxt in registers.
-        Item* cur = reinterpret_cast<Item*>(smem + C::PSTATE_OFF);
-        Item* nxt = cur + NC;
-        unsigned pending = 0;                          // lane 0: next item index (in flight)
-        if (lane == 0) pending = atomicAdd(a.counter, 1u);
-        int cur_id[NC], nxt_id[NC], chunk[NC], fills[NC];
-
-        auto acquire = [&](Item* slot) -> int {
-            const int idx = static_cast<int>(__shfl_sync(FULL, pending, 0));
-            if (lane == 0) pending = atomicAdd(a.counter, 1u);
-            const Item it = decode_item(idx, n_items, s_ctx, s_end, a.batch, a.H, a.P);
-            int id = 0;
-            if (it.valid) {
-                const int nblk = (it.ntok + a.B - 1) / a.B;
-                if (lane < nblk)
-                    id = a.tables[static_cast<int64_t>(it.s) * a.max_blocks + it.tok0 / a.B + lane];
-            }
-            if (lane == 0) *slot = it;
-            __syncwarp();
-            return id;
+        // Lane w feeds consumer w; lanes >= NC only take part in warp votes.
+        const bool mine = lane < NC;
+        const int w = mine ? lane : 0;
+        const int rpc = a.B < CT ? a.B : CT;           // token rows per copy (whole block if B <= CT)
+        const uint32_t tile = static_cast<uint32_t>(rpc) * C::ROW;
+        unsigned pending = 0;                          // next item index (atomic in flight)
+        if (mine) pending = atomicAdd(a.counter, 1u);
+        auto take = [&]() {
+            const int idx = static_cast<int>(pending);
+            pending = atomicAdd(a.counter, 1u);
+            return decode_item<CT>(idx, n_items, s_ctx, s_end, a.batch, a.H, a.P);
         };
-
-        #pragma unroll
-        for (int w = 0; w < NC; ++w) {
-            cur_id[w] = acquire(&cur[w]);
-            nxt_id[w] = acquire(&nxt[w]);
-            chunk[w] = 0;
-            fills[w] = 0;
-        }
-        unsigned alive = (1u << NC) - 1u;
-        bool failed = false;
-        const int CB = CT / a.B;                        // blocks per full chunk
-        const uint32_t tile = static_cast<uint32_t>(a.B) * C::ROW;
-        while (alive && !failed) {
+        int ids[CBMAX];
+        auto load_ids = [&](const Item& it, int chunk) {
+            const int nt = it.valid ? min(CT, it.ntok - chunk * CT) : 0;
+            const int ncp = nt > 0 ? (nt + rpc - 1) / rpc : 0;
+            const int64_t row = static_cast<int64_t>(it.s) * a.max_blocks;
+            const int t0 = it.tok0 + chunk * CT;
             #pragma unroll
-            for (int w = 0; w < NC; ++w) {
-                if (!(alive & (1u << w)) || failed) continue;
-                const int st = fills[w] % NSW;
-                const uint32_t par = ((fills[w] / NSW) & 1) ^ 1;
-                if (!mbar_wait_bounded(empty_bar(w, st), par, a.err)) { failed = true; continue; }
+            for (int j = 0; j < CBMAX; ++j) ids[j] = j < ncp ? a.tables[row + (t0 + j * rpc) / a.B] : 0;
+        };
+        Item cur{}, nxt{};
+        int c = 0, fills = 0;
+        bool alive = mine;
+        if (mine) {
+            cur = take();
+            if (cur.valid) nxt = take();
+            load_ids(cur, 0);
+        }
+        bool failed = false;
+        uint64_t idle_since = 0;
+        while (__any_sync(FULL, alive) && !failed) {
+            const int st = fills % NSW;
+            bool ready = false;
+            if (alive) ready = mbar_test_wait(empty_bar(w, st), ((fills / NSW) & 1) ^ 1);
+            if (ready) {
                 char* stg = stage_ptr(w, st);
                 Meta* meta = reinterpret_cast<Meta*>(stg + C::META_OFF);
                 const uint32_t fb = full_bar(w, st);
-                const Item it = cur[w];
-                if (!it.valid) {
-                    if (lane == 0) {
-                        meta->flags = F_TERM;
-                        mbar_arrive(fb);
-                    }
-                    alive &= ~(1u << w);
+                if (!cur.valid) {
+                    meta->flags = F_TERM;
+                    mbar_arrive(fb);
+                    alive = false;
                 } else {
-                    const int c = chunk[w];
-                    const int nt = min(CT, it.ntok - c * CT);      // 0 only for an empty sequence
-                    const int nblk = nt > 0 ? (nt + a.B - 1) / a.B : 0;
-                    // block ids of this chunk: item block c*CB + j lives in producer lane c*CB + j
-                    int id = __shfl_sync(FULL, cur_id[w], (c * CB + lane) & 31);
-                    if (lane < nblk && (id < 0 || id >= a.num_blocks)) {
-                        atomicOr(a.err, KV_DEVERR_BLOCK_ID);
-                        id = 0;
-                    }
-                    int scidx = 0;
-                    if constexpr (C::FP8) {
-                        const int bits = lane < nblk ? ((id & 3) << (2 * lane)) : 0;
-                        scidx = __reduce_or_sync(FULL, bits);
+                    const int nt = min(CT, cur.ntok - c * CT);     // 0 only for an empty sequence
+                    const int nblk = nt > 0 ? (nt + rpc - 1) / rpc : 0;   // copies of this chunk
+                    const int row0 = (cur.tok0 + c * CT) % a.B;   // first row inside the block
+                    #pragma unroll
+                    for (int j = 0; j < CBMAX; ++j) {
+                        if (j < nblk && (ids[j] < 0 || ids[j] >= a.num_blocks)) {
+                            atomicOr(a.err, KV_DEVERR_BLOCK_ID);
+                            ids[j] = 0;
+                        }
                     }
                     const bool with_q = (c == 0) && nt > 0;
-                    const uint32_t bytes = nblk * (2 * tile + (C::FP8 ? 32u : 0u)) +
-                                           (with_q ? C::Q_BYTES : 0);
-                    if (lane == 0) {
-                        meta->s = it.s;
-                        meta->h = it.h;
-                        meta->p = it.p;
-                        meta->ntok = nt;
-                        meta->flags = (c == 0 ? F_FIRST : 0) | (c == it.nchunks - 1 ? F_LAST : 0) |
-                                      (it.single ? F_SINGLE : 0);
-                        meta->scidx = scidx;
-                        if (bytes) mbar_arrive_expect_tx(fb, bytes);
-                        else mbar_arrive(fb);
+                    const uint32_t bytes = nblk * 2 * tile + (with_q ? C::Q_BYTES : 0);
+                    meta->s = cur.s;
+                    meta->h = cur.h;
+                    meta->p = cur.p;
+                    meta->ntok = nt;
+                    meta->flags = (c == 0 ? F_FIRST : 0) | (c == cur.nchunks - 1 ? F_LAST : 0) |
+                                  (cur.single ? F_SINGLE : 0);
+                    if constexpr (C::FP8) {
+                        #pragma unroll
+                        for (int j = 0; j < CBMAX; ++j) meta->ids[j] = ids[j];
                     }
-                    __syncwarp();
-                    if (lane < nblk) {
-                        const int64_t toff = (static_cast<int64_t>(id) * a.H + it.h) * tile;
-                        const uint32_t dst = smem_u32(stg) + lane * tile;
-                        bulk_g2s(dst + C::K_OFF, a.kpool + toff, tile, fb);
-                        bulk_g2s(dst + C::V_OFF, a.vpool + toff, tile, fb);
-                        if constexpr (C::FP8) {
-                            const uint32_t sc = smem_u32(stg) + C::SC_OFF + lane * 16;
-                            bulk_g2s(sc, a.kscale + (id & ~3), 16, fb);
-                            bulk_g2s(sc + 64, a.vscale + (id & ~3), 16, fb);
+                    if (bytes) mbar_arrive_expect_tx(fb, bytes);
+                    else mbar_arrive(fb);
+                    const uint32_t dst = smem_u32(stg);
+                    #pragma unroll
+                    for (int j = 0; j < CBMAX; ++j) {
+                        if (j < nblk) {
+                            const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h) * a.B +
+                                                  row0) * C::ROW;
+                            bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
+                            bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
                         }
                     }
-                    if (with_q && lane == 0) {
+                    if (with_q) {
                         const char* qsrc = static_cast<const char*>(a.q) +
-                                           (static_cast<int64_t>(it.s) * a.H + it.h) * C::Q_BYTES;
-                        bulk_g2s(smem_u32(stg) + C::Q_OFF, qsrc, C::Q_BYTES, fb);
+                                           (static_cast<int64_t>(cur.s) * a.H + cur.h) * C::Q_BYTES;
+                        bulk_g2s(dst + C::Q_OFF, qsrc, C::Q_BYTES, fb);
                     }
-                    if (++chunk[w] == it.nchunks) {
-                        const Item n = nxt[w];
-                        __syncwarp();
-                        if (lane == 0) cur[w] = n;
-                        cur_id[w] = nxt_id[w];
-                        chunk[w] = 0;
-                        if (n.valid) {
-                            nxt_id[w] = acquire(&nxt[w]);
-                        } else {
-                            __syncwarp();
-                        }
+                    if (++c == cur.nchunks) {
+                        cur = nxt;
+                        c = 0;
+                        nxt = Item{};
+                        if (cur.valid) nxt = take();
                     }
+                    load_ids(cur, c);                  // used at this lane's next fill
                 }
-                ++fills[w];
-                __syncwarp();
+                ++fills;
+            }
+            // watchdog: no stage became free anywhere for about a second -> give up
+            if (__any_sync(FULL, ready)) {
+                idle_since = 0;
+            } else {
+                const uint64_t now = global_timer_ns();
+                if (idle_since == 0) idle_since = now;
+                else if (now - idle_since > kWaitLimitNs) {
+                    if (lane == 0) atomicOr(a.err, KV_DEVERR_TIMEOUT);
+                    failed = true;
+                }
+                __nanosleep(32);
             }
         }
-        // Drain: every fill this warp issued has landed before the CTA may exit.
-        #pragma unroll
-        for (int w = 0; w < NC; ++w) {
-            for (int st = 0; st < NSW && st < fills[w]; ++st) {
-                const int last = fills[w] - 1 - ((fills[w] - 1 - st) % NSW);
+        // Drain: every fill this lane issued has landed before the CTA may exit.
+        if (mine) {
+            for (int st = 0; st < NSW && st < fills; ++st) {
+                const int last = fills - 1 - ((fills - 1 - st) % NSW);
                 mbar_wait_bounded(full_bar(w, st), (last / NSW) & 1, a.err);
             }
         }
@@ -360,10 +403,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
 
     // ==================================================================== consumer
     const int w = warp;
-    float qf[C::DPL], acc[C::DPL];
+    const int half = lane >> 4;                 // which token of each row pair
+    const int sub = lane & 15;                  // which DPL-element slice of the row
+    const int tok_l = 2 * (lane & (TPL - 1)) + half;     // token whose score this lane holds
+    const bool primary = (lane & 15) < TPL;              // one holder per token when CT = 16
+    float2 q2[DPL / 2], acc[DPL / 2];
     float m = -CUDART_INF_F, lsum = 0.f;
     #pragma unroll
-    for (int i = 0; i < C::DPL; ++i) { qf[i] = 0.f; acc[i] = 0.f; }
+    for (int i = 0; i < DPL / 2; ++i) { q2[i] = make_float2(0.f, 0.f); acc[i] = make_float2(0.f, 0.f); }
 
     for (int j = 0;; ++j) {
         const int st = j % NSW;
@@ -374,32 +421,46 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
             break;
         }
         const char* stg = stage_ptr(w, st);
-        const Meta meta = *reinterpret_cast<const Meta*>(stg + C::META_OFF);
+        struct { int s, h, p, ntok, flags; } meta;
+        {
+            const int4 m0 = *reinterpret_cast<const int4*>(stg + C::META_OFF);
+            meta.s = m0.x; meta.h = m0.y; meta.p = m0.z; meta.ntok = m0.w;
+            meta.flags = reinterpret_cast<const Meta*>(stg + C::META_OFF)->flags;
+        }
         if (meta.flags & F_TERM) break;
         const int nt = meta.ntok;
         if (meta.flags & F_FIRST) {
             m = -CUDART_INF_F;
             lsum = 0.f;
             #pragma unroll
-            for (int i = 0; i < C::DPL; ++i) acc[i] = 0.f;
-            if (nt > 0) load_q<C>(stg + C::Q_OFF, lane, a.qscale, qf);
+            for (int i = 0; i < DPL / 2; ++i) acc[i] = make_float2(0.f, 0.f);
+            if (nt > 0) load_q<C>(stg + C::Q_OFF, sub, a.qscale, q2);
         }
         if (nt > 0) {
-            const char* K = stg + C::K_OFF;
-            const char* V = stg + C::V_OFF;
-            float part[CT];
-            #pragma unroll
-            for (int t = 0; t < CT; ++t) {
-                float kx[C::DPL];
-                load_row<C>(K + t * C::ROW, lane, kx);
-                float d = 0.f;
-                #pragma unroll
-                for (int i = 0; i < C::DPL; ++i) d = fmaf(qf[i], kx[i], d);
-                part[t] = d;
+            float ks = 1.f, vs = 1.f;
+            if constexpr (C::FP8) {
+                // per-block scales of this lane's token, loaded now and used after the dot
+                // products; the producer validated the ids
+                const int id = reinterpret_cast<const Meta*>(stg + C::META_OFF)
+                                   ->ids[tok_l / (a.B < CT ? a.B : CT)];
+                ks = __ldg(a.kscale + id);
+                vs = __ldg(a.vscale + id);
             }
-            // transpose-reduce: after the loop lane t holds the full dot product of token t
+            const char* K = stg + C::K_OFF + half * C::ROW;
+            const char* V = stg + C::V_OFF + half * C::ROW;
+            float part[TPL];
             #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
+            for (int i = 0; i < TPL; ++i) {          // token 2i + half
+                float2 kx[DPL / 2];
+                load_row<C>(K + 2 * i * C::ROW, sub, kx);
+                float2 d2 = make_float2(0.f, 0.f);
+                #pragma unroll
+                for (int u = 0; u < DPL / 2; ++u) d2 = ffma2(q2[u], kx[u], d2);
+                part[i] = d2.x + d2.y;
+            }
+            // transpose-reduce over the 16 lanes of each half: lane ends with token tok_l
+            #pragma unroll
+            for (int off = TPL / 2; off >= 1; off >>= 1) {
                 const bool upper = (lane & off) != 0;
                 #pragma unroll
                 for (int i = 0; i < off; ++i) {
@@ -409,64 +470,63 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
                 }
             }
             float x = part[0];
-            float vs = 1.f;
-            if constexpr (C::FP8) {
-                const int blk = lane / a.B;                 // block of token `lane` in the chunk
-                const int sub = (meta.scidx >> (2 * blk)) & 3;
-                const float* sc = reinterpret_cast<const float*>(stg + C::SC_OFF);
-                x *= sc[blk * 4 + sub];
-                vs = sc[16 + blk * 4 + sub];
-            }
-            x = lane < nt ? x : -CUDART_INF_F;
-            const float m_new = fmaxf(m, warp_max(x));
-            const float corr = ex2_approx(m - m_new);
-            const float pr = ex2_approx(x - m_new);
-            lsum = fmaf(lsum, corr, pr);
             #pragma unroll
-            for (int i = 0; i < C::DPL; ++i) acc[i] *= corr;
+            for (int off = TPL; off < 16; off <<= 1) x += __shfl_xor_sync(FULL, x, off);
+            if constexpr (C::FP8) x *= ks;
+            x = tok_l < nt ? x : -CUDART_INF_F;
+            if (__any_sync(FULL, x > m + 8.f)) {      // raise the running max only when needed
+                const float m_new = fmaxf(m, warp_max(x));
+                const float corr = ex2_approx(m - m_new);
+                lsum *= corr;
+                #pragma unroll
+                for (int i = 0; i < DPL / 2; ++i) { acc[i].x *= corr; acc[i].y *= corr; }
+                m = m_new;
+            }
+            const float pr = ex2_approx(x - m);
+            if (primary) lsum += pr;
             const float pv = pr * vs;
-            if (nt == CT) {
-                #pragma unroll
-                for (int t = 0; t < CT; ++t) {
-                    const float pt = __shfl_sync(FULL, pv, t);
-                    float vx[C::DPL];
-                    load_row<C>(V + t * C::ROW, lane, vx);
+            #pragma unroll
+            for (int i = 0; i < TPL; ++i) {          // token 2i + half, its p from lane i (+16)
+                const float pt = __shfl_sync(FULL, pv, i + (lane & 16));
+                if (nt == CT || 2 * i + half < nt) {
+                    float2 vx[DPL / 2];
+                    load_row<C>(V + 2 * i * C::ROW, sub, vx);
+                    const float2 p2 = make_float2(pt, pt);
                     #pragma unroll
-                    for (int i = 0; i < C::DPL; ++i) acc[i] = fmaf(pt, vx[i], acc[i]);
-                }
-            } else {
-                #pragma unroll
-                for (int t = 0; t < CT; ++t) {
-                    if (t < nt) {
-                        const float pt = __shfl_sync(FULL, pv, t);
-                        float vx[C::DPL];
-                        load_row<C>(V + t * C::ROW, lane, vx);
-                        #pragma unroll
-                        for (int i = 0; i < C::DPL; ++i) acc[i] = fmaf(pt, vx[i], acc[i]);
-                    }
+                    for (int u = 0; u < DPL / 2; ++u) acc[u] = ffma2(p2, vx[u], acc[u]);
                 }
             }
-            m = m_new;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(w, st));
         if (meta.flags & F_LAST) {
             const float l = warp_sum(lsum);
+            float2 o[DPL / 2];
+            #pragma unroll
+            for (int i = 0; i < DPL / 2; ++i) {       // the two halves saw different tokens
+                o[i].x = acc[i].x + __shfl_xor_sync(FULL, acc[i].x, 16);
+                o[i].y = acc[i].y + __shfl_xor_sync(FULL, acc[i].y, 16);
+            }
             const int64_t sh = static_cast<int64_t>(meta.s) * a.H + meta.h;
             if (meta.flags & F_SINGLE) {
-                float* o = a.out + sh * D + lane * C::DPL;
-                const float inv = nt > 0 ? 1.f / l : 0.f;   // empty sequence -> zeros
-                #pragma unroll
-                for (int i = 0; i < C::DPL; ++i) o[i] = nt > 0 ? acc[i] * inv : 0.f;
+                if (half == 0) {
+                    float2* dst = reinterpret_cast<float2*>(a.out + sh * D + sub * DPL);
+                    const float inv = nt > 0 ? 1.f / l : 0.f;   // empty sequence -> zeros
+                    #pragma unroll
+                    for (int i = 0; i < DPL / 2; ++i)
+                        dst[i] = nt > 0 ? make_float2(o[i].x * inv, o[i].y * inv) : make_float2(0.f, 0.f);
+                }
             } else {
                 const int64_t idx = sh * a.max_parts + meta.p;
                 if (lane == 0) {
                     a.part_ml[2 * idx] = m;
                     a.part_ml[2 * idx + 1] = l;
                 }
-                float* o = a.part_o + idx * D + lane * C::DPL;
-                #pragma unroll
-                for (int i = 0; i < C::DPL; ++i) o[i] = acc[i];
+                if (half == 0) {
+                    float2* dst = reinterpret_cast<float2*>(a.part_o + idx * D + sub * DPL);
+                    #pragma unroll
+                    for (int i = 0; i < DPL / 2; ++i) dst[i] = o[i];
+                }
             }
         }
     }
@@ -572,16 +632,16 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     const int nc = consumers_for(d);
     int P;
     if (partition_tokens > 0) {
-        if (partition_tokens % CT != 0 || partition_tokens > cap) return KV_ERR_INVALID_ARG;
+        if (partition_tokens % kPartAlign != 0 || partition_tokens > cap) return KV_ERR_INVALID_ARG;
         P = partition_tokens;
     } else if (partition_tokens == 0) {
         const int64_t units = static_cast<int64_t>(batch > 0 ? batch : 1) * d.num_heads;
-        const int64_t target = 4ll * pool->num_sms * nc;     // >= 4 items per consumer warp
+        const int64_t target = 8ll * pool->num_sms * nc;     // >= 8 items per consumer warp
         int64_t parts = (target + units - 1) / units;
         if (parts < 1) parts = 1;
         int64_t p = (max_context + parts - 1) / parts;
-        p = (p + CT - 1) / CT * CT;
-        if (p < CT) p = CT;
+        p = (p + kPartAlign - 1) / kPartAlign * kPartAlign;
+        if (p < kPartAlign) p = kPartAlign;
         if (p > cap) p = cap;
         P = static_cast<int>(p);
     } else {
