@@ -311,16 +311,21 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     from paged_kv_cache_169_gb300 import abi
-    plan_parts = ws.numel() > 256                                     # split-context partials in use
-    launches_per_layer = 2 + (1 if plan_parts else 0) + (w.batch - 1) // 1024
+    # my kernels per layer: the attention kernel (one per 1024 sequences) [+ kv_append]
+    launches_per_layer = (1 if args.unfused else 0) + 1 + (w.batch - 1) // 1024
 
     def step(ev=None):
         for l in range(L):
-            cache.append(l, k_new[l], v_new[l], slots)
+            if args.unfused:
+                cache.append(l, k_new[l], v_new[l], slots)
             if ev is not None:
                 ev[l][0].record(stream)
-            cache.attention(l, q[l], bt, cl, max_ctx, w.scale, out=out[l], partition_tokens=args.partition,
-                            workspace=ws)
+            if args.unfused:
+                cache.attention(l, q[l], bt, cl, max_ctx, w.scale, out=out[l],
+                                partition_tokens=args.partition, workspace=ws)
+            else:   # one launch: append each sequence's newest token, then attend
+                cache.attention_append(l, q[l], k_new[l], v_new[l], bt, cl, max_ctx, w.scale, out=out[l],
+                                       partition_tokens=args.partition, workspace=ws)
             if ev is not None:
                 ev[l][1].record(stream)
 
@@ -387,10 +392,14 @@ def run_ours(args):
     # ---- numbers
     alg = algorithmic_bytes(w)
     step_bytes = alg * L
+    # the timed call's own minimum traffic: the fused call also reads the new K/V and
+    # writes them into the pool
+    esz = 1 if w.kv == "fp8" else 2
+    call_bytes = alg if args.unfused else alg + w.batch * H * d * 2 * (2 + esz)
     ms_per_step = elapsed_ms / args.steps
     value = job_throughput(world, step_bytes, args.steps, elapsed_ms)
     peak, peak_src = measured_peak()
-    achieved = alg / (attn_ms_mean / 1e3) / 1e9
+    achieved = call_bytes / (attn_ms_mean / 1e3) / 1e9
     src = os.path.join(ROOT, "paged_kv_cache_169_gb300", "csrc", "decode_attention.cu")
     traffic = traffic_record(src) if args.workload == "llama13b" else None
     cpu = None
@@ -406,13 +415,17 @@ def run_ours(args):
                    "context_max": max_ctx, "pool_gib": round(2 * L * w.num_blocks * H * BS * d *
                                                              (1 if w.kv == "fp8" else 2) / 2 ** 30, 2),
                    "l2": "no flush: inputs (the KV pool) larger than L2",
-                   "partition_tokens": args.partition or "auto", "parallelism": f"replica x{world}"},
+                   "partition_tokens": args.partition or "auto", "parallelism": f"replica x{world}",
+                   "step": "kv_append + paged_decode_attention" if args.unfused
+                           else "paged_decode_attention_append (fused)"},
         "pct_of_peak": 100.0 * value / world / peak,
         "seq_steps_per_s": world * w.batch * args.steps / (elapsed_ms / 1e3),
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (partition + reduce)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("paged_decode_attention" if args.unfused
+                                else "paged_decode_attention_append (fused append + attention)"),
                      "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": alg, "mean_call_ms": attn_ms_mean},
+                     "algorithmic_bytes_per_launch": call_bytes, "mean_call_ms": attn_ms_mean},
         "cpu_baseline": cpu,
         "e2e": {"value": job_throughput(world, step_bytes, args.steps, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
@@ -441,6 +454,7 @@ def main():
     ap.add_argument("--cpu-units", type=int, default=38400, help="oracle sample size for cpu_baseline")
     ap.add_argument("--ref-units", type=int, default=768, help="oracle units per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true", help="time kv_append + paged_decode_attention as two calls")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

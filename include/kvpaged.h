@@ -181,6 +181,27 @@ KV_API int paged_decode_attention(kv_pool* pool, int layer, const void* q, float
                            float scale, int partition_tokens, void* workspace,
                            size_t workspace_bytes, kv_stream_t stream);
 
+/* One decode step of a layer in one launch: append each sequence's newest token, then
+ * attend (the fused append + attention of the decode loop).  For every sequence s with
+ * n = context_lens[s] >= 1, token n-1 is the token produced this step: its K and V
+ * (k_new, v_new: device [batch][num_heads][head_dim] of in_dtype, 16-byte aligned; dtype
+ * rules as kv_append) are stored into the slot block_tables[s][(n-1)/B]*B + (n-1)%B of
+ * every head, and out is what paged_decode_attention returns over the updated cache.
+ * The pool bytes written and the output are identical to kv_append followed by
+ * paged_decode_attention.  Requirement: the block receiving a sequence's new token must
+ * not be shared with another sequence of the batch (copy-on-write already done, as the
+ * host allocator guarantees); a sequence with context_len 0 appends nothing.  All other
+ * arguments, the workspace and the errors are those of paged_decode_attention.
+ * The write-then-read order of [KV Cache篇] §3.1 and the batched cache update of
+ * [KV缓存机制解析] §6.2, done inside the attention kernel by the warp that owns the
+ * sequence's last chunk. */
+KV_API int paged_decode_attention_append(kv_pool* pool, int layer, const void* q, const void* k_new,
+                                         const void* v_new, kv_dtype in_dtype, float* out,
+                                         const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* context_lens, int batch, int max_context,
+                                         float scale, int partition_tokens, void* workspace,
+                                         size_t workspace_bytes, kv_stream_t stream);
+
 /* Size of the library's fixed device scratch array used by paged_decode_attention_static. */
 #define KV_STATIC_SCRATCH_BYTES (16u << 20)
 

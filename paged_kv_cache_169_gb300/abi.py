@@ -48,6 +48,9 @@ _SIGS = {
     "paged_decode_workspace_size": (C.c_size_t, [_VP, C.c_int, C.c_int, C.c_int]),
     "paged_decode_attention": (C.c_int, [_VP, C.c_int, _VP, _VP, _VP, C.c_int, _VP, C.c_int,
                                          C.c_int, C.c_float, C.c_int, _VP, C.c_size_t, _VP]),
+    "paged_decode_attention_append": (C.c_int, [_VP, C.c_int, _VP, _VP, _VP, C.c_int, _VP, _VP, C.c_int,
+                                                _VP, C.c_int, C.c_int, C.c_float, C.c_int, _VP,
+                                                C.c_size_t, _VP]),
     "paged_decode_attention_static": (C.c_int, [_VP, C.c_int, _VP, _VP, _VP, C.c_int, _VP, C.c_int,
                                                 C.c_int, C.c_float, C.c_int, _VP]),
     "kv_alloc_create": (C.c_int, [C.c_int, C.c_int, _I32P, C.POINTER(_VP)]),
@@ -169,6 +172,16 @@ def paged_decode_attention(pool: int, layer: int, q: int, out: int, block_tables
     _check("paged_decode_attention", load().paged_decode_attention(
         pool, layer, q, out, block_tables, max_blocks_per_seq, context_lens, batch, max_context,
         scale, partition_tokens, workspace, workspace_bytes, stream))
+
+
+def paged_decode_attention_append(pool: int, layer: int, q: int, k_new: int, v_new: int,
+                                  in_dtype: int, out: int, block_tables: int, max_blocks_per_seq: int,
+                                  context_lens: int, batch: int, max_context: int, scale: float,
+                                  partition_tokens: int, workspace: int, workspace_bytes: int,
+                                  stream: int = 0) -> None:
+    _check("paged_decode_attention_append", load().paged_decode_attention_append(
+        pool, layer, q, k_new, v_new, in_dtype, out, block_tables, max_blocks_per_seq, context_lens,
+        batch, max_context, scale, partition_tokens, workspace, workspace_bytes, stream))
 
 
 KV_STATIC_SCRATCH_BYTES = 16 << 20

@@ -106,6 +106,28 @@ class PagedKVCache:
             partition_tokens, _dev_ptr(ws, "workspace"), ws.numel(), _stream(stream))
         return out
 
+    def attention_append(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                         block_tables: torch.Tensor, context_lens: torch.Tensor, max_context: int,
+                         scale: float, out: torch.Tensor | None = None, partition_tokens: int = 0,
+                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Fused decode step: store each sequence's newest token (k_new, v_new [batch, H, d])
+        at position context_lens[s]-1 through its table, then attend.  Returns out."""
+        batch = q.shape[0]
+        if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+            raise ValueError("block_tables and context_lens must be int32")
+        if k_new.shape != (batch, self.num_heads, self.head_dim) or v_new.shape != k_new.shape \
+                or k_new.dtype != v_new.dtype:
+            raise ValueError("k_new and v_new must be [batch, H, d] of one dtype")
+        if out is None:
+            out = torch.empty((batch, self.num_heads, self.head_dim), dtype=torch.float32, device=q.device)
+        ws = workspace if workspace is not None else self.workspace(batch, max_context, partition_tokens)
+        abi.paged_decode_attention_append(
+            self.handle, layer, _dev_ptr(q, "q"), _dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"),
+            _IN_DTYPE[k_new.dtype], _dev_ptr(out, "out"), _dev_ptr(block_tables, "block_tables"),
+            block_tables.shape[1], _dev_ptr(context_lens, "context_lens"), batch, max_context,
+            float(scale), partition_tokens, _dev_ptr(ws, "workspace"), ws.numel(), _stream(stream))
+        return out
+
     def device_error(self, clear: bool = True, stream=None) -> int:
         return abi.kv_get_device_error(self.handle, _stream(stream), clear)
 

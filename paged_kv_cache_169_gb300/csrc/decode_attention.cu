@@ -26,8 +26,9 @@
 //   by shuffle, and the two halves are summed once per item.  ("KV Cache篇" §6.3:
 //   tiles in on-chip SRAM, softmax state kept on chip.)
 // * A sequence that fits one partition is normalised and written directly; longer
-//   ones write (m, l, o) partials merged by attention_reduce_kernel (exact
-//   log-sum-exp merge).
+//   ones write (m, l, o) partials.  Each (sequence, head) counts its finished
+//   partitions with an atomic ticket; the warp that finishes the last one merges them
+//   (exact log-sum-exp merge) — no second kernel, and no warp ever waits for another.
 //
 // No tensor cores: one query row per head is a matrix-vector product bound by HBM.
 
@@ -43,11 +44,13 @@ constexpr int kMaxSub = 64;        // launches per call -> batch <= 65536
 constexpr int kPartAlign = 32;     // partition sizes are multiples of this
 constexpr unsigned FULL = 0xffffffffu;
 
-enum : int { F_FIRST = 1, F_LAST = 2, F_TERM = 4, F_SINGLE = 8 };
+enum : int { F_FIRST = 1, F_LAST = 2, F_TERM = 4, F_SINGLE = 8, F_PATCH = 16 };
 
 struct __align__(16) Meta {
     int s, h, p, ntok;      // item (sequence, head, partition); valid tokens in the chunk
-    int flags, pad0, pad1, pad2;
+    int flags;
+    int patch_row;          // F_PATCH: chunk row of the token appended by this call
+    int patch_id, patch_off;   // F_PATCH: its physical block and offset inside the block
     int ids[4];             // physical block of each copy in the chunk (FP8: scale lookup)
 };
 
@@ -107,8 +110,8 @@ struct Cfg {
 };
 
 struct AttnArgs {
-    const char* kpool;
-    const char* vpool;
+    char* kpool;           // written only by the fused append (the new token's slot)
+    char* vpool;
     const float* kscale;
     const float* vscale;
     const void* q;
@@ -118,6 +121,10 @@ struct AttnArgs {
     float* part_ml;        // [batch*H*max_parts][2]  (m in log2 units, l)
     float* part_o;         // [batch*H*max_parts][D]  unnormalised
     unsigned* counter;
+    unsigned* arrivals;    // [batch*H] partitions finished per (sequence, head)
+    const char* k_new;     // fused append: [batch][H][D] new-token K (nullptr: no append)
+    const char* v_new;
+    int in_bytes;          // element size of k_new / v_new (2 or 4)
     int* err;
     int batch, H, B, max_blocks, ctx_limit, P, max_parts, num_blocks;
     float qscale;          // scale * log2(e)
@@ -207,7 +214,7 @@ __device__ __forceinline__ void load_q(const char* qrow, int sub, float qs, floa
 }
 
 struct __align__(16) Item {
-    int s, h, p, tok0, ntok, nchunks, single, valid;
+    int s, h, p, tok0, ntok, nchunks, single, valid, last;   // last: final partition
 };
 
 // (s, h, p) of compact item index `it` (items ordered by sequence, head, partition).
@@ -234,7 +241,94 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
     r.ntok = min(P, ctx - r.tok0);
     r.nchunks = r.ntok > 0 ? (r.ntok + CT - 1) / CT : 1;
     r.single = np == 1;
+    r.last = r.p == np - 1;
     return r;
+}
+
+// Split-context merge of the np partials of one (sequence, head), by one warp:
+// M = max m_p, L = sum l_p 2^(m_p - M), out = sum o_p 2^(m_p - M) / L.
+// The partials were written by other SMs; they are read through L2 (ld.global.cg).
+template <int D>
+__device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh, int np, int lane) {
+    constexpr int DW = D / 32;
+    const int64_t base = sh * a.max_parts;
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + base;
+    float mx = -CUDART_INF_F;
+    for (int p = lane; p < np; p += 32) mx = fmaxf(mx, __ldcg(ml + p).x);
+    mx = warp_max(mx);
+    float L = 0.f, acc[DW];
+    #pragma unroll
+    for (int i = 0; i < DW; ++i) acc[i] = 0.f;
+    #pragma unroll 4
+    for (int p = 0; p < np; ++p) {
+        const float2 v = __ldcg(ml + p);
+        const float wgt = ex2_approx(v.x - mx);
+        L = fmaf(v.y, wgt, L);
+        const float* o = a.part_o + (base + p) * D + lane * DW;
+        if constexpr (DW == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
+            acc[0] = fmaf(wgt, x.x, acc[0]); acc[1] = fmaf(wgt, x.y, acc[1]);
+            acc[2] = fmaf(wgt, x.z, acc[2]); acc[3] = fmaf(wgt, x.w, acc[3]);
+        } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(o));
+            acc[0] = fmaf(wgt, x.x, acc[0]); acc[1] = fmaf(wgt, x.y, acc[1]);
+        }
+    }
+    const float inv = 1.f / L;
+    float* out = a.out + sh * D + lane * DW;
+    #pragma unroll
+    for (int i = 0; i < DW; ++i) out[i] = acc[i] * inv;
+}
+
+// Fused append: lane's D/32 elements of one new-token row (src, in_bytes per element)
+// are converted to the pool type (FP8: RNE-satfinite(x / scale)) and written both into
+// the consumer's stage row and into the pool slot, so the attention below sees exactly
+// the bytes a separate kv_append would have stored.
+template <typename C>
+__device__ __forceinline__ void patch_row(const char* src, int in_bytes, char* srow, char* grow,
+                                          float scale, int lane) {
+    constexpr int DW = C::D / 32;
+    const int e0 = lane * DW;
+    if constexpr (C::ESZ == 4) {
+        static_assert(DW == 4 || DW == 2, "head_dim 64 or 128");
+        if constexpr (DW == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src + e0 * 4);
+            *reinterpret_cast<float4*>(srow + e0 * 4) = v;
+            *reinterpret_cast<float4*>(grow + e0 * 4) = v;
+        } else {
+            const float2 v = *reinterpret_cast<const float2*>(src + e0 * 4);
+            *reinterpret_cast<float2*>(srow + e0 * 4) = v;
+            *reinterpret_cast<float2*>(grow + e0 * 4) = v;
+        }
+    } else if constexpr (C::ESZ == 2) {
+        if constexpr (DW == 4) {
+            const uint2 v = *reinterpret_cast<const uint2*>(src + e0 * 2);
+            *reinterpret_cast<uint2*>(srow + e0 * 2) = v;
+            *reinterpret_cast<uint2*>(grow + e0 * 2) = v;
+        } else {
+            const uint32_t v = *reinterpret_cast<const uint32_t*>(src + e0 * 2);
+            *reinterpret_cast<uint32_t*>(srow + e0 * 2) = v;
+            *reinterpret_cast<uint32_t*>(grow + e0 * 2) = v;
+        }
+    } else {
+        float x[DW];
+        #pragma unroll
+        for (int i = 0; i < DW; ++i)
+            x[i] = in_bytes == 2 ? __half2float(reinterpret_cast<const __half*>(src)[e0 + i])
+                                 : reinterpret_cast<const float*>(src)[e0 + i];
+        uint16_t q[DW / 2];
+        #pragma unroll
+        for (int i = 0; i < DW / 2; ++i)
+            q[i] = float2_to_e4m3x2(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
+        if constexpr (DW == 4) {
+            const uint32_t v = static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 16);
+            *reinterpret_cast<uint32_t*>(srow + e0) = v;
+            *reinterpret_cast<uint32_t*>(grow + e0) = v;
+        } else {
+            *reinterpret_cast<uint16_t*>(srow + e0) = q[0];
+            *reinterpret_cast<uint16_t*>(grow + e0) = q[0];
+        }
+    }
 }
 
 template <typename C>
@@ -345,12 +439,22 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
                     meta->h = cur.h;
                     meta->p = cur.p;
                     meta->ntok = nt;
+                    // fused append: the sequence's newest token is the last row of the
+                    // last chunk of its last partition
+                    const bool patch = a.k_new != nullptr && cur.last && c == cur.nchunks - 1 && nt > 0;
                     meta->flags = (c == 0 ? F_FIRST : 0) | (c == cur.nchunks - 1 ? F_LAST : 0) |
-                                  (cur.single ? F_SINGLE : 0);
-                    if constexpr (C::FP8) {
+                                  (cur.single ? F_SINGLE : 0) | (patch ? F_PATCH : 0);
+                    if (patch) {
+                        const int r = nt - 1, jr = r / rpc;
+                        int pid = ids[0];
                         #pragma unroll
-                        for (int j = 0; j < CBMAX; ++j) meta->ids[j] = ids[j];
+                        for (int j = 1; j < CBMAX; ++j) if (j == jr) pid = ids[j];
+                        meta->patch_row = r;
+                        meta->patch_id = pid;
+                        meta->patch_off = row0 + r % rpc;
                     }
+                    #pragma unroll
+                    for (int j = 0; j < CBMAX; ++j) meta->ids[j] = ids[j];
                     if (bytes) mbar_arrive_expect_tx(fb, bytes);
                     else mbar_arrive(fb);
                     const uint32_t dst = smem_u32(stg);
@@ -435,6 +539,26 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
             #pragma unroll
             for (int i = 0; i < DPL / 2; ++i) acc[i] = make_float2(0.f, 0.f);
             if (nt > 0) load_q<C>(stg + C::Q_OFF, sub, a.qscale, q2);
+        }
+        if (meta.flags & F_PATCH) {
+            // this warp owns the stage now: put the new token into its row and its slot
+            const Meta* mp = reinterpret_cast<const Meta*>(stg + C::META_OFF);
+            const int r = mp->patch_row;
+            const int64_t sh = static_cast<int64_t>(meta.s) * a.H + meta.h;
+            const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + meta.h) * a.B + mp->patch_off;
+            float ksc = 1.f, vsc = 1.f;
+            if constexpr (C::FP8) {
+                ksc = __ldg(a.kscale + mp->patch_id);
+                vsc = __ldg(a.vscale + mp->patch_id);
+            }
+            char* srow = const_cast<char*>(stg);
+            patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, srow + C::K_OFF + r * C::ROW,
+                         a.kpool + grow * C::ROW, ksc, lane);
+            patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, srow + C::V_OFF + r * C::ROW,
+                         a.vpool + grow * C::ROW, vsc, lane);
+            // the stage is refilled by the TMA engine later: order these generic writes first
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
         }
         if (nt > 0) {
             float ks = 1.f, vs = 1.f;
@@ -527,42 +651,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
                     #pragma unroll
                     for (int i = 0; i < DPL / 2; ++i) dst[i] = o[i];
                 }
+                // publish the partial, then take a ticket; the last partition merges
+                __threadfence();
+                __syncwarp();
+                unsigned prev = 0;
+                if (lane == 0) prev = atomicAdd(a.arrivals + sh, 1u);
+                prev = __shfl_sync(FULL, prev, 0);
+                const int np = nparts_of(s_ctx[meta.s], a.P);
+                if (prev == static_cast<unsigned>(np - 1)) {
+                    __threadfence();
+                    merge_partials<D>(a, sh, np, lane);
+                }
             }
         }
     }
-}
-
-// Merge the partials of every (sequence, head) split into more than one partition:
-// M = max m_p, L = sum l_p 2^(m_p - M), out = sum o_p 2^(m_p - M) / L.
-template <int D>
-__global__ void __launch_bounds__(256) attention_reduce_kernel(AttnArgs a) {
-    constexpr int DPL = D / 32;
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (gw >= static_cast<int64_t>(a.batch) * a.H) return;
-    const int s = static_cast<int>(gw / a.H);
-    int ctx = a.lens[s];
-    ctx = ctx < 0 ? 0 : (ctx > a.ctx_limit ? a.ctx_limit : ctx);
-    const int np = nparts_of(ctx, a.P);
-    if (np <= 1) return;
-    const int64_t base = gw * a.max_parts;
-    float mx = -CUDART_INF_F;
-    for (int p = lane; p < np; p += 32) mx = fmaxf(mx, a.part_ml[2 * (base + p)]);
-    mx = warp_max(mx);
-    float L = 0.f, acc[DPL];
-    #pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-    for (int p = 0; p < np; ++p) {
-        const float wgt = ex2_approx(a.part_ml[2 * (base + p)] - mx);
-        L = fmaf(a.part_ml[2 * (base + p) + 1], wgt, L);
-        const float* o = a.part_o + (base + p) * D + lane * DPL;
-        #pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(wgt, o[i], acc[i]);
-    }
-    const float inv = 1.f / L;
-    float* out = a.out + gw * D + lane * DPL;
-    #pragma unroll
-    for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
 }
 
 template <typename C>
@@ -586,10 +688,16 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
         sa.out = args.out + static_cast<int64_t>(s0) * args.H * C::D;
         sa.tables = args.tables + static_cast<int64_t>(s0) * args.max_blocks;
         sa.lens = args.lens + s0;
+        if (args.k_new) {
+            const int64_t nofs = static_cast<int64_t>(s0) * args.H * C::D * args.in_bytes;
+            sa.k_new = args.k_new + nofs;
+            sa.v_new = args.v_new + nofs;
+        }
         const int64_t pofs = static_cast<int64_t>(s0) * args.H * args.max_parts;
         if (args.part_ml) {
             sa.part_ml = args.part_ml + 2 * pofs;
             sa.part_o = args.part_o + pofs * C::D;
+            sa.arrivals = args.arrivals + static_cast<int64_t>(s0) * args.H;
         }
         sa.counter = counters + sub;
         const int64_t upper = static_cast<int64_t>(sa.batch) * args.H * args.max_parts;
@@ -599,12 +707,7 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
         attention_partition_kernel<C><<<static_cast<int>(grid), C::THREADS, C::SMEM, stream>>>(sa);
         if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     }
-    if (plan.max_parts > 1) {
-        const int64_t warps = static_cast<int64_t>(total) * args.H;
-        const int blocks = static_cast<int>((warps + 7) / 8);
-        attention_reduce_kernel<C::D><<<blocks, 256, 0, stream>>>(args);
-        if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
-    }
+    (void)plan;
     return KV_OK;
 }
 
@@ -653,6 +756,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     size_t ws = 256;                                // kMaxSub work counters
     if (plan->max_parts > 1) {
         const size_t n = static_cast<size_t>(batch) * d.num_heads * plan->max_parts;
+        ws += align256(static_cast<size_t>(batch) * d.num_heads * sizeof(unsigned));   // arrivals
         ws += align256(n * 2 * sizeof(float));
         ws += align256(n * d.head_dim * sizeof(float));
     }
@@ -664,16 +768,29 @@ int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,
                      const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                      int batch, int max_context, float scale, const AttnPlan& plan,
                      void* workspace, cudaStream_t stream) {
+    return launch_attention_append(pool, layer, q, nullptr, nullptr, 0, out, block_tables, max_blocks,
+                                   context_lens, batch, max_context, scale, plan, workspace, stream);
+}
+
+int launch_attention_append(const kv_pool* pool, int layer, const void* q, const void* k_new,
+                            const void* v_new, int in_bytes, float* out, const int32_t* block_tables,
+                            int max_blocks, const int32_t* context_lens, int batch, int max_context,
+                            float scale, const AttnPlan& plan, void* workspace, cudaStream_t stream) {
     const kv_pool_desc& d = pool->desc;
     if (batch == 0) return KV_OK;
     char* ws = static_cast<char*>(workspace);
     unsigned* counters = reinterpret_cast<unsigned*>(ws);
-    const int nsub = (batch + kMaxBatch - 1) / kMaxBatch;
-    if (cudaMemsetAsync(counters, 0, nsub * sizeof(unsigned), stream) != cudaSuccess) return KV_ERR_CUDA;
+    const size_t arrivals_bytes =
+        plan.max_parts > 1 ? align256(static_cast<size_t>(batch) * d.num_heads * sizeof(unsigned)) : 0;
+    // work counters and per-(sequence, head) arrival counters start at zero every call
+    if (cudaMemsetAsync(counters, 0, 256 + arrivals_bytes, stream) != cudaSuccess) return KV_ERR_CUDA;
 
     AttnArgs a{};
-    a.kpool = static_cast<const char*>(pool->k_layers[layer]);
-    a.vpool = static_cast<const char*>(pool->v_layers[layer]);
+    a.kpool = static_cast<char*>(pool->k_layers[layer]);
+    a.vpool = static_cast<char*>(pool->v_layers[layer]);
+    a.k_new = static_cast<const char*>(k_new);
+    a.v_new = static_cast<const char*>(v_new);
+    a.in_bytes = in_bytes;
     a.kscale = pool->k_scales ? pool->k_scales[layer] : nullptr;
     a.vscale = pool->v_scales ? pool->v_scales[layer] : nullptr;
     a.q = q;
@@ -682,8 +799,9 @@ int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,
     a.lens = context_lens;
     if (plan.max_parts > 1) {
         const size_t n = static_cast<size_t>(batch) * d.num_heads * plan.max_parts;
-        a.part_ml = reinterpret_cast<float*>(ws + 256);
-        a.part_o = reinterpret_cast<float*>(ws + 256 + align256(n * 2 * sizeof(float)));
+        a.arrivals = reinterpret_cast<unsigned*>(ws + 256);
+        a.part_ml = reinterpret_cast<float*>(ws + 256 + arrivals_bytes);
+        a.part_o = reinterpret_cast<float*>(ws + 256 + arrivals_bytes + align256(n * 2 * sizeof(float)));
     }
     a.err = pool->d_err;
     a.batch = batch;
