@@ -133,3 +133,23 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale:
         k_seqs.append(Ks)
         v_seqs.append(Vs)
     return decode_attention(q, k_seqs, v_seqs, scale)
+
+
+def decode_attention_gqa(q, k_seqs, v_seqs, scale: float) -> np.ndarray:
+    """Grouped-query decode attention ([KV Cache篇] §6.2: groups of query heads share one
+    K/V head; MQA is a single shared head).
+
+    q: [batch, Hq, d]; k_seqs/v_seqs: list of [n_s, Hkv, d] with Hq a multiple of Hkv.
+    Query head j of a group of G = Hq / Hkv consecutive heads reads K/V head j // G.
+    """
+    q = _f64(q)
+    b, Hq, d = q.shape
+    out = np.zeros((b, Hq, d), dtype=np.float64)
+    for s in range(b):
+        Ks, Vs = _f64(k_seqs[s]), _f64(v_seqs[s])
+        Hkv = Ks.shape[1]
+        assert Hq % Hkv == 0
+        G = Hq // Hkv
+        for j in range(Hq):
+            out[s, j] = decode_attention_one(q[s, j], Ks[:, j // G, :], Vs[:, j // G, :], scale)
+    return out

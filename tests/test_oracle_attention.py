@@ -261,3 +261,33 @@ def test_fp8_paged_dequantises_with_block_scale():
     V = np.stack([fp8.decode(codes_v[table[0, t // B], :, t % B]) * vs[table[0, t // B]] for t in range(n)])
     want = A.decode_attention(q, [K], [V], 0.3)
     np.testing.assert_allclose(got, want, rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------- grouped-query attention
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_gqa_equals_mha_on_replicated_kv_heads(G):
+    """Sharing a K/V head among G query heads is MHA over K/V heads repeated G times."""
+    rng = np.random.default_rng(500 + G)
+    Hkv, d, lens = 3, 16, [1, 9, 40]
+    q = rng.standard_normal((len(lens), Hkv * G, d))
+    ks = [rng.standard_normal((n, Hkv, d)) for n in lens]
+    vs = [rng.standard_normal((n, Hkv, d)) for n in lens]
+    got = A.decode_attention_gqa(q, ks, vs, 0.3)
+    want = A.decode_attention(q, [np.repeat(k, G, axis=1) for k in ks], [np.repeat(v, G, axis=1) for v in vs], 0.3)
+    assert np.array_equal(got, want)
+    if G == 1:
+        assert np.array_equal(got, A.decode_attention(q, ks, vs, 0.3))
+
+
+def test_gqa_matches_torch_sdpa_enable_gqa():
+    rng = np.random.default_rng(510)
+    Hkv, G, d, n = 2, 4, 32, 21
+    q = rng.standard_normal((1, Hkv * G, d))
+    k = rng.standard_normal((n, Hkv, d))
+    v = rng.standard_normal((n, Hkv, d))
+    got = A.decode_attention_gqa(q, [k], [v], 1 / math.sqrt(d))[0]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q[0]).view(1, Hkv * G, 1, d), torch.from_numpy(k).permute(1, 0, 2)[None],
+        torch.from_numpy(v).permute(1, 0, 2)[None], enable_gqa=True).view(Hkv * G, d).numpy()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13)
