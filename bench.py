@@ -35,6 +35,8 @@ def make_workload(name: str):
     elif name == "llama7b":
         w = W.llama7b()
         w.lens = [n + w.steps for n in w.lens]       # context after the last of the 64 steps
+    elif name == "gqa70b":
+        w = W.gqa70b()
     elif name.startswith("ragged"):
         # ragged_f16_b16 | ragged_fp8_b8 ...
         _, dt, b = name.split("_")
@@ -59,9 +61,10 @@ def algorithmic_bytes(w) -> int:
     and for FP8 pools the two per-block scales."""
     kv_elem = 1 if w.kv == "fp8" else 2
     H, d, B = w.num_heads, w.head_dim, w.block_size
+    Hq = w.q_heads                                   # query heads (grouped-query: > H)
     kv = sum(w.lens) * H * d * kv_elem * 2
-    q = w.batch * H * d * 2
-    out = w.batch * H * d * 4
+    q = w.batch * Hq * d * 2
+    out = w.batch * Hq * d * 4
     tables = sum(-(-n // B) for n in w.lens) * 4
     lens = w.batch * 4
     scales = sum(-(-n // B) for n in w.lens) * 8 if w.kv == "fp8" else 0
@@ -299,15 +302,22 @@ def run_ours(args):
     tdt = torch.float16
     g = torch.Generator(device=dev)
     g.manual_seed(w.seed * 7 + 1)
-    q = torch.randn((L, w.batch, H, d), generator=g, device=dev).to(tdt)
+    Hq = w.q_heads
+    q = torch.randn((L, w.batch, Hq, d), generator=g, device=dev).to(tdt)
     k_new = torch.randn((L, w.batch, H, d), generator=g, device=dev).to(tdt)
     v_new = torch.randn((L, w.batch, H, d), generator=g, device=dev).to(tdt)
     bt = torch.from_numpy(tables).to(dev)
     cl = torch.from_numpy(lens_h).to(dev)
     slots = torch.from_numpy(slots_h).to(dev)
-    out = torch.empty((L, w.batch, H, d), dtype=torch.float32, device=dev)
+    out = torch.empty((L, w.batch, Hq, d), dtype=torch.float32, device=dev)
     max_ctx = max(w.lens)
-    ws = cache.workspace(w.batch, max_ctx, args.partition)
+    grouped = Hq != H
+    if grouped:
+        from paged_kv_cache_169_gb300 import abi as _abi
+        ws = torch.empty(_abi.paged_decode_workspace_size_gqa(cache.handle, w.batch, Hq, max_ctx, args.partition),
+                         dtype=torch.uint8, device=dev)
+    else:
+        ws = cache.workspace(w.batch, max_ctx, args.partition)
     stream = torch.cuda.current_stream(dev)
 
     from paged_kv_cache_169_gb300 import abi
@@ -320,7 +330,12 @@ def run_ours(args):
                 cache.append(l, k_new[l], v_new[l], slots)
             if ev is not None:
                 ev[l][0].record(stream)
-            if args.unfused:
+            if grouped:
+                cache.attention_gqa(l, q[l], bt, cl, max_ctx, w.scale,
+                                    k_new=None if args.unfused else k_new[l],
+                                    v_new=None if args.unfused else v_new[l], out=out[l],
+                                    partition_tokens=args.partition, workspace=ws)
+            elif args.unfused:
                 cache.attention(l, q[l], bt, cl, max_ctx, w.scale, out=out[l],
                                 partition_tokens=args.partition, workspace=ws)
             else:   # one launch: append each sequence's newest token, then attend
@@ -355,8 +370,8 @@ def run_ours(args):
     attn_ms_mean = sum(attn_ms) / len(attn_ms)
 
     # ---- end-to-end through the public API with host buffers
-    pin = dict(q=torch.empty(q.shape, dtype=tdt).pin_memory(), k=torch.empty(q.shape, dtype=tdt).pin_memory(),
-               v=torch.empty(q.shape, dtype=tdt).pin_memory(), out=torch.empty(out.shape).pin_memory(),
+    pin = dict(q=torch.empty(q.shape, dtype=tdt).pin_memory(), k=torch.empty(k_new.shape, dtype=tdt).pin_memory(),
+               v=torch.empty(v_new.shape, dtype=tdt).pin_memory(), out=torch.empty(out.shape).pin_memory(),
                slots=torch.from_numpy(slots_h).pin_memory(), bt=torch.from_numpy(tables).pin_memory(),
                cl=torch.from_numpy(lens_h).pin_memory())
     pin["q"].copy_(q.cpu())
@@ -410,7 +425,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32-accum/" + w.kv, "data": "synthetic",
-        "config": {"workload": args.workload, "layers": L, "batch": w.batch, "heads": H, "head_dim": d,
+        "config": {"workload": args.workload, "layers": L, "batch": w.batch, "heads": H, "q_heads": Hq,
+                   "head_dim": d,
                    "block_size": BS, "kv_dtype": w.kv, "context_mean": sum(w.lens) / len(w.lens),
                    "context_max": max_ctx, "pool_gib": round(2 * L * w.num_blocks * H * BS * d *
                                                              (1 if w.kv == "fp8" else 2) / 2 ** 30, 2),

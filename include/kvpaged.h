@@ -202,6 +202,26 @@ KV_API int paged_decode_attention_append(kv_pool* pool, int layer, const void* q
                                          float scale, int partition_tokens, void* workspace,
                                          size_t workspace_bytes, kv_stream_t stream);
 
+/* Grouped-query (GQA) and multi-query (MQA) decode attention: num_q_heads query heads
+ * share the pool's num_heads KV heads; query head j reads KV head j / G with
+ * G = num_q_heads / num_heads in {1, 2, 4, 8} (G > 1: fp16 and FP8 pools).  Each K/V tile
+ * is read once for its G query heads.
+ *   q    device [batch][num_q_heads][head_dim] (as paged_decode_attention).
+ *   out  device float32 [batch][num_q_heads][head_dim].
+ *   k_new, v_new  NULL, or the newest token's K/V [batch][num_heads][head_dim] of in_dtype
+ *        appended first exactly as paged_decode_attention_append does.
+ * Everything else as paged_decode_attention; the workspace size comes from
+ * paged_decode_workspace_size_gqa.  [KV Cache篇] §6.2 (MQA/GQA: KV heads shared by
+ * groups of query heads, fewer bytes read). */
+KV_API size_t paged_decode_workspace_size_gqa(const kv_pool* pool, int batch, int num_q_heads,
+                                              int max_context, int partition_tokens);
+KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, int num_q_heads,
+                                      const void* k_new, const void* v_new, kv_dtype in_dtype,
+                                      float* out, const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int batch, int max_context,
+                                      float scale, int partition_tokens, void* workspace,
+                                      size_t workspace_bytes, kv_stream_t stream);
+
 /* Size of the library's fixed device scratch array used by paged_decode_attention_static. */
 #define KV_STATIC_SCRATCH_BYTES (16u << 20)
 

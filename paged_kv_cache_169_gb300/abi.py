@@ -51,6 +51,10 @@ _SIGS = {
     "paged_decode_attention_append": (C.c_int, [_VP, C.c_int, _VP, _VP, _VP, C.c_int, _VP, _VP, C.c_int,
                                                 _VP, C.c_int, C.c_int, C.c_float, C.c_int, _VP,
                                                 C.c_size_t, _VP]),
+    "paged_decode_workspace_size_gqa": (C.c_size_t, [_VP, C.c_int, C.c_int, C.c_int, C.c_int]),
+    "paged_decode_attention_gqa": (C.c_int, [_VP, C.c_int, _VP, C.c_int, _VP, _VP, C.c_int, _VP, _VP,
+                                             C.c_int, _VP, C.c_int, C.c_int, C.c_float, C.c_int, _VP,
+                                             C.c_size_t, _VP]),
     "paged_decode_attention_static": (C.c_int, [_VP, C.c_int, _VP, _VP, _VP, C.c_int, _VP, C.c_int,
                                                 C.c_int, C.c_float, C.c_int, _VP]),
     "kv_alloc_create": (C.c_int, [C.c_int, C.c_int, _I32P, C.POINTER(_VP)]),
@@ -182,6 +186,24 @@ def paged_decode_attention_append(pool: int, layer: int, q: int, k_new: int, v_n
     _check("paged_decode_attention_append", load().paged_decode_attention_append(
         pool, layer, q, k_new, v_new, in_dtype, out, block_tables, max_blocks_per_seq, context_lens,
         batch, max_context, scale, partition_tokens, workspace, workspace_bytes, stream))
+
+
+def paged_decode_workspace_size_gqa(pool: int, batch: int, num_q_heads: int, max_context: int,
+                                    partition_tokens: int = 0) -> int:
+    n = load().paged_decode_workspace_size_gqa(pool, batch, num_q_heads, max_context, partition_tokens)
+    if n == 0:
+        raise KvError("paged_decode_workspace_size_gqa", KV_ERR_INVALID_ARG)
+    return n
+
+
+def paged_decode_attention_gqa(pool: int, layer: int, q: int, num_q_heads: int, k_new: int, v_new: int,
+                               in_dtype: int, out: int, block_tables: int, max_blocks_per_seq: int,
+                               context_lens: int, batch: int, max_context: int, scale: float,
+                               partition_tokens: int, workspace: int, workspace_bytes: int,
+                               stream: int = 0) -> None:
+    _check("paged_decode_attention_gqa", load().paged_decode_attention_gqa(
+        pool, layer, q, num_q_heads, k_new, v_new, in_dtype, out, block_tables, max_blocks_per_seq,
+        context_lens, batch, max_context, scale, partition_tokens, workspace, workspace_bytes, stream))
 
 
 KV_STATIC_SCRATCH_BYTES = 16 << 20

@@ -23,7 +23,8 @@ LIB = os.path.join(OUT_DIR, "libkvpaged.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-DKVPAGED_BUILD"]
-SOURCES = ["api.cu", "append_copy.cu", "decode_attention.cu", "static_scratch.cu", "allocator.cpp"]
+SOURCES = ["api.cu", "append_copy.cu", "decode_attention.cu", "decode_attention_gqa.cu",
+           "static_scratch.cu", "allocator.cpp"]
 
 
 def _nvcc() -> str:

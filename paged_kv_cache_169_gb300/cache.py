@@ -128,6 +128,33 @@ class PagedKVCache:
             float(scale), partition_tokens, _dev_ptr(ws, "workspace"), ws.numel(), _stream(stream))
         return out
 
+    def attention_gqa(self, layer: int, q: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, max_context: int, scale: float,
+                      k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None, partition_tokens: int = 0,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Grouped-query decode attention: q [batch, Hq, d] with Hq a multiple (1, 2, 4, 8) of
+        the pool's KV heads; optional fused append of k_new/v_new [batch, H, d]."""
+        batch, hq = q.shape[0], q.shape[1]
+        if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+            raise ValueError("block_tables and context_lens must be int32")
+        if out is None:
+            out = torch.empty((batch, hq, self.head_dim), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            n = abi.paged_decode_workspace_size_gqa(self.handle, batch, hq, max_context, partition_tokens)
+            if self._ws is None or self._ws.numel() < n:
+                self._ws = torch.empty(n, dtype=torch.uint8, device=self.k[0].device)
+            workspace = self._ws
+        kp = _dev_ptr(k_new, "k_new") if k_new is not None else 0
+        vp = _dev_ptr(v_new, "v_new") if v_new is not None else 0
+        dt = _IN_DTYPE[k_new.dtype] if k_new is not None else 0
+        abi.paged_decode_attention_gqa(
+            self.handle, layer, _dev_ptr(q, "q"), hq, kp, vp, dt, _dev_ptr(out, "out"),
+            _dev_ptr(block_tables, "block_tables"), block_tables.shape[1],
+            _dev_ptr(context_lens, "context_lens"), batch, max_context, float(scale), partition_tokens,
+            _dev_ptr(workspace, "workspace"), workspace.numel(), _stream(stream))
+        return out
+
     def device_error(self, clear: bool = True, stream=None) -> int:
         return abi.kv_get_device_error(self.handle, _stream(stream), clear)
 

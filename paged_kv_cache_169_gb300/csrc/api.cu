@@ -208,4 +208,50 @@ int paged_decode_attention_append(kv_pool* pool, int layer, const void* q, const
                                         max_context, scale, plan, workspace, stream);
 }
 
+size_t paged_decode_workspace_size_gqa(const kv_pool* pool, int batch, int num_q_heads, int max_context,
+                                       int partition_tokens) {
+    if (!pool || num_q_heads < 1 || num_q_heads % pool->desc.num_heads != 0) return 0;
+    kvp::AttnPlan plan;
+    if (kvp::plan_attention(pool, batch, max_context, partition_tokens, &plan,
+                            num_q_heads / pool->desc.num_heads) != KV_OK)
+        return 0;
+    return plan.ws_bytes;
+}
+
+int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, int num_q_heads,
+                               const void* k_new, const void* v_new, kv_dtype in_dtype, float* out,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int batch, int max_context, float scale,
+                               int partition_tokens, void* workspace, size_t workspace_bytes,
+                               kv_stream_t stream) {
+    if (!pool || layer < 0 || layer >= pool->desc.num_layers || batch < 0 || max_context < 0)
+        return KV_ERR_INVALID_ARG;
+    if (num_q_heads < 1 || num_q_heads % pool->desc.num_heads != 0) return KV_ERR_INVALID_ARG;
+    const int group = num_q_heads / pool->desc.num_heads;
+    if (!kvp::valid_group(pool->desc, group)) return KV_ERR_INVALID_ARG;
+    if (batch == 0) return KV_OK;
+    if (!q || !out || !block_tables || !context_lens || !workspace || max_blocks_per_seq < 1)
+        return KV_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return KV_ERR_INVALID_ARG;
+    if (!kvp::aligned16(q) || !kvp::aligned16(out) || (k_new && (!kvp::aligned16(k_new) || !kvp::aligned16(v_new))) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KV_ERR_INVALID_ARG;
+    if (k_new) {
+        const kv_dtype pd = pool->desc.dtype;
+        if (pd == KV_FP8_E4M3) {
+            if (in_dtype != KV_F16 && in_dtype != KV_F32) return KV_ERR_INVALID_ARG;
+        } else if (in_dtype != pd) {
+            return KV_ERR_INVALID_ARG;
+        }
+    }
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return KV_ERR_INVALID_ARG;
+    kvp::AttnPlan plan;
+    int rc = kvp::plan_attention(pool, batch, max_context, partition_tokens, &plan, group);
+    if (rc != KV_OK) return rc;
+    if (workspace_bytes < plan.ws_bytes) return KV_ERR_INVALID_ARG;
+    return kvp::launch_attention_append(pool, layer, q, k_new, v_new, k_new ? kvp::elem_bytes(in_dtype) : 0,
+                                        out, block_tables, max_blocks_per_seq, context_lens, batch,
+                                        max_context, scale, plan, workspace, stream);
+}
+
 }  // extern "C"

@@ -1,745 +1,60 @@
-// paged_decode_attention: one query token per (sequence, head) against that
-// sequence's cached K/V, read through its block table.
-//
-// What is computed ("大模型推理加速——KV Cache篇" §3.1; "KV缓存机制解析" §5.1):
-//   out[s,h] = softmax_t(scale * q[s,h] . K[s,t,h]) . V[s,t,h],  t < context_lens[s]
-// with the cache stored in fixed-size physical blocks found through a block table
-// ("KV Cache与PagedAttention" §2.1, §3.2).  The page's kernel sketch loads each
-// block into shared memory and attends block by block; here the same idea is laid
-// out for sm_103a:
-//
-// * Work items are (sequence, head, partition) triples; a partition is P tokens
-//   (split-context, flash-decoding style).  Items are handed out dynamically with one
-//   atomic counter, so ragged batches balance.
-// * Each CTA is persistent (one per SM): warps 0..NC-1 are consumers, warp NC is the
-//   producer.  Producer lane w serves consumer w: it polls that consumer's ring without
-//   blocking, and for every physical block of the next CT-token chunk issues one 1-D
-//   bulk copy (cp.async.bulk, the TMA engine) of the contiguous (block, head) K tile
-//   and one of the V tile into the ring stage, completing on the stage's mbarrier.
-//   Block-table entries are fetched one chunk ahead, work items one item ahead.
-// * A consumer warp owns NSW ring stages.  Its two half-warps read two token rows per
-//   16-byte shared-memory load (lane: head_dim/16 dims of one row).  Each lane forms
-//   partial dot products for its CT/2 tokens; a transpose-reduce over the 16 lanes of
-//   a half leaves one token's score per lane.  Softmax runs in fp32 in the log2
-//   domain with a running maximum that is only raised (and the state rescaled) when
-//   some score exceeds it by more than 8; V is accumulated in fp32 with p_t broadcast
-//   by shuffle, and the two halves are summed once per item.  ("KV Cache篇" §6.3:
-//   tiles in on-chip SRAM, softmax state kept on chip.)
-// * A sequence that fits one partition is normalised and written directly; longer
-//   ones write (m, l, o) partials.  Each (sequence, head) counts its finished
-//   partitions with an atomic ticket; the warp that finishes the last one merges them
-//   (exact log-sum-exp merge) — no second kernel, and no warp ever waits for another.
-//
-// No tensor cores: one query row per head is a matrix-vector product bound by HBM.
+// paged_decode_attention host side: partition plan, workspace layout and launches of the
+// kernel in attention_kernel.cuh (head groups of 1 here; larger groups in
+// decode_attention_gqa.cu).
 
-#include <math_constants.h>
-
-#include "kvp_internal.cuh"
+#include "attention_kernel.cuh"
 
 namespace kvp {
 namespace {
 
-constexpr int kMaxBatch = 1024;    // sequences per launch (prefix table in shared memory)
-constexpr int kMaxSub = 64;        // launches per call -> batch <= 65536
-constexpr int kPartAlign = 32;     // partition sizes are multiples of this
-constexpr unsigned FULL = 0xffffffffu;
-
-enum : int { F_FIRST = 1, F_LAST = 2, F_TERM = 4, F_SINGLE = 8, F_PATCH = 16 };
-
-struct __align__(16) Meta {
-    int s, h, p, ntok;      // item (sequence, head, partition); valid tokens in the chunk
-    int flags;
-    int patch_row;          // F_PATCH: chunk row of the token appended by this call
-    int patch_id, patch_off;   // F_PATCH: its physical block and offset inside the block
-    int ids[4];             // physical block of each copy in the chunk (FP8: scale lookup)
-};
-
-constexpr int round_up(int a, int b) { return (a + b - 1) / b * b; }
-
-// Launch shape per storage type: tokens per chunk (CT), consumer warps (NC), ring stages
-// per consumer (NSW).  Compile-time overrides exist only for tuning sweeps
-// (KVP_F16_CT/NC/NSW, KVP_FP8_CT/NC/NSW).
-template <int ESZ> struct Tune { static constexpr int CT = 32, NC = 0, NSW = 0; };   // 0: by stage size
-#if !defined(KVP_F16_CT)
-template <> struct Tune<2> { static constexpr int CT = 16, NC = 12, NSW = 0; };
-#endif
-#if !defined(KVP_FP8_CT)
-template <> struct Tune<1> { static constexpr int CT = 32, NC = 12, NSW = 0; };
-#endif
-#if defined(KVP_F16_CT) && defined(KVP_F16_NC) && defined(KVP_F16_NSW)
-template <> struct Tune<2> { static constexpr int CT = KVP_F16_CT, NC = KVP_F16_NC, NSW = KVP_F16_NSW; };
-#endif
-#if defined(KVP_FP8_CT) && defined(KVP_FP8_NC) && defined(KVP_FP8_NSW)
-template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_NC, NSW = KVP_FP8_NSW; };
-#endif
-
-template <int D_, typename KV_, typename QT_>
-struct Cfg {
-    static constexpr int D = D_;
-    using KV = KV_;
-    using QT = QT_;
-    static constexpr int ESZ = sizeof(KV);
-    static constexpr bool FP8 = (ESZ == 1);
-    static constexpr int CT = Tune<ESZ>::CT;
-    static constexpr int TPL = CT / 2;                    // tokens per lane per chunk
-    static constexpr int DPL = D / 16;                    // dims per lane
-    static constexpr int CBMAX = CT / 8;                  // blocks per chunk at B = 8
-    static constexpr int ROW = D * ESZ;                   // bytes of one token row of one head
-    static constexpr int KV_BYTES = CT * ROW;             // bytes of K (or V) per chunk
-    static constexpr int Q_BYTES = D * sizeof(QT);
-    static constexpr int SC_BYTES = 0;
-    static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = KV_BYTES;
-    static constexpr int Q_OFF = 2 * KV_BYTES;
-    static constexpr int SC_OFF = Q_OFF + Q_BYTES;
-    static constexpr int META_OFF = SC_OFF + SC_BYTES;
-    static constexpr int STAGE = round_up(META_OFF + (int)sizeof(Meta), 128);
-    static constexpr int NC = Tune<ESZ>::NC ? Tune<ESZ>::NC
-                                            : (STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3));
-    // stages that fit beside the prefix table and the barriers
-    static constexpr int NSW_FIT = (227 * 1024 - 2 * kMaxBatch * 4 - 1024) / (NC * STAGE);
-    static constexpr int NSW = Tune<ESZ>::NSW ? Tune<ESZ>::NSW : (NSW_FIT > 4 ? 4 : NSW_FIT);
-    static_assert(NSW >= 2, "at least double buffering");
-    static constexpr int THREADS = (NC + 1) * 32;
-    static constexpr int BAR_OFF = NC * NSW * STAGE;
-    static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
-    static constexpr int SMEM = PREFIX_OFF + 2 * kMaxBatch * 4;
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    static_assert(NC <= 32 && (CT == 16 || CT == 32), "launch shape");
-    static_assert(Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && META_OFF % 16 == 0, "alignment");
-};
-
-struct AttnArgs {
-    char* kpool;           // written only by the fused append (the new token's slot)
-    char* vpool;
-    const float* kscale;
-    const float* vscale;
-    const void* q;
-    float* out;
-    const int32_t* tables;
-    const int32_t* lens;
-    float* part_ml;        // [batch*H*max_parts][2]  (m in log2 units, l)
-    float* part_o;         // [batch*H*max_parts][D]  unnormalised
-    unsigned* counter;
-    unsigned* arrivals;    // [batch*H] partitions finished per (sequence, head)
-    const char* k_new;     // fused append: [batch][H][D] new-token K (nullptr: no append)
-    const char* v_new;
-    int in_bytes;          // element size of k_new / v_new (2 or 4)
-    int* err;
-    int batch, H, B, max_blocks, ctx_limit, P, max_parts, num_blocks;
-    float qscale;          // scale * log2(e)
-};
-
-__device__ __forceinline__ int nparts_of(int ctx, int P) { return ctx <= P ? 1 : (ctx + P - 1) / P; }
-
-__device__ __forceinline__ float warp_max(float v) {
-    #pragma unroll
-    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-    #pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-    return v;
-}
-
-// d = a * b + c on two fp32 lanes at once (packed FFMA2, sm_100 family)
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// The lane's DPL consecutive elements of one token row, as DPL/2 float pairs.
-template <typename C>
-__device__ __forceinline__ void load_row(const char* row, int sub, float2 (&x)[C::DPL / 2]) {
-    const char* p = row + sub * C::DPL * C::ESZ;
-    if constexpr (C::ESZ == 4) {
-        #pragma unroll
-        for (int i = 0; i < C::DPL / 4; ++i) {
-            const float4 v = reinterpret_cast<const float4*>(p)[i];
-            x[2 * i] = make_float2(v.x, v.y);
-            x[2 * i + 1] = make_float2(v.z, v.w);
-        }
-    } else if constexpr (C::ESZ == 2) {
-        if constexpr (C::DPL == 8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(p);
-            x[0] = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-            x[1] = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-            x[2] = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
-            x[3] = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
-        } else {
-            const uint2 v = *reinterpret_cast<const uint2*>(p);
-            x[0] = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-            x[1] = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-        }
-    } else {
-        if constexpr (C::DPL == 8) {
-            const uint2 v = *reinterpret_cast<const uint2*>(p);
-            x[0] = e4m3x2_to_float2(static_cast<uint16_t>(v.x & 0xffffu));
-            x[1] = e4m3x2_to_float2(static_cast<uint16_t>(v.x >> 16));
-            x[2] = e4m3x2_to_float2(static_cast<uint16_t>(v.y & 0xffffu));
-            x[3] = e4m3x2_to_float2(static_cast<uint16_t>(v.y >> 16));
-        } else {
-            const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
-            x[0] = e4m3x2_to_float2(static_cast<uint16_t>(v & 0xffffu));
-            x[1] = e4m3x2_to_float2(static_cast<uint16_t>(v >> 16));
-        }
-    }
-}
-
-template <typename C>
-__device__ __forceinline__ void load_q(const char* qrow, int sub, float qs, float2 (&x)[C::DPL / 2]) {
-    using QT = typename C::QT;
-    const QT* p = reinterpret_cast<const QT*>(qrow) + sub * C::DPL;
-    #pragma unroll
-    for (int i = 0; i < C::DPL / 2; ++i)
-        x[i] = make_float2(static_cast<float>(p[2 * i]) * qs, static_cast<float>(p[2 * i + 1]) * qs);
-}
-
-struct __align__(16) Item {
-    int s, h, p, tok0, ntok, nchunks, single, valid, last;   // last: final partition
-};
-
-// (s, h, p) of compact item index `it` (items ordered by sequence, head, partition).
-template <int CT>
-__device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ctx, const int* s_end,
-                                            int batch, int H, int P) {
-    Item r{};
-    r.valid = it < n_items;
-    if (!r.valid) return r;
-    int lo = 0, hi = batch - 1;          // first s with s_end[s] > it
-    while (lo < hi) {
-        int mid = (lo + hi) >> 1;
-        if (s_end[mid] > it) hi = mid; else lo = mid + 1;
-    }
-    const int s = lo;
-    const int start = s ? s_end[s - 1] : 0;
-    const int ctx = s_ctx[s];
-    const int np = nparts_of(ctx, P);
-    const int rr = it - start;
-    r.s = s;
-    r.h = rr / np;
-    r.p = rr - r.h * np;
-    r.tok0 = r.p * P;
-    r.ntok = min(P, ctx - r.tok0);
-    r.nchunks = r.ntok > 0 ? (r.ntok + CT - 1) / CT : 1;
-    r.single = np == 1;
-    r.last = r.p == np - 1;
-    return r;
-}
-
-// Split-context merge of the np partials of one (sequence, head), by one warp:
-// M = max m_p, L = sum l_p 2^(m_p - M), out = sum o_p 2^(m_p - M) / L.
-// The partials were written by other SMs; they are read through L2 (ld.global.cg).
-template <int D>
-__device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh, int np, int lane) {
-    constexpr int DW = D / 32;
-    const int64_t base = sh * a.max_parts;
-    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + base;
-    float mx = -CUDART_INF_F;
-    for (int p = lane; p < np; p += 32) mx = fmaxf(mx, __ldcg(ml + p).x);
-    mx = warp_max(mx);
-    float L = 0.f, acc[DW];
-    #pragma unroll
-    for (int i = 0; i < DW; ++i) acc[i] = 0.f;
-    #pragma unroll 4
-    for (int p = 0; p < np; ++p) {
-        const float2 v = __ldcg(ml + p);
-        const float wgt = ex2_approx(v.x - mx);
-        L = fmaf(v.y, wgt, L);
-        const float* o = a.part_o + (base + p) * D + lane * DW;
-        if constexpr (DW == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
-            acc[0] = fmaf(wgt, x.x, acc[0]); acc[1] = fmaf(wgt, x.y, acc[1]);
-            acc[2] = fmaf(wgt, x.z, acc[2]); acc[3] = fmaf(wgt, x.w, acc[3]);
-        } else {
-            const float2 x = __ldcg(reinterpret_cast<const float2*>(o));
-            acc[0] = fmaf(wgt, x.x, acc[0]); acc[1] = fmaf(wgt, x.y, acc[1]);
-        }
-    }
-    const float inv = 1.f / L;
-    float* out = a.out + sh * D + lane * DW;
-    #pragma unroll
-    for (int i = 0; i < DW; ++i) out[i] = acc[i] * inv;
-}
-
-// Fused append: lane's D/32 elements of one new-token row (src, in_bytes per element)
-// are converted to the pool type (FP8: RNE-satfinite(x / scale)) and written both into
-// the consumer's stage row and into the pool slot, so the attention below sees exactly
-// the bytes a separate kv_append would have stored.
-template <typename C>
-__device__ __forceinline__ void patch_row(const char* src, int in_bytes, char* srow, char* grow,
-                                          float scale, int lane) {
-    constexpr int DW = C::D / 32;
-    const int e0 = lane * DW;
-    if constexpr (C::ESZ == 4) {
-        static_assert(DW == 4 || DW == 2, "head_dim 64 or 128");
-        if constexpr (DW == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src + e0 * 4);
-            *reinterpret_cast<float4*>(srow + e0 * 4) = v;
-            *reinterpret_cast<float4*>(grow + e0 * 4) = v;
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(src + e0 * 4);
-            *reinterpret_cast<float2*>(srow + e0 * 4) = v;
-            *reinterpret_cast<float2*>(grow + e0 * 4) = v;
-        }
-    } else if constexpr (C::ESZ == 2) {
-        if constexpr (DW == 4) {
-            const uint2 v = *reinterpret_cast<const uint2*>(src + e0 * 2);
-            *reinterpret_cast<uint2*>(srow + e0 * 2) = v;
-            *reinterpret_cast<uint2*>(grow + e0 * 2) = v;
-        } else {
-            const uint32_t v = *reinterpret_cast<const uint32_t*>(src + e0 * 2);
-            *reinterpret_cast<uint32_t*>(srow + e0 * 2) = v;
-            *reinterpret_cast<uint32_t*>(grow + e0 * 2) = v;
-        }
-    } else {
-        float x[DW];
-        #pragma unroll
-        for (int i = 0; i < DW; ++i)
-            x[i] = in_bytes == 2 ? __half2float(reinterpret_cast<const __half*>(src)[e0 + i])
-                                 : reinterpret_cast<const float*>(src)[e0 + i];
-        uint16_t q[DW / 2];
-        #pragma unroll
-        for (int i = 0; i < DW / 2; ++i)
-            q[i] = float2_to_e4m3x2(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
-        if constexpr (DW == 4) {
-            const uint32_t v = static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 16);
-            *reinterpret_cast<uint32_t*>(srow + e0) = v;
-            *reinterpret_cast<uint32_t*>(grow + e0) = v;
-        } else {
-            *reinterpret_cast<uint16_t*>(srow + e0) = q[0];
-            *reinterpret_cast<uint16_t*>(grow + e0) = q[0];
-        }
-    }
-}
-
-template <typename C>
-__global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(AttnArgs a) {
-    constexpr int NC = C::NC, NSW = C::NSW, D = C::D, CT = C::CT, TPL = C::TPL, DPL = C::DPL;
-    constexpr int CBMAX = C::CBMAX;
-    extern __shared__ __align__(128) char smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);   // full[NC*NSW], empty[NC*NSW]
-    int* s_ctx = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
-    int* s_end = s_ctx + kMaxBatch;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // ---- prologue: clamp lengths, items per sequence, inclusive prefix
-    for (int s = tid; s < a.batch; s += C::THREADS) {
-        int c = a.lens[s];
-        if (c < 0 || c > a.ctx_limit) {
-            if (blockIdx.x == 0) atomicOr(a.err, KV_DEVERR_CONTEXT);
-            c = c < 0 ? 0 : a.ctx_limit;
-        }
-        s_ctx[s] = c;
-        s_end[s] = a.H * nparts_of(c, a.P);
-    }
-    if (tid == 0) {
-        for (int i = 0; i < 2 * NC * NSW; ++i) mbar_init(smem_u32(&bars[i]), 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int carry = 0;
-        for (int base = 0; base < a.batch; base += 32) {
-            int v = base + lane < a.batch ? s_end[base + lane] : 0;
-            #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int n = __shfl_up_sync(FULL, v, o);
-                if (lane >= o) v += n;
-            }
-            v += carry;
-            if (base + lane < a.batch) s_end[base + lane] = v;
-            carry = __shfl_sync(FULL, v, 31);
-        }
-    }
-    __syncthreads();
-    const int n_items = s_end[a.batch - 1];
-
-    auto full_bar = [&](int w, int st) { return smem_u32(&bars[w * NSW + st]); };
-    auto empty_bar = [&](int w, int st) { return smem_u32(&bars[NC * NSW + w * NSW + st]); };
-    auto stage_ptr = [&](int w, int st) { return smem + (w * NSW + st) * C::STAGE; };
-
-    if (warp == NC) {
-        // ================================================================ producer
-        // Lane w feeds consumer w; lanes >= NC only take part in warp votes.
-        const bool mine = lane < NC;
-        const int w = mine ? lane : 0;
-        const int rpc = a.B < CT ? a.B : CT;           // token rows per copy (whole block if B <= CT)
-        const uint32_t tile = static_cast<uint32_t>(rpc) * C::ROW;
-        unsigned pending = 0;                          // next item index (atomic in flight)
-        if (mine) pending = atomicAdd(a.counter, 1u);
-        auto take = [&]() {
-            const int idx = static_cast<int>(pending);
-            pending = atomicAdd(a.counter, 1u);
-            return decode_item<CT>(idx, n_items, s_ctx, s_end, a.batch, a.H, a.P);
-        };
-        int ids[CBMAX];
-        auto load_ids = [&](const Item& it, int chunk) {
-            const int nt = it.valid ? min(CT, it.ntok - chunk * CT) : 0;
-            const int ncp = nt > 0 ? (nt + rpc - 1) / rpc : 0;
-            const int64_t row = static_cast<int64_t>(it.s) * a.max_blocks;
-            const int t0 = it.tok0 + chunk * CT;
-            #pragma unroll
-            for (int j = 0; j < CBMAX; ++j) ids[j] = j < ncp ? a.tables[row + (t0 + j * rpc) / a.B] : 0;
-        };
-        Item cur{}, nxt{};
-        int c = 0, fills = 0;
-        bool alive = mine;
-        if (mine) {
-            cur = take();
-            if (cur.valid) nxt = take();
-            load_ids(cur, 0);
-        }
-        bool failed = false;
-        uint64_t idle_since = 0;
-        while (__any_sync(FULL, alive) && !failed) {
-            const int st = fills % NSW;
-            bool ready = false;
-            if (alive) ready = mbar_test_wait(empty_bar(w, st), ((fills / NSW) & 1) ^ 1);
-            if (ready) {
-                char* stg = stage_ptr(w, st);
-                Meta* meta = reinterpret_cast<Meta*>(stg + C::META_OFF);
-                const uint32_t fb = full_bar(w, st);
-                if (!cur.valid) {
-                    meta->flags = F_TERM;
-                    mbar_arrive(fb);
-                    alive = false;
-                } else {
-                    const int nt = min(CT, cur.ntok - c * CT);     // 0 only for an empty sequence
-                    const int nblk = nt > 0 ? (nt + rpc - 1) / rpc : 0;   // copies of this chunk
-                    const int row0 = (cur.tok0 + c * CT) % a.B;   // first row inside the block
-                    #pragma unroll
-                    for (int j = 0; j < CBMAX; ++j) {
-                        if (j < nblk && (ids[j] < 0 || ids[j] >= a.num_blocks)) {
-                            atomicOr(a.err, KV_DEVERR_BLOCK_ID);
-                            ids[j] = 0;
-                        }
-                    }
-                    const bool with_q = (c == 0) && nt > 0;
-                    const uint32_t bytes = nblk * 2 * tile + (with_q ? C::Q_BYTES : 0);
-                    meta->s = cur.s;
-                    meta->h = cur.h;
-                    meta->p = cur.p;
-                    meta->ntok = nt;
-                    // fused append: the sequence's newest token is the last row of the
-                    // last chunk of its last partition
-                    const bool patch = a.k_new != nullptr && cur.last && c == cur.nchunks - 1 && nt > 0;
-                    meta->flags = (c == 0 ? F_FIRST : 0) | (c == cur.nchunks - 1 ? F_LAST : 0) |
-                                  (cur.single ? F_SINGLE : 0) | (patch ? F_PATCH : 0);
-                    if (patch) {
-                        const int r = nt - 1, jr = r / rpc;
-                        int pid = ids[0];
-                        #pragma unroll
-                        for (int j = 1; j < CBMAX; ++j) if (j == jr) pid = ids[j];
-                        meta->patch_row = r;
-                        meta->patch_id = pid;
-                        meta->patch_off = row0 + r % rpc;
-                    }
-                    #pragma unroll
-                    for (int j = 0; j < CBMAX; ++j) meta->ids[j] = ids[j];
-                    if (bytes) mbar_arrive_expect_tx(fb, bytes);
-                    else mbar_arrive(fb);
-                    const uint32_t dst = smem_u32(stg);
-                    #pragma unroll
-                    for (int j = 0; j < CBMAX; ++j) {
-                        if (j < nblk) {
-                            const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h) * a.B +
-                                                  row0) * C::ROW;
-                            bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
-                            bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
-                        }
-                    }
-                    if (with_q) {
-                        const char* qsrc = static_cast<const char*>(a.q) +
-                                           (static_cast<int64_t>(cur.s) * a.H + cur.h) * C::Q_BYTES;
-                        bulk_g2s(dst + C::Q_OFF, qsrc, C::Q_BYTES, fb);
-                    }
-                    if (++c == cur.nchunks) {
-                        cur = nxt;
-                        c = 0;
-                        nxt = Item{};
-                        if (cur.valid) nxt = take();
-                    }
-                    load_ids(cur, c);                  // used at this lane's next fill
-                }
-                ++fills;
-            }
-            // watchdog: no stage became free anywhere for about a second -> give up
-            if (__any_sync(FULL, ready)) {
-                idle_since = 0;
-            } else {
-                const uint64_t now = global_timer_ns();
-                if (idle_since == 0) idle_since = now;
-                else if (now - idle_since > kWaitLimitNs) {
-                    if (lane == 0) atomicOr(a.err, KV_DEVERR_TIMEOUT);
-                    failed = true;
-                }
-                __nanosleep(32);
-            }
-        }
-        // Drain: every fill this lane issued has landed before the CTA may exit.
-        if (mine) {
-            for (int st = 0; st < NSW && st < fills; ++st) {
-                const int last = fills - 1 - ((fills - 1 - st) % NSW);
-                mbar_wait_bounded(full_bar(w, st), (last / NSW) & 1, a.err);
-            }
-        }
-        return;
-    }
-
-    // ==================================================================== consumer
-    const int w = warp;
-    const int half = lane >> 4;                 // which token of each row pair
-    const int sub = lane & 15;                  // which DPL-element slice of the row
-    const int tok_l = 2 * (lane & (TPL - 1)) + half;     // token whose score this lane holds
-    const bool primary = (lane & 15) < TPL;              // one holder per token when CT = 16
-    float2 q2[DPL / 2], acc[DPL / 2];
-    float m = -CUDART_INF_F, lsum = 0.f;
-    #pragma unroll
-    for (int i = 0; i < DPL / 2; ++i) { q2[i] = make_float2(0.f, 0.f); acc[i] = make_float2(0.f, 0.f); }
-
-    for (int j = 0;; ++j) {
-        const int st = j % NSW;
-        const uint32_t par = (j / NSW) & 1;
-        const uint32_t fb = full_bar(w, st);
-        if (!mbar_wait_bounded(fb, par, a.err)) {
-            mbar_wait_bounded(fb, par, a.err);      // let copies in flight land, then leave
-            break;
-        }
-        const char* stg = stage_ptr(w, st);
-        struct { int s, h, p, ntok, flags; } meta;
-        {
-            const int4 m0 = *reinterpret_cast<const int4*>(stg + C::META_OFF);
-            meta.s = m0.x; meta.h = m0.y; meta.p = m0.z; meta.ntok = m0.w;
-            meta.flags = reinterpret_cast<const Meta*>(stg + C::META_OFF)->flags;
-        }
-        if (meta.flags & F_TERM) break;
-        const int nt = meta.ntok;
-        if (meta.flags & F_FIRST) {
-            m = -CUDART_INF_F;
-            lsum = 0.f;
-            #pragma unroll
-            for (int i = 0; i < DPL / 2; ++i) acc[i] = make_float2(0.f, 0.f);
-            if (nt > 0) load_q<C>(stg + C::Q_OFF, sub, a.qscale, q2);
-        }
-        if (meta.flags & F_PATCH) {
-            // this warp owns the stage now: put the new token into its row and its slot
-            const Meta* mp = reinterpret_cast<const Meta*>(stg + C::META_OFF);
-            const int r = mp->patch_row;
-            const int64_t sh = static_cast<int64_t>(meta.s) * a.H + meta.h;
-            const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + meta.h) * a.B + mp->patch_off;
-            float ksc = 1.f, vsc = 1.f;
-            if constexpr (C::FP8) {
-                ksc = __ldg(a.kscale + mp->patch_id);
-                vsc = __ldg(a.vscale + mp->patch_id);
-            }
-            char* srow = const_cast<char*>(stg);
-            patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, srow + C::K_OFF + r * C::ROW,
-                         a.kpool + grow * C::ROW, ksc, lane);
-            patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, srow + C::V_OFF + r * C::ROW,
-                         a.vpool + grow * C::ROW, vsc, lane);
-            // the stage is refilled by the TMA engine later: order these generic writes first
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-        }
-        if (nt > 0) {
-            float ks = 1.f, vs = 1.f;
-            if constexpr (C::FP8) {
-                // per-block scales of this lane's token, loaded now and used after the dot
-                // products; the producer validated the ids
-                const int id = reinterpret_cast<const Meta*>(stg + C::META_OFF)
-                                   ->ids[tok_l / (a.B < CT ? a.B : CT)];
-                ks = __ldg(a.kscale + id);
-                vs = __ldg(a.vscale + id);
-            }
-            const char* K = stg + C::K_OFF + half * C::ROW;
-            const char* V = stg + C::V_OFF + half * C::ROW;
-            float part[TPL];
-            #pragma unroll
-            for (int i = 0; i < TPL; ++i) {          // token 2i + half
-                float2 kx[DPL / 2];
-                load_row<C>(K + 2 * i * C::ROW, sub, kx);
-                float2 d2 = make_float2(0.f, 0.f);
-                #pragma unroll
-                for (int u = 0; u < DPL / 2; ++u) d2 = ffma2(q2[u], kx[u], d2);
-                part[i] = d2.x + d2.y;
-            }
-            // transpose-reduce over the 16 lanes of each half: lane ends with token tok_l
-            #pragma unroll
-            for (int off = TPL / 2; off >= 1; off >>= 1) {
-                const bool upper = (lane & off) != 0;
-                #pragma unroll
-                for (int i = 0; i < off; ++i) {
-                    const float send = upper ? part[i] : part[i + off];
-                    const float keep = upper ? part[i + off] : part[i];
-                    part[i] = keep + __shfl_xor_sync(FULL, send, off);
-                }
-            }
-            float x = part[0];
-            #pragma unroll
-            for (int off = TPL; off < 16; off <<= 1) x += __shfl_xor_sync(FULL, x, off);
-            if constexpr (C::FP8) x *= ks;
-            x = tok_l < nt ? x : -CUDART_INF_F;
-            if (__any_sync(FULL, x > m + 8.f)) {      // raise the running max only when needed
-                const float m_new = fmaxf(m, warp_max(x));
-                const float corr = ex2_approx(m - m_new);
-                lsum *= corr;
-                #pragma unroll
-                for (int i = 0; i < DPL / 2; ++i) { acc[i].x *= corr; acc[i].y *= corr; }
-                m = m_new;
-            }
-            const float pr = ex2_approx(x - m);
-            if (primary) lsum += pr;
-            const float pv = pr * vs;
-            #pragma unroll
-            for (int i = 0; i < TPL; ++i) {          // token 2i + half, its p from lane i (+16)
-                const float pt = __shfl_sync(FULL, pv, i + (lane & 16));
-                if (nt == CT || 2 * i + half < nt) {
-                    float2 vx[DPL / 2];
-                    load_row<C>(V + 2 * i * C::ROW, sub, vx);
-                    const float2 p2 = make_float2(pt, pt);
-                    #pragma unroll
-                    for (int u = 0; u < DPL / 2; ++u) acc[u] = ffma2(p2, vx[u], acc[u]);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(w, st));
-        if (meta.flags & F_LAST) {
-            const float l = warp_sum(lsum);
-            float2 o[DPL / 2];
-            #pragma unroll
-            for (int i = 0; i < DPL / 2; ++i) {       // the two halves saw different tokens
-                o[i].x = acc[i].x + __shfl_xor_sync(FULL, acc[i].x, 16);
-                o[i].y = acc[i].y + __shfl_xor_sync(FULL, acc[i].y, 16);
-            }
-            const int64_t sh = static_cast<int64_t>(meta.s) * a.H + meta.h;
-            if (meta.flags & F_SINGLE) {
-                if (half == 0) {
-                    float2* dst = reinterpret_cast<float2*>(a.out + sh * D + sub * DPL);
-                    const float inv = nt > 0 ? 1.f / l : 0.f;   // empty sequence -> zeros
-                    #pragma unroll
-                    for (int i = 0; i < DPL / 2; ++i)
-                        dst[i] = nt > 0 ? make_float2(o[i].x * inv, o[i].y * inv) : make_float2(0.f, 0.f);
-                }
-            } else {
-                const int64_t idx = sh * a.max_parts + meta.p;
-                if (lane == 0) {
-                    a.part_ml[2 * idx] = m;
-                    a.part_ml[2 * idx + 1] = l;
-                }
-                if (half == 0) {
-                    float2* dst = reinterpret_cast<float2*>(a.part_o + idx * D + sub * DPL);
-                    #pragma unroll
-                    for (int i = 0; i < DPL / 2; ++i) dst[i] = o[i];
-                }
-                // publish the partial, then take a ticket; the last partition merges
-                __threadfence();
-                __syncwarp();
-                unsigned prev = 0;
-                if (lane == 0) prev = atomicAdd(a.arrivals + sh, 1u);
-                prev = __shfl_sync(FULL, prev, 0);
-                const int np = nparts_of(s_ctx[meta.s], a.P);
-                if (prev == static_cast<unsigned>(np - 1)) {
-                    __threadfence();
-                    merge_partials<D>(a, sh, np, lane);
-                }
-            }
-        }
-    }
-}
-
-template <typename C>
-int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsigned* counters,
-                 cudaStream_t stream) {
-    // the shared-memory opt-in is a per-device function attribute
-    static unsigned long long attr_done = 0;
-    const unsigned long long bit = 1ull << (pool->device & 63);
-    if (!(attr_done & bit)) {
-        if (cudaFuncSetAttribute(attention_partition_kernel<C>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return KV_ERR_CUDA;
-        attr_done |= bit;
-    }
-    const int total = args.batch;
-    const size_t qrow = static_cast<size_t>(args.H) * C::D * sizeof(typename C::QT);
-    for (int s0 = 0, sub = 0; s0 < total; s0 += kMaxBatch, ++sub) {
-        AttnArgs sa = args;
-        sa.batch = total - s0 < kMaxBatch ? total - s0 : kMaxBatch;
-        sa.q = static_cast<const char*>(args.q) + s0 * qrow;
-        sa.out = args.out + static_cast<int64_t>(s0) * args.H * C::D;
-        sa.tables = args.tables + static_cast<int64_t>(s0) * args.max_blocks;
-        sa.lens = args.lens + s0;
-        if (args.k_new) {
-            const int64_t nofs = static_cast<int64_t>(s0) * args.H * C::D * args.in_bytes;
-            sa.k_new = args.k_new + nofs;
-            sa.v_new = args.v_new + nofs;
-        }
-        const int64_t pofs = static_cast<int64_t>(s0) * args.H * args.max_parts;
-        if (args.part_ml) {
-            sa.part_ml = args.part_ml + 2 * pofs;
-            sa.part_o = args.part_o + pofs * C::D;
-            sa.arrivals = args.arrivals + static_cast<int64_t>(s0) * args.H;
-        }
-        sa.counter = counters + sub;
-        const int64_t upper = static_cast<int64_t>(sa.batch) * args.H * args.max_parts;
-        int64_t grid = (upper + C::NC - 1) / C::NC;
-        if (grid > pool->num_sms) grid = pool->num_sms;
-        if (grid < 1) grid = 1;
-        attention_partition_kernel<C><<<static_cast<int>(grid), C::THREADS, C::SMEM, stream>>>(sa);
-        if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
-    }
-    (void)plan;
-    return KV_OK;
-}
-
 template <typename C>
 int consumers_of() { return C::NC; }
 
-int consumers_for(const kv_pool_desc& d) {
-    if (d.dtype == KV_F32) return d.head_dim == 128 ? consumers_of<Cfg<128, float, float>>()
-                                                    : consumers_of<Cfg<64, float, float>>();
-    if (d.dtype == KV_F16) return d.head_dim == 128 ? consumers_of<Cfg<128, __half, __half>>()
-                                                    : consumers_of<Cfg<64, __half, __half>>();
-    return d.head_dim == 128 ? consumers_of<Cfg<128, uint8_t, __half>>()
-                             : consumers_of<Cfg<64, uint8_t, __half>>();
+template <int G>
+int consumers_for_g(const kv_pool_desc& d) {
+    if constexpr (G == 1) {                        // fp32 pools have no grouped path
+        if (d.dtype == KV_F32) return d.head_dim == 128 ? consumers_of<Cfg<128, float, float>>()
+                                                        : consumers_of<Cfg<64, float, float>>();
+    }
+    if (d.dtype == KV_F16) return d.head_dim == 128 ? consumers_of<Cfg<128, __half, __half, G>>()
+                                                    : consumers_of<Cfg<64, __half, __half, G>>();
+    return d.head_dim == 128 ? consumers_of<Cfg<128, uint8_t, __half, G>>()
+                             : consumers_of<Cfg<64, uint8_t, __half, G>>();
+}
+
+int consumers_for(const kv_pool_desc& d, int group) {
+    switch (group) {
+        case 2: return consumers_for_g<2>(d);
+        case 4: return consumers_for_g<4>(d);
+        case 8: return consumers_for_g<8>(d);
+        default: return consumers_for_g<1>(d);
+    }
 }
 
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
+bool valid_group(const kv_pool_desc& d, int group) {
+    if (group == 1) return true;
+    return (group == 2 || group == 4 || group == 8) && d.dtype != KV_F32;
+}
+
 int plan_attention(const kv_pool* pool, int batch, int max_context, int partition_tokens,
-                   AttnPlan* plan) {
+                   AttnPlan* plan, int group) {
     const kv_pool_desc& d = pool->desc;
     if (batch < 0 || max_context < 0 || batch > kMaxBatch * kMaxSub) return KV_ERR_INVALID_ARG;
+    if (!valid_group(d, group)) return KV_ERR_INVALID_ARG;
     const int cap = 32 * d.block_size;             // one producer lane per block of a partition
-    const int nc = consumers_for(d);
+    const int nc = consumers_for(d, group);
     int P;
     if (partition_tokens > 0) {
         if (partition_tokens % kPartAlign != 0 || partition_tokens > cap) return KV_ERR_INVALID_ARG;
         P = partition_tokens;
     } else if (partition_tokens == 0) {
+        // work items are (sequence, KV head, partition): aim at >= 8 per consumer warp
         const int64_t units = static_cast<int64_t>(batch > 0 ? batch : 1) * d.num_heads;
-        const int64_t target = 8ll * pool->num_sms * nc;     // >= 8 items per consumer warp
+        const int64_t target = 8ll * pool->num_sms * nc;
         int64_t parts = (target + units - 1) / units;
         if (parts < 1) parts = 1;
         int64_t p = (max_context + parts - 1) / parts;
@@ -753,9 +68,10 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     plan->partition = P;
     plan->max_parts = max_context <= P ? 1 : (max_context + P - 1) / P;
     plan->consumers = nc;
+    plan->group = group;
     size_t ws = 256;                                // kMaxSub work counters
     if (plan->max_parts > 1) {
-        const size_t n = static_cast<size_t>(batch) * d.num_heads * plan->max_parts;
+        const size_t n = static_cast<size_t>(batch) * d.num_heads * group * plan->max_parts;
         ws += align256(static_cast<size_t>(batch) * d.num_heads * sizeof(unsigned));   // arrivals
         ws += align256(n * 2 * sizeof(float));
         ws += align256(n * d.head_dim * sizeof(float));
@@ -778,11 +94,12 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
                             float scale, const AttnPlan& plan, void* workspace, cudaStream_t stream) {
     const kv_pool_desc& d = pool->desc;
     if (batch == 0) return KV_OK;
+    const int group = plan.group;
     char* ws = static_cast<char*>(workspace);
     unsigned* counters = reinterpret_cast<unsigned*>(ws);
     const size_t arrivals_bytes =
         plan.max_parts > 1 ? align256(static_cast<size_t>(batch) * d.num_heads * sizeof(unsigned)) : 0;
-    // work counters and per-(sequence, head) arrival counters start at zero every call
+    // work counters and per-(sequence, KV head) arrival counters start at zero every call
     if (cudaMemsetAsync(counters, 0, 256 + arrivals_bytes, stream) != cudaSuccess) return KV_ERR_CUDA;
 
     AttnArgs a{};
@@ -798,7 +115,7 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     a.tables = block_tables;
     a.lens = context_lens;
     if (plan.max_parts > 1) {
-        const size_t n = static_cast<size_t>(batch) * d.num_heads * plan.max_parts;
+        const size_t n = static_cast<size_t>(batch) * d.num_heads * group * plan.max_parts;
         a.arrivals = reinterpret_cast<unsigned*>(ws + 256);
         a.part_ml = reinterpret_cast<float*>(ws + 256 + arrivals_bytes);
         a.part_o = reinterpret_cast<float*>(ws + 256 + arrivals_bytes + align256(n * 2 * sizeof(float)));
@@ -815,6 +132,7 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     a.num_blocks = d.num_blocks;
     a.qscale = scale * 1.4426950408889634f;        // log2(e): softmax evaluated with 2^x
 
+    if (group != 1) return launch_attention_grouped(group, pool, a, plan, counters, stream);
     if (d.dtype == KV_F32) {
         if (d.head_dim == 128) return launch_typed<Cfg<128, float, float>>(pool, a, plan, counters, stream);
         return launch_typed<Cfg<64, float, float>>(pool, a, plan, counters, stream);

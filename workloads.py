@@ -22,6 +22,8 @@ pages "KV缓存机制解析" §3.1 and "KV Cache与PagedAttention" §1.1):
             prompt, each decodes 128 tokens.
   ragged    256 sequences, lengths floor(exp(U(ln 16, ln 16384))), 32 heads,
             d 128, fp16 (and an FP8-E4M3 pool variant), B in {8, 16, 32}.
+  gqa70b    80 layers, 64 query heads over 8 K/V heads (LLaMA-2-70B shape), d 128, fp16,
+            B 16, batch 32, every length 4096.
 """
 
 from __future__ import annotations
@@ -46,6 +48,11 @@ class Workload:
     num_blocks: int = 0
     scale: float = 0.0
     steps: int = 1
+    num_q_heads: int = 0            # query heads (0: same as num_heads; more = grouped-query)
+
+    @property
+    def q_heads(self) -> int:
+        return self.num_q_heads or self.num_heads
 
     @property
     def elem_bytes(self) -> int:
@@ -97,6 +104,14 @@ def ragged(block_size: int = 16) -> Workload:
                     num_blocks=need + need // 10, scale=1.0 / math.sqrt(128))
 
 
+def gqa70b(num_layers: int = 80) -> Workload:
+    """LLaMA-2-70B-shaped grouped-query layer stack: 64 query heads share 8 K/V heads,
+    d 128, fp16, B 16, batch 32, every context 4096 after the decode append."""
+    return Workload("gqa70b", seed=6, num_layers=num_layers, num_heads=8, head_dim=128, block_size=16,
+                    dtype="f16", batch=32, lens=[4096] * 32, num_blocks=32 * 256,
+                    scale=1.0 / math.sqrt(128), num_q_heads=64)
+
+
 PROMPT_LEN_PARALLEL = 1030
 CANDIDATES_PARALLEL = 8
 
@@ -129,9 +144,9 @@ def host_tokens(w: Workload, seq: int, n_tokens: int, kind: str) -> np.ndarray:
 
 
 def host_queries(w: Workload, step: int = 0, layer: int = 0) -> np.ndarray:
-    """N(0,1) queries ``[batch, H, d]`` for one decode step of one layer."""
+    """N(0,1) queries ``[batch, Hq, d]`` for one decode step of one layer."""
     rng = np.random.default_rng([w.seed, 1_000_000 + step, layer])
-    x = rng.standard_normal((w.batch, w.num_heads, w.head_dim), dtype=np.float32)
+    x = rng.standard_normal((w.batch, w.q_heads, w.head_dim), dtype=np.float32)
     return x.astype(_np_dtype(w.dtype))
 
 
