@@ -153,3 +153,17 @@ def decode_attention_gqa(q, k_seqs, v_seqs, scale: float) -> np.ndarray:
         for j in range(Hq):
             out[s, j] = decode_attention_one(q[s, j], Ks[:, j // G, :], Vs[:, j // G, :], scale)
     return out
+
+
+def decode_attention_window(q, k_seqs, v_seqs, scale: float, window: int) -> np.ndarray:
+    """Sliding-window decode ([KV缓存机制解析] §8, 滚动窗口缓存: keep only the most recent
+    WINDOW_SIZE tokens): each query attends to the last ``window`` cached tokens of its
+    sequence (all of them when the context is shorter).  ``window <= 0`` means no window.
+    Query heads may be grouped over K/V heads as in ``decode_attention_gqa``."""
+    ks, vs = [], []
+    for K, V in zip(k_seqs, v_seqs):
+        n = np.asarray(K).shape[0]
+        lo = max(0, n - window) if window > 0 else 0
+        ks.append(np.asarray(K)[lo:])
+        vs.append(np.asarray(V)[lo:])
+    return decode_attention_gqa(q, ks, vs, scale)

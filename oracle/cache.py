@@ -120,7 +120,8 @@ class BlockManager:
         self.tables[sid] = list(self.tables[parent])
         self.lens[sid] = self.lens[parent]
         for blk in self.tables[sid]:
-            self.ref[blk] += 1
+            if blk >= 0:
+                self.ref[blk] += 1
         return sid
 
     def append_slot(self, sid: int):
@@ -167,9 +168,23 @@ class BlockManager:
         cow = 1 if (n % self.B != 0 and self.ref[self.tables[sid][-1]] > 1) else 0
         return new_blocks + cow
 
+    def trim(self, sid: int, keep_from: int) -> list:
+        """Sliding window: release every block that lies wholly before token ``keep_from``
+        (its table entry becomes -1; later entries keep their logical positions).
+        Returns the released block ids."""
+        table = self.tables[sid]
+        released = []
+        for j in range(min(keep_from // self.B, len(table))):
+            if table[j] >= 0:
+                released.append(table[j])
+                self._release(table[j])
+                table[j] = -1
+        return released
+
     def free_seq(self, sid: int) -> None:
         for blk in self.tables.pop(sid):
-            self._release(blk)
+            if blk >= 0:
+                self._release(blk)
         del self.lens[sid]
 
     # -- views

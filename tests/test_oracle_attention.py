@@ -291,3 +291,26 @@ def test_gqa_matches_torch_sdpa_enable_gqa():
         torch.from_numpy(q[0]).view(1, Hkv * G, 1, d), torch.from_numpy(k).permute(1, 0, 2)[None],
         torch.from_numpy(v).permute(1, 0, 2)[None], enable_gqa=True).view(Hkv * G, d).numpy()
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- sliding window
+
+def test_window_closed_forms():
+    rng = np.random.default_rng(520)
+    H, d, lens = 2, 16, [1, 5, 40]
+    q = rng.standard_normal((3, H, d))
+    ks = [rng.standard_normal((n, H, d)) for n in lens]
+    vs = [rng.standard_normal((n, H, d)) for n in lens]
+    full = A.decode_attention(q, ks, vs, 0.25)
+    # a window at least as long as every context, or none, changes nothing
+    assert np.array_equal(A.decode_attention_window(q, ks, vs, 0.25, 40), full)
+    assert np.array_equal(A.decode_attention_window(q, ks, vs, 0.25, 0), full)
+    # a window of one token returns that token's value row exactly
+    w1 = A.decode_attention_window(q, ks, vs, 0.25, 1)
+    for s, n in enumerate(lens):
+        assert np.array_equal(w1[s], vs[s][n - 1])
+    # window W equals full attention over the last W rows, and differs from the full context
+    w7 = A.decode_attention_window(q, ks, vs, 0.25, 7)
+    np.testing.assert_allclose(w7[2], A.decode_attention(q[2:], [ks[2][-7:]], [vs[2][-7:]], 0.25)[0],
+                               rtol=0, atol=0)
+    assert not np.allclose(w7[2], full[2])

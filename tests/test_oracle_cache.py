@@ -185,3 +185,19 @@ def test_fp8_append_uses_the_block_scale():
     assert np.array_equal(kc[1, :, 2], fp8.quantize(k[0], ks[1]))
     assert np.array_equal(vc[3, :, 7], fp8.quantize(v[1], vs[3]))
     assert math.isclose(float(fp8.decode(kc[1, 0, 2, 0])) * 0.01, float(k[0, 0, 0]), rel_tol=0.07)
+
+
+def test_trim_releases_only_blocks_wholly_before_the_window():
+    m = C.BlockManager(num_blocks=20, block_size=8)
+    s = m.new_seq()
+    m.append_slots(s, 45)                    # 6 blocks, the last with 5 tokens
+    t = m.table(s)
+    released = m.trim(s, 45 - 20)            # keep tokens 25..44: blocks 0..2 (tokens 0..23) go
+    assert released == t[:3] and m.table(s)[:3] == [-1, -1, -1] and m.table(s)[3:] == t[3:]
+    assert m.used_blocks() == 3 and m.lens[s] == 45
+    assert m.trim(s, 25) == []               # idempotent
+    c = m.fork(s)                            # a fork shares only the live blocks
+    assert all(m.ref[b] == 2 for b in t[3:])
+    m.free_seq(s)
+    m.free_seq(c)
+    assert m.used_blocks() == 0 and all(r == 0 for r in m.ref)
