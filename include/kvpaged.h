@@ -222,6 +222,44 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
                                       float scale, int partition_tokens, void* workspace,
                                       size_t workspace_bytes, kv_stream_t stream);
 
+/* Every option of one decode-attention launch in one struct (field meanings as in the
+ * entry points above).
+ *   num_q_heads  0 = the pool's num_heads; else a multiple (grouped-query, as
+ *                paged_decode_attention_gqa).
+ *   k_new, v_new NULL, or the newest token's K/V (fused append, as
+ *                paged_decode_attention_append; in_dtype ignored when NULL).
+ *   window       0 = the whole context; W > 0: sliding-window decode — each query attends
+ *                only to the last W tokens of its sequence (all of them when shorter), as the
+ *                rolling-window cache of [KV缓存机制解析] §8 keeps the most recent tokens.
+ *                Blocks lying wholly before position context_len - W are never read, so the
+ *                host may release them (kv_alloc_seq_trim) and leave their table entries -1. */
+typedef struct {
+    int layer;
+    const void* q;
+    int num_q_heads;
+    const void* k_new;
+    const void* v_new;
+    kv_dtype in_dtype;
+    float* out;
+    const int32_t* block_tables;
+    int max_blocks_per_seq;
+    const int32_t* context_lens;
+    int batch;
+    int max_context;
+    int window;
+    float scale;
+    int partition_tokens;
+    void* workspace;
+    size_t workspace_bytes;
+    kv_stream_t stream;
+} kv_decode_args;
+
+/* Workspace bytes for paged_decode_attention_ex with these arguments (0 on invalid ones). */
+KV_API size_t paged_decode_workspace_size_ex(const kv_pool* pool, const kv_decode_args* args);
+
+/* Decode attention with every option of kv_decode_args; errors as paged_decode_attention. */
+KV_API int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* args);
+
 /* Size of the library's fixed device scratch array used by paged_decode_attention_static. */
 #define KV_STATIC_SCRATCH_BYTES (16u << 20)
 
@@ -276,6 +314,12 @@ KV_API int kv_alloc_seq_fork(kv_alloc* a, int parent, int* child);
  * the free list is too short for the whole request. */
 KV_API int kv_alloc_append_slots(kv_alloc* a, int seq, int count, int64_t* slots_out,
                           int32_t* cow_pair_out);
+
+/* Sliding window: release every block of `seq` that lies wholly before token keep_from
+ * (count - 1, back to the free list at 0) and set its table entry to -1; later entries
+ * keep their logical positions and the length is unchanged.  *released (may be NULL)
+ * receives the number of table entries cleared.  Idempotent. */
+KV_API int kv_alloc_seq_trim(kv_alloc* a, int seq, int64_t keep_from, int* released);
 
 /* Drop the sequence: every block's count - 1, blocks reaching 0 return to the free list. */
 KV_API int kv_alloc_seq_free(kv_alloc* a, int seq);

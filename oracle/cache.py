@@ -172,6 +172,7 @@ class BlockManager:
         """Sliding window: release every block that lies wholly before token ``keep_from``
         (its table entry becomes -1; later entries keep their logical positions).
         Returns the released block ids."""
+        assert 0 <= keep_from <= self.lens[sid]      # the block for the next token stays
         table = self.tables[sid]
         released = []
         for j in range(min(keep_from // self.B, len(table))):

@@ -29,6 +29,15 @@ class kv_pool_desc(C.Structure):
                 ("num_heads", C.c_int), ("head_dim", C.c_int), ("dtype", C.c_int)]
 
 
+class kv_decode_args(C.Structure):
+    _fields_ = [("layer", C.c_int), ("q", C.c_void_p), ("num_q_heads", C.c_int),
+                ("k_new", C.c_void_p), ("v_new", C.c_void_p), ("in_dtype", C.c_int),
+                ("out", C.c_void_p), ("block_tables", C.c_void_p), ("max_blocks_per_seq", C.c_int),
+                ("context_lens", C.c_void_p), ("batch", C.c_int), ("max_context", C.c_int),
+                ("window", C.c_int), ("scale", C.c_float), ("partition_tokens", C.c_int),
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("stream", C.c_void_p)]
+
+
 class kv_alloc_stats_t(C.Structure):
     _fields_ = [("num_blocks", C.c_int), ("free_blocks", C.c_int), ("shared_blocks", C.c_int),
                 ("num_seqs", C.c_int), ("used_slots", C.c_int64), ("wasted_slots", C.c_int64)]
@@ -63,6 +72,9 @@ _SIGS = {
     "kv_alloc_seq_fork": (C.c_int, [_VP, C.c_int, C.POINTER(C.c_int)]),
     "kv_alloc_append_slots": (C.c_int, [_VP, C.c_int, C.c_int, _I64P, _I32P]),
     "kv_alloc_seq_free": (C.c_int, [_VP, C.c_int]),
+    "kv_alloc_seq_trim": (C.c_int, [_VP, C.c_int, C.c_int64, C.POINTER(C.c_int)]),
+    "paged_decode_workspace_size_ex": (C.c_size_t, [_VP, _VP]),
+    "paged_decode_attention_ex": (C.c_int, [_VP, _VP]),
     "kv_alloc_seq_info": (C.c_int, [_VP, C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int)]),
     "kv_alloc_block_table": (C.c_int, [_VP, C.c_int, _I32P, C.c_int, C.POINTER(C.c_int)]),
     "kv_alloc_build_tables": (C.c_int, [_VP, _I32P, C.c_int, _I32P, C.c_int, _I32P]),
@@ -206,6 +218,17 @@ def paged_decode_attention_gqa(pool: int, layer: int, q: int, num_q_heads: int, 
         context_lens, batch, max_context, scale, partition_tokens, workspace, workspace_bytes, stream))
 
 
+def paged_decode_workspace_size_ex(pool: int, args: "kv_decode_args") -> int:
+    n = load().paged_decode_workspace_size_ex(pool, C.byref(args))
+    if n == 0:
+        raise KvError("paged_decode_workspace_size_ex", KV_ERR_INVALID_ARG)
+    return n
+
+
+def paged_decode_attention_ex(pool: int, args: "kv_decode_args") -> None:
+    _check("paged_decode_attention_ex", load().paged_decode_attention_ex(pool, C.byref(args)))
+
+
 KV_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -256,6 +279,13 @@ def kv_alloc_append_slots(a: int, seq: int, count: int):
     _check("kv_alloc_append_slots", load().kv_alloc_append_slots(a, seq, count, _i64(slots), _i32(pair)))
     cow = (pair[0], pair[1]) if pair[0] >= 0 else None
     return list(slots), cow
+
+
+def kv_alloc_seq_trim(a: int, seq: int, keep_from: int) -> int:
+    """Release the blocks wholly before token keep_from; returns how many entries were cleared."""
+    n = C.c_int(0)
+    _check("kv_alloc_seq_trim", load().kv_alloc_seq_trim(a, seq, keep_from, C.byref(n)))
+    return n.value
 
 
 def kv_alloc_seq_free(a: int, seq: int) -> None:

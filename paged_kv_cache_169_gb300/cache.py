@@ -155,6 +155,37 @@ class PagedKVCache:
             _dev_ptr(workspace, "workspace"), workspace.numel(), _stream(stream))
         return out
 
+    def attention_ex(self, layer: int, q: torch.Tensor, block_tables: torch.Tensor,
+                     context_lens: torch.Tensor, max_context: int, scale: float, window: int = 0,
+                     k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None, partition_tokens: int = 0,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Every decode option in one call (paged_decode_attention_ex): grouped-query heads
+        (q [batch, Hq, d]), optional fused append, and a sliding window of ``window`` tokens."""
+        batch, hq = q.shape[0], q.shape[1]
+        if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+            raise ValueError("block_tables and context_lens must be int32")
+        if out is None:
+            out = torch.empty((batch, hq, self.head_dim), dtype=torch.float32, device=q.device)
+        a = abi.kv_decode_args()
+        a.layer, a.q, a.num_q_heads = layer, _dev_ptr(q, "q"), hq
+        a.k_new = _dev_ptr(k_new, "k_new") if k_new is not None else None
+        a.v_new = _dev_ptr(v_new, "v_new") if v_new is not None else None
+        a.in_dtype = _IN_DTYPE[k_new.dtype] if k_new is not None else 0
+        a.out = _dev_ptr(out, "out")
+        a.block_tables, a.max_blocks_per_seq = _dev_ptr(block_tables, "block_tables"), block_tables.shape[1]
+        a.context_lens, a.batch, a.max_context = _dev_ptr(context_lens, "context_lens"), batch, max_context
+        a.window, a.scale, a.partition_tokens = window, float(scale), partition_tokens
+        if workspace is None:
+            n = abi.paged_decode_workspace_size_ex(self.handle, a)
+            if self._ws is None or self._ws.numel() < n:
+                self._ws = torch.empty(n, dtype=torch.uint8, device=self.k[0].device)
+            workspace = self._ws
+        a.workspace, a.workspace_bytes = _dev_ptr(workspace, "workspace"), workspace.numel()
+        a.stream = _stream(stream)
+        abi.paged_decode_attention_ex(self.handle, a)
+        return out
+
     def device_error(self, clear: bool = True, stream=None) -> int:
         return abi.kv_get_device_error(self.handle, _stream(stream), clear)
 
@@ -188,6 +219,9 @@ class BlockAllocator:
 
     def free_seq(self, seq: int) -> None:
         abi.kv_alloc_seq_free(self.handle, seq)
+
+    def trim(self, seq: int, keep_from: int) -> int:
+        return abi.kv_alloc_seq_trim(self.handle, seq, keep_from)
 
     def seq_info(self, seq: int):
         return abi.kv_alloc_seq_info(self.handle, seq)

@@ -105,7 +105,8 @@ int kv_alloc_seq_fork(kv_alloc* a, int parent, int* child) {
     auto it = a->seqs.find(parent);
     if (it == a->seqs.end()) return KV_ERR_STATE;
     kv_alloc::Seq s = it->second;
-    for (int32_t b : s.table) a->ref[b] += 1;
+    for (int32_t b : s.table)
+        if (b >= 0) a->ref[b] += 1;                  // entries a window trimmed are -1
     int id = a->next_id++;
     a->seqs.emplace(id, std::move(s));
     *child = id;
@@ -145,8 +146,27 @@ int kv_alloc_seq_free(kv_alloc* a, int seq) {
     if (it == a->seqs.end()) return KV_ERR_STATE;
     int rc = KV_OK;
     for (int32_t b : it->second.table)
-        if (release(a, b) != KV_OK) rc = KV_ERR_STATE;
+        if (b >= 0 && release(a, b) != KV_OK) rc = KV_ERR_STATE;
     a->seqs.erase(it);
+    return rc;
+}
+
+int kv_alloc_seq_trim(kv_alloc* a, int seq, int64_t keep_from, int* released) {
+    if (!a || keep_from < 0) return KV_ERR_INVALID_ARG;
+    auto it = a->seqs.find(seq);
+    if (it == a->seqs.end()) return KV_ERR_STATE;
+    kv_alloc::Seq& s = it->second;
+    // the block that receives the next token must stay: keep_from may not pass the length
+    if (keep_from > s.len) return KV_ERR_INVALID_ARG;
+    const int64_t whole = keep_from / a->block_size;      // blocks ending at or before keep_from
+    int n = 0, rc = KV_OK;
+    for (int64_t j = 0; j < whole && j < (int64_t)s.table.size(); ++j) {
+        if (s.table[j] < 0) continue;
+        if (release(a, s.table[j]) != KV_OK) rc = KV_ERR_STATE;
+        s.table[j] = -1;
+        ++n;
+    }
+    if (released) *released = n;
     return rc;
 }
 
@@ -209,7 +229,8 @@ int kv_alloc_stats(const kv_alloc* a, kv_alloc_stats_t* st) {
     st->num_seqs = (int)a->seqs.size();
     int64_t used = 0, waste = 0;
     for (const auto& kv : a->seqs) {
-        used += kv.second.len;
+        const int64_t trimmed = std::count(kv.second.table.begin(), kv.second.table.end(), -1);
+        used += kv.second.len - trimmed * a->block_size;  // tokens still held in live blocks
         waste += (int64_t)kv.second.table.size() * a->block_size - kv.second.len;
     }
     st->used_slots = used;

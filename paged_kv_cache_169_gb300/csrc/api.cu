@@ -254,4 +254,51 @@ int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, int num_
                                         max_context, scale, plan, workspace, stream);
 }
 
+size_t paged_decode_workspace_size_ex(const kv_pool* pool, const kv_decode_args* x) {
+    if (!pool || !x) return 0;
+    const int hq = x->num_q_heads ? x->num_q_heads : pool->desc.num_heads;
+    if (hq < 1 || hq % pool->desc.num_heads != 0) return 0;
+    kvp::AttnPlan plan;
+    if (kvp::plan_attention(pool, x->batch, x->max_context, x->partition_tokens, &plan,
+                            hq / pool->desc.num_heads, x->window) != KV_OK)
+        return 0;
+    return plan.ws_bytes;
+}
+
+int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* x) {
+    if (!pool || !x) return KV_ERR_INVALID_ARG;
+    if (x->layer < 0 || x->layer >= pool->desc.num_layers || x->batch < 0 || x->max_context < 0 ||
+        x->window < 0)
+        return KV_ERR_INVALID_ARG;
+    const int hq = x->num_q_heads ? x->num_q_heads : pool->desc.num_heads;
+    if (hq < 1 || hq % pool->desc.num_heads != 0) return KV_ERR_INVALID_ARG;
+    const int group = hq / pool->desc.num_heads;
+    if (!kvp::valid_group(pool->desc, group)) return KV_ERR_INVALID_ARG;
+    if (x->batch == 0) return KV_OK;
+    if (!x->q || !x->out || !x->block_tables || !x->context_lens || !x->workspace || x->max_blocks_per_seq < 1)
+        return KV_ERR_INVALID_ARG;
+    if ((x->k_new == nullptr) != (x->v_new == nullptr)) return KV_ERR_INVALID_ARG;
+    if (!kvp::aligned16(x->q) || !kvp::aligned16(x->out) ||
+        (x->k_new && (!kvp::aligned16(x->k_new) || !kvp::aligned16(x->v_new))) ||
+        (reinterpret_cast<uintptr_t>(x->workspace) & 255u) != 0)
+        return KV_ERR_INVALID_ARG;
+    if (x->k_new) {
+        const kv_dtype pd = pool->desc.dtype;
+        if (pd == KV_FP8_E4M3) {
+            if (x->in_dtype != KV_F16 && x->in_dtype != KV_F32) return KV_ERR_INVALID_ARG;
+        } else if (x->in_dtype != pd) {
+            return KV_ERR_INVALID_ARG;
+        }
+    }
+    if (!(x->scale > 0.f) || !(x->scale < 3.0e38f)) return KV_ERR_INVALID_ARG;
+    kvp::AttnPlan plan;
+    int rc = kvp::plan_attention(pool, x->batch, x->max_context, x->partition_tokens, &plan, group, x->window);
+    if (rc != KV_OK) return rc;
+    if (x->workspace_bytes < plan.ws_bytes) return KV_ERR_INVALID_ARG;
+    return kvp::launch_attention_append(pool, x->layer, x->q, x->k_new, x->v_new,
+                                        x->k_new ? kvp::elem_bytes(x->in_dtype) : 0, x->out, x->block_tables,
+                                        x->max_blocks_per_seq, x->context_lens, x->batch, x->max_context,
+                                        x->scale, plan, x->workspace, x->stream);
+}
+
 }  // extern "C"

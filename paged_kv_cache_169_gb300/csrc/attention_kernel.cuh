@@ -59,6 +59,7 @@ struct AttnArgs {
     const char* k_new;     // fused append: [batch][H][D] new-token K (nullptr: no append)
     const char* v_new;
     int in_bytes;          // element size of k_new / v_new (2 or 4)
+    int window;            // > 0: attend only to the last `window` tokens of each sequence
     int* err;
     int batch, H, B, max_blocks, ctx_limit, P, max_parts, num_blocks;
     float qscale;          // scale * log2(e)
@@ -83,6 +84,8 @@ struct __align__(16) Meta {
     int patch_row;          // F_PATCH: chunk row of the token appended by this call
     int patch_id, patch_off;   // F_PATCH: its physical block and offset inside the block
     int ids[4];             // physical block of each copy in the chunk (FP8: scale lookup)
+    int lo;                 // sliding window: chunk rows below lo lie before the window
+    int pad[3];
 };
 
 constexpr int round_up(int a, int b) { return (a + b - 1) / b * b; }
@@ -147,6 +150,16 @@ struct Cfg {
 
 
 __device__ __forceinline__ int nparts_of(int ctx, int P) { return ctx <= P ? 1 : (ctx + P - 1) / P; }
+
+// Sliding window: the first attended token, and the first token actually read — rounded
+// down to a whole copy unit (rpc rows) so every copy stays inside blocks the window still
+// holds.  Rows in [first, start) are read but masked.
+__device__ __forceinline__ int attend_start(int ctx, int window) {
+    return (window > 0 && ctx > window) ? ctx - window : 0;
+}
+__device__ __forceinline__ int attend_first(int ctx, int window, int rpc) {
+    return attend_start(ctx, window) / rpc * rpc;
+}
 
 __device__ __forceinline__ float warp_max(float v) {
     #pragma unroll
@@ -231,12 +244,13 @@ __device__ __forceinline__ void load_q(const char* qrow, int sub, float qs, floa
 
 struct __align__(16) Item {
     int s, h, p, tok0, ntok, nchunks, single, valid, last;   // last: final partition
+    int lo;                                                    // masked rows at the start
 };
 
 // (s, h, p) of compact item index `it` (items ordered by sequence, head, partition).
 template <int CT>
 __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ctx, const int* s_end,
-                                            int batch, int H, int P) {
+                                            int batch, int H, int P, int window, int rpc) {
     Item r{};
     r.valid = it < n_items;
     if (!r.valid) return r;
@@ -248,13 +262,15 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
     const int s = lo;
     const int start = s ? s_end[s - 1] : 0;
     const int ctx = s_ctx[s];
-    const int np = nparts_of(ctx, P);
+    const int first = attend_first(ctx, window, rpc);
+    const int np = nparts_of(ctx - first, P);
     const int rr = it - start;
     r.s = s;
     r.h = rr / np;
     r.p = rr - r.h * np;
-    r.tok0 = r.p * P;
+    r.tok0 = first + r.p * P;
     r.ntok = min(P, ctx - r.tok0);
+    r.lo = r.p == 0 ? attend_start(ctx, window) - first : 0;
     r.nchunks = r.ntok > 0 ? (r.ntok + CT - 1) / CT : 1;
     r.single = np == 1;
     r.last = r.p == np - 1;
@@ -365,7 +381,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
             c = c < 0 ? 0 : a.ctx_limit;
         }
         s_ctx[s] = c;
-        s_end[s] = a.H * nparts_of(c, a.P);
+        s_end[s] = a.H * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), a.P);
     }
     if (tid == 0) {
         for (int i = 0; i < 2 * NC * NSW; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -405,7 +421,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
         auto take = [&]() {
             const int idx = static_cast<int>(pending);
             pending = atomicAdd(a.counter, 1u);
-            return decode_item<CT>(idx, n_items, s_ctx, s_end, a.batch, a.H, a.P);
+            return decode_item<CT>(idx, n_items, s_ctx, s_end, a.batch, a.H, a.P, a.window, rpc);
         };
         int ids[CBMAX];
         auto load_ids = [&](const Item& it, int chunk) {
@@ -455,6 +471,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
                     meta->h = cur.h;
                     meta->p = cur.p;
                     meta->ntok = nt;
+                    meta->lo = c == 0 ? cur.lo : 0;
                     // fused append: the sequence's newest token is the last row of the
                     // last chunk of its last partition
                     const bool patch = a.k_new != nullptr && cur.last && c == cur.nchunks - 1 && nt > 0;
@@ -555,6 +572,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
         }
         if (meta.flags & F_TERM) break;
         const int nt = meta.ntok;
+        const int lo = reinterpret_cast<const Meta*>(stg + C::META_OFF)->lo;
         if (meta.flags & F_FIRST) {
             #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -628,7 +646,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
                 #pragma unroll
                 for (int off = TPL; off < 16; off <<= 1) x += __shfl_xor_sync(FULL, x, off);
                 if constexpr (C::FP8) x *= ks;
-                x = tok_l < nt ? x : -CUDART_INF_F;
+                x = (tok_l < nt && tok_l >= lo) ? x : -CUDART_INF_F;
                 if (__any_sync(FULL, x > m[g] + 8.f)) {   // raise the running max only when needed
                     const float m_new = fmaxf(m[g], warp_max(x));
                     const float corr = ex2_approx(m[g] - m_new);
@@ -646,7 +664,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
                 float pt[G];
                 #pragma unroll
                 for (int g = 0; g < G; ++g) pt[g] = __shfl_sync(FULL, pv[g], i + (lane & 16));
-                if (nt == CT || 2 * i + half < nt) {
+                if ((nt == CT && lo == 0) || (2 * i + half < nt && 2 * i + half >= lo)) {
                     float2 vx[DPL / 2];
                     load_row<C>(V + 2 * i * C::ROW, sub, vx);
                     #pragma unroll
@@ -700,7 +718,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
                 unsigned prev = 0;
                 if (lane == 0) prev = atomicAdd(a.arrivals + shk, 1u);
                 prev = __shfl_sync(FULL, prev, 0);
-                const int np = nparts_of(s_ctx[meta.s], a.P);
+                const int ctx_s = s_ctx[meta.s];
+                const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
                 if (prev == static_cast<unsigned>(np - 1)) {
                     __threadfence();
                     #pragma unroll 1

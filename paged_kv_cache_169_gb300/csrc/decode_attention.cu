@@ -41,9 +41,11 @@ bool valid_group(const kv_pool_desc& d, int group) {
 }
 
 int plan_attention(const kv_pool* pool, int batch, int max_context, int partition_tokens,
-                   AttnPlan* plan, int group) {
+                   AttnPlan* plan, int group, int window) {
     const kv_pool_desc& d = pool->desc;
-    if (batch < 0 || max_context < 0 || batch > kMaxBatch * kMaxSub) return KV_ERR_INVALID_ARG;
+    if (batch < 0 || max_context < 0 || window < 0 || batch > kMaxBatch * kMaxSub) return KV_ERR_INVALID_ARG;
+    // a sliding window bounds the tokens read per sequence (window + up to 31 masked rows)
+    const int span = (window > 0 && window + 32 < max_context) ? window + 32 : max_context;
     if (!valid_group(d, group)) return KV_ERR_INVALID_ARG;
     const int cap = 32 * d.block_size;             // one producer lane per block of a partition
     const int nc = consumers_for(d, group);
@@ -57,7 +59,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
         const int64_t target = 8ll * pool->num_sms * nc;
         int64_t parts = (target + units - 1) / units;
         if (parts < 1) parts = 1;
-        int64_t p = (max_context + parts - 1) / parts;
+        int64_t p = (span + parts - 1) / parts;
         p = (p + kPartAlign - 1) / kPartAlign * kPartAlign;
         if (p < kPartAlign) p = kPartAlign;
         if (p > cap) p = cap;
@@ -66,9 +68,10 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
         return KV_ERR_INVALID_ARG;
     }
     plan->partition = P;
-    plan->max_parts = max_context <= P ? 1 : (max_context + P - 1) / P;
+    plan->max_parts = span <= P ? 1 : (span + P - 1) / P;
     plan->consumers = nc;
     plan->group = group;
+    plan->window = window;
     size_t ws = 256;                                // kMaxSub work counters
     if (plan->max_parts > 1) {
         const size_t n = static_cast<size_t>(batch) * d.num_heads * group * plan->max_parts;
@@ -131,6 +134,7 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     a.max_parts = plan.max_parts;
     a.num_blocks = d.num_blocks;
     a.qscale = scale * 1.4426950408889634f;        // log2(e): softmax evaluated with 2^x
+    a.window = plan.window;
 
     if (group != 1) return launch_attention_grouped(group, pool, a, plan, counters, stream);
     if (d.dtype == KV_F32) {

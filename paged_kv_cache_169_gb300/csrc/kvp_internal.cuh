@@ -34,12 +34,13 @@ struct AttnPlan {
     int max_parts;       // ceil(max_context / partition)
     int consumers;       // consumer warps per CTA
     int group;           // query heads per KV head
+    int window;          // > 0: sliding window of the last `window` tokens
     size_t ws_bytes;     // workspace bytes
 };
 // group: query heads per KV head (1, or 2/4/8 for fp16 and FP8 pools)
 bool valid_group(const kv_pool_desc& d, int group);
 int plan_attention(const kv_pool* pool, int batch, int max_context, int partition_tokens,
-                   AttnPlan* plan, int group = 1);
+                   AttnPlan* plan, int group = 1, int window = 0);
 int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,
                      const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                      int batch, int max_context, float scale, const AttnPlan& plan,

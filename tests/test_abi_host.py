@@ -97,6 +97,11 @@ def _run_both(num_blocks, B, order, ops):
                 ca, cm = ids.pop(op[1])
                 abi.kv_alloc_seq_free(a, ca)
                 m.free_seq(cm)
+            elif kind == "trim":                     # keep the last op[2] tokens
+                ca, cm = ids[op[1]]
+                keep_from = max(0, m.lens[cm] - op[2])
+                n = abi.kv_alloc_seq_trim(a, ca, keep_from)
+                assert n == len(m.trim(cm, keep_from))
             # state comparison after every operation
             assert abi.kv_alloc_free_list(a, num_blocks) == m.free
             assert [abi.kv_alloc_ref_count(a, b) for b in range(num_blocks)] == m.ref
@@ -106,7 +111,7 @@ def _run_both(num_blocks, B, order, ops):
         st = abi.kv_alloc_stats(a)
         assert st.free_blocks == len(m.free) and st.shared_blocks == m.shared_blocks()
         assert st.num_seqs == len(ids)
-        assert st.used_slots == sum(m.lens[cm] for _, cm in ids.values())
+        assert st.used_slots == sum(m.lens[cm] - m.table(cm).count(-1) * B for _, cm in ids.values())
         assert st.wasted_slots == sum(len(m.table(cm)) * B - m.lens[cm] for _, cm in ids.values())
     finally:
         abi.kv_alloc_destroy(a)
@@ -135,8 +140,10 @@ def test_allocator_matches_oracle_random_ops(lib):
                 ops.append(("fork", live[int(rng.integers(len(live)))], k))
                 live.append(k)
                 k += 1
-            elif r < 8 and len(live) > 1:
+            elif r < 8 and len(live) > 1 and rng.integers(2):
                 ops.append(("free", live.pop(int(rng.integers(len(live))))))
+            elif r < 9:
+                ops.append(("trim", live[int(rng.integers(len(live)))], int(rng.integers(1, 60))))
             else:
                 ops.append(("new", k))
                 live.append(k)
@@ -158,6 +165,8 @@ def test_allocator_errors(lib):
         assert e.value.status == abi.KV_ERR_STATE
         with pytest.raises(abi.KvError):
             abi.kv_alloc_append_slots(a, s, 0)
+        with pytest.raises(abi.KvError):
+            abi.kv_alloc_seq_trim(a, s, 33)                   # beyond the length
         with pytest.raises(abi.KvError):
             abi.kv_alloc_build_tables(a, [s], 3)              # table longer than max_blocks
         tabs, lens = abi.kv_alloc_build_tables(a, [s], 6)
