@@ -197,3 +197,47 @@ class BlockManager:
 
     def shared_blocks(self) -> int:
         return sum(1 for r in self.ref if r > 1)
+
+
+# --------------------------------------------------------------------------
+# block swap to / from host memory
+# --------------------------------------------------------------------------
+
+def swap_out(k_pools, v_pools, blocks, k_scales=(), v_scales=()) -> np.ndarray:
+    """Host image of physical blocks ([KV缓存机制解析] §6.1: blocks of a long context kept in
+    CPU memory; [PagedAttention] §7.2: cold blocks swapped to CPU memory).
+
+    Layout (bytes): for each listed block i, for each layer l: the whole K block, then the
+    whole V block (raw bytes of [H, B, d]); after all blocks, for FP8 pools, per block and
+    layer the K scale then the V scale (float32).
+    """
+    parts = []
+    for b in np.asarray(blocks).tolist():
+        for kp, vp in zip(k_pools, v_pools):
+            parts.append(np.ascontiguousarray(kp[b]).view(np.uint8).reshape(-1))
+            parts.append(np.ascontiguousarray(vp[b]).view(np.uint8).reshape(-1))
+    if len(k_scales):
+        sc = [np.float32(s[b]) for b in np.asarray(blocks).tolist() for ks, vs in zip(k_scales, v_scales)
+              for s in (ks, vs)]
+        parts.append(np.array(sc, dtype=np.float32).view(np.uint8))
+    return np.concatenate(parts) if parts else np.zeros(0, dtype=np.uint8)
+
+
+def swap_in(k_pools, v_pools, blocks, image, k_scales=(), v_scales=()) -> None:
+    """Write a host image made by ``swap_out`` back into the listed physical blocks."""
+    image = np.asarray(image, dtype=np.uint8)
+    pos = 0
+    for b in np.asarray(blocks).tolist():
+        for kp, vp in zip(k_pools, v_pools):
+            for p in (kp, vp):
+                n = p[b].nbytes
+                p[b] = image[pos:pos + n].view(p.dtype).reshape(p[b].shape)
+                pos += n
+    if len(k_scales):
+        sc = image[pos:].view(np.float32)
+        i = 0
+        for b in np.asarray(blocks).tolist():
+            for ks, vs in zip(k_scales, v_scales):
+                ks[b] = sc[i]
+                vs[b] = sc[i + 1]
+                i += 2

@@ -201,3 +201,31 @@ def test_trim_releases_only_blocks_wholly_before_the_window():
     m.free_seq(s)
     m.free_seq(c)
     assert m.used_blocks() == 0 and all(r == 0 for r in m.ref)
+
+
+def test_swap_round_trip_and_layout():
+    rng = np.random.default_rng(6)
+    L, nb, H, B, d = 3, 7, 2, 4, 8
+    kp = [rng.standard_normal((nb, H, B, d)).astype(np.float16) for _ in range(L)]
+    vp = [rng.standard_normal((nb, H, B, d)).astype(np.float16) for _ in range(L)]
+    ks = [rng.uniform(0.1, 1, nb).astype(np.float32) for _ in range(L)]
+    vs = [rng.uniform(0.1, 1, nb).astype(np.float32) for _ in range(L)]
+    blocks = [5, 0, 3]
+    img = C.swap_out(kp, vp, blocks, ks, vs)
+    blk = H * B * d * 2
+    assert img.size == len(blocks) * L * 2 * blk + len(blocks) * L * 2 * 4
+    # block 0 of the list, layer 1, V part sits at (0*L + 1)*2 + 1 block slots
+    off = ((0 * L + 1) * 2 + 1) * blk
+    assert np.array_equal(img[off:off + blk].view(np.float16).reshape(H, B, d), vp[1][5])
+    # scales: list block 2 (physical 3), layer 2, K then V
+    sc = img[len(blocks) * L * 2 * blk:].view(np.float32)
+    assert sc[(2 * L + 2) * 2] == ks[2][3] and sc[(2 * L + 2) * 2 + 1] == vs[2][3]
+    # round trip into other blocks, nothing else touched
+    before = [p.copy() for p in kp + vp]
+    C.swap_in(kp, vp, [1, 2, 6], img, ks, vs)
+    for l in range(L):
+        for src, dst in zip(blocks, [1, 2, 6]):
+            assert np.array_equal(kp[l][dst].view(np.uint16), before[l][src].view(np.uint16))
+            assert np.array_equal(vp[l][dst].view(np.uint16), before[L + l][src].view(np.uint16))
+            assert ks[l][dst] == ks[l][src] and vs[l][dst] == vs[l][src]
+        assert np.array_equal(kp[l][4], before[l][4])
