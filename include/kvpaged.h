@@ -146,6 +146,34 @@ KV_API int kv_append(kv_pool* pool, int layer, const void* k, const void* v, kv_
 KV_API int kv_copy_blocks(kv_pool* pool, const int32_t* pairs, int num_pairs, int layer_begin,
                    int layer_end, kv_stream_t stream);
 
+/* ---------------------------------------------------------------- swap to host memory */
+
+/* Bytes of the host image of num_blocks blocks over layers [layer_begin, layer_end):
+ * num_blocks * layers * 2 * (num_heads*block_size*head_dim*element bytes), plus for FP8
+ * pools num_blocks * layers * 2 * 4 bytes of scales.  0 on invalid arguments. */
+KV_API size_t kv_swap_bytes(const kv_pool* pool, int num_blocks, int layer_begin, int layer_end);
+
+/* Copy the listed physical blocks (device int32 blocks[num_blocks]) of every layer in
+ * [layer_begin, layer_end) (at most 64 layers per call) into host_dst: host memory the GPU
+ * can address, 16-byte aligned, of kv_swap_bytes bytes — pinned memory (cudaHostAlloc /
+ * cudaHostRegister), or on systems with coherent pageable-memory access (e.g. Grace with
+ * NVLink-C2C) any host memory; anything else gives KV_ERR_INVALID_ARG.
+ * Image layout: for block i, layer l: the K block then the V block (raw [H][B][d]); after
+ * all blocks, for FP8 pools, per block and layer the K then the V scale (float32).  One
+ * kernel moves everything through the device mapping.  Asynchronous: host_dst is complete
+ * when the stream reaches this point.  Ids outside the pool set KV_DEVERR_BLOCK_ID and are
+ * skipped.  With the allocator the caller then releases the blocks (kv_alloc_seq_free) to
+ * preempt a sequence.
+ * Cold blocks moved to CPU memory: [KV缓存机制解析] §6.1 (缓存分块加载) and
+ * [PagedAttention] §7.2 (冷块交换到CPU内存). */
+KV_API int kv_swap_out(kv_pool* pool, const int32_t* blocks, int num_blocks, int layer_begin, int layer_end,
+                       void* host_dst, kv_stream_t stream);
+
+/* The reverse: write an image made by kv_swap_out into the listed (freshly allocated)
+ * physical blocks, bit-exact.  Same rules. */
+KV_API int kv_swap_in(kv_pool* pool, const void* host_src, const int32_t* blocks, int num_blocks,
+                      int layer_begin, int layer_end, kv_stream_t stream);
+
 /* ---------------------------------------------------------------- decode attention */
 
 /* Bytes of device workspace paged_decode_attention needs for these arguments

@@ -54,6 +54,9 @@ _SIGS = {
     "kv_get_device_error": (C.c_int, [_VP, _VP, C.c_int, C.POINTER(C.c_int)]),
     "kv_append": (C.c_int, [_VP, C.c_int, _VP, _VP, C.c_int, _VP, C.c_int, _VP]),
     "kv_copy_blocks": (C.c_int, [_VP, _VP, C.c_int, C.c_int, C.c_int, _VP]),
+    "kv_swap_bytes": (C.c_size_t, [_VP, C.c_int, C.c_int, C.c_int]),
+    "kv_swap_out": (C.c_int, [_VP, _VP, C.c_int, C.c_int, C.c_int, _VP, _VP]),
+    "kv_swap_in": (C.c_int, [_VP, _VP, _VP, C.c_int, C.c_int, C.c_int, _VP]),
     "paged_decode_workspace_size": (C.c_size_t, [_VP, C.c_int, C.c_int, C.c_int]),
     "paged_decode_attention": (C.c_int, [_VP, C.c_int, _VP, _VP, _VP, C.c_int, _VP, C.c_int,
                                          C.c_int, C.c_float, C.c_int, _VP, C.c_size_t, _VP]),
@@ -172,6 +175,20 @@ def kv_append(pool: int, layer: int, k: int, v: int, in_dtype: int, slot_mapping
 def kv_copy_blocks(pool: int, pairs: int, num_pairs: int, layer_begin: int, layer_end: int,
                    stream: int = 0) -> None:
     _check("kv_copy_blocks", load().kv_copy_blocks(pool, pairs, num_pairs, layer_begin, layer_end, stream))
+
+
+def kv_swap_bytes(pool: int, num_blocks: int, layer_begin: int, layer_end: int) -> int:
+    return load().kv_swap_bytes(pool, num_blocks, layer_begin, layer_end)
+
+
+def kv_swap_out(pool: int, blocks: int, num_blocks: int, layer_begin: int, layer_end: int, host_dst: int,
+                stream: int = 0) -> None:
+    _check("kv_swap_out", load().kv_swap_out(pool, blocks, num_blocks, layer_begin, layer_end, host_dst, stream))
+
+
+def kv_swap_in(pool: int, host_src: int, blocks: int, num_blocks: int, layer_begin: int, layer_end: int,
+               stream: int = 0) -> None:
+    _check("kv_swap_in", load().kv_swap_in(pool, host_src, blocks, num_blocks, layer_begin, layer_end, stream))
 
 
 def paged_decode_workspace_size(pool: int, batch: int, max_context: int, partition_tokens: int = 0) -> int:

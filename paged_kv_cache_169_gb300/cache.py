@@ -78,6 +78,26 @@ class PagedKVCache:
         abi.kv_copy_blocks(self.handle, _dev_ptr(pairs, "pairs") if pairs.numel() else 0,
                            pairs.shape[0], layer_begin, le, _stream(stream))
 
+    def swap_out(self, blocks: torch.Tensor, host: torch.Tensor | None = None, layer_begin: int = 0,
+                 layer_end: int | None = None, stream=None) -> torch.Tensor:
+        """Copy physical blocks (device int32 [n]) of the layers to a pinned host image
+        (uint8, allocated if not given).  Asynchronous on the stream."""
+        le = self.num_layers if layer_end is None else layer_end
+        n = abi.kv_swap_bytes(self.handle, blocks.numel(), layer_begin, le)
+        if host is None:
+            host = torch.empty(n, dtype=torch.uint8).pin_memory()
+        if host.numel() < n or host.is_cuda:
+            raise ValueError("host image must be a pinned CPU tensor of kv_swap_bytes bytes")
+        abi.kv_swap_out(self.handle, _dev_ptr(blocks, "blocks"), blocks.numel(), layer_begin, le,
+                        host.data_ptr(), _stream(stream))
+        return host
+
+    def swap_in(self, host: torch.Tensor, blocks: torch.Tensor, layer_begin: int = 0,
+                layer_end: int | None = None, stream=None) -> None:
+        le = self.num_layers if layer_end is None else layer_end
+        abi.kv_swap_in(self.handle, host.data_ptr(), _dev_ptr(blocks, "blocks"), blocks.numel(),
+                       layer_begin, le, _stream(stream))
+
     def workspace_bytes(self, batch: int, max_context: int, partition_tokens: int = 0) -> int:
         return abi.paged_decode_workspace_size(self.handle, batch, max_context, partition_tokens)
 

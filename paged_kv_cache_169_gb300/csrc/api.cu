@@ -301,4 +301,32 @@ int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* x) {
                                         x->scale, plan, x->workspace, x->stream);
 }
 
+size_t kv_swap_bytes(const kv_pool* pool, int num_blocks, int layer_begin, int layer_end) {
+    if (!pool || num_blocks < 0 || layer_begin < 0 || layer_end < layer_begin ||
+        layer_end > pool->desc.num_layers)
+        return 0;
+    return kvp::swap_bytes(pool, num_blocks, layer_begin, layer_end);
+}
+
+static int swap_common(kv_pool* pool, bool out, const int32_t* blocks, int num_blocks, int layer_begin,
+                       int layer_end, void* host, kv_stream_t stream) {
+    if (!pool || num_blocks < 0 || layer_begin < 0 || layer_end < layer_begin ||
+        layer_end > pool->desc.num_layers || num_blocks > 65535)
+        return KV_ERR_INVALID_ARG;
+    if (num_blocks == 0 || layer_end == layer_begin) return KV_OK;
+    if (!blocks || !host || !kvp::aligned16(host)) return KV_ERR_INVALID_ARG;
+    return kvp::launch_swap(pool, out, blocks, num_blocks, layer_begin, layer_end, host, stream);
+}
+
+int kv_swap_out(kv_pool* pool, const int32_t* blocks, int num_blocks, int layer_begin, int layer_end,
+                void* host_dst, kv_stream_t stream) {
+    return swap_common(pool, true, blocks, num_blocks, layer_begin, layer_end, host_dst, stream);
+}
+
+int kv_swap_in(kv_pool* pool, const void* host_src, const int32_t* blocks, int num_blocks, int layer_begin,
+               int layer_end, kv_stream_t stream) {
+    return swap_common(pool, false, blocks, num_blocks, layer_begin, layer_end, const_cast<void*>(host_src),
+                       stream);
+}
+
 }  // extern "C"

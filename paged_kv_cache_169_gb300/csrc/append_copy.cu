@@ -101,6 +101,37 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(
     }
 }
 
+// Swap: grid = (blocks, layers, 2 [K or V]).  Each CTA moves one block tensor between the
+// pool and its slot in a pinned host image (reached through its device mapping), 16 bytes
+// per access.  Image layout: [block i][layer l][K, V][block_bytes], then the FP8 scales
+// [block i][layer l][K, V] as float32.
+template <bool OUT>
+__global__ void __launch_bounds__(256) swap_kernel(const int32_t* __restrict__ blocks, LayerPtrs ptrs,
+                                                   char* image, int64_t block_bytes, int nblocks_listed,
+                                                   int nl, int num_blocks, int* err) {
+    const int i = blockIdx.x, layer = blockIdx.y, which = blockIdx.z;
+    const int b = blocks[i];
+    if (b < 0 || b >= num_blocks) {
+        if (threadIdx.x == 0 && layer == 0 && which == 0) atomicOr(err, KV_DEVERR_BLOCK_ID);
+        return;
+    }
+    char* pool = static_cast<char*>(which == 0 ? ptrs.k[layer] : ptrs.v[layer]) + static_cast<int64_t>(b) * block_bytes;
+    char* img = image + ((static_cast<int64_t>(i) * nl + layer) * 2 + which) * block_bytes;
+    uint4* dst = reinterpret_cast<uint4*>(OUT ? img : pool);
+    const uint4* src = reinterpret_cast<const uint4*>(OUT ? pool : img);
+    const int64_t n = block_bytes / 16;
+    for (int64_t k = threadIdx.x; k < n; k += blockDim.x) dst[k] = src[k];
+    if (threadIdx.x == 0) {
+        float* sc = which == 0 ? ptrs.ks[layer] : ptrs.vs[layer];
+        if (sc) {
+            float* img_sc = reinterpret_cast<float*>(image + static_cast<int64_t>(nblocks_listed) * nl * 2 * block_bytes) +
+                            (static_cast<int64_t>(i) * nl + layer) * 2 + which;
+            if (OUT) *img_sc = sc[b];
+            else sc[b] = *img_sc;
+        }
+    }
+}
+
 }  // namespace
 
 int launch_append(const kv_pool* pool, int layer, const void* k, const void* v, kv_dtype in_dtype,
@@ -155,6 +186,52 @@ int launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int num_pairs,
         if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     }
     return KV_OK;
+}
+
+}  // namespace kvp
+
+namespace kvp {
+
+size_t swap_bytes(const kv_pool* pool, int num_blocks, int layer_begin, int layer_end) {
+    const kv_pool_desc& d = pool->desc;
+    const int64_t block_bytes =
+        static_cast<int64_t>(d.num_heads) * d.block_size * d.head_dim * elem_bytes(d.dtype);
+    const int64_t nl = layer_end - layer_begin;
+    int64_t n = static_cast<int64_t>(num_blocks) * nl * 2 * block_bytes;
+    if (d.dtype == KV_FP8_E4M3) n += static_cast<int64_t>(num_blocks) * nl * 2 * sizeof(float);
+    return static_cast<size_t>(n);
+}
+
+int launch_swap(const kv_pool* pool, bool out, const int32_t* blocks, int num_blocks, int layer_begin,
+                int layer_end, void* host, cudaStream_t stream) {
+    const kv_pool_desc& d = pool->desc;
+    if (num_blocks == 0 || layer_end == layer_begin) return KV_OK;
+    if (layer_end - layer_begin > kMaxCopyLayers) return KV_ERR_UNSUPPORTED;
+    void* dev = nullptr;
+    // the host image must be addressable by the device: pinned memory, or any host memory
+    // where the GPU has coherent pageable-memory access
+    if (cudaHostGetDevicePointer(&dev, host, 0) != cudaSuccess || !dev) {
+        cudaGetLastError();
+        return KV_ERR_INVALID_ARG;
+    }
+    const int64_t block_bytes =
+        static_cast<int64_t>(d.num_heads) * d.block_size * d.head_dim * elem_bytes(d.dtype);
+    const int nl = layer_end - layer_begin;
+    LayerPtrs p{};
+    for (int i = 0; i < nl; ++i) {
+        p.k[i] = pool->k_layers[layer_begin + i];
+        p.v[i] = pool->v_layers[layer_begin + i];
+        p.ks[i] = pool->k_scales ? pool->k_scales[layer_begin + i] : nullptr;
+        p.vs[i] = pool->v_scales ? pool->v_scales[layer_begin + i] : nullptr;
+    }
+    const dim3 grid(num_blocks, nl, 2);
+    if (out)
+        swap_kernel<true><<<grid, 256, 0, stream>>>(blocks, p, static_cast<char*>(dev), block_bytes, num_blocks,
+                                                    nl, d.num_blocks, pool->d_err);
+    else
+        swap_kernel<false><<<grid, 256, 0, stream>>>(blocks, p, static_cast<char*>(dev), block_bytes, num_blocks,
+                                                     nl, d.num_blocks, pool->d_err);
+    return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 }  // namespace kvp

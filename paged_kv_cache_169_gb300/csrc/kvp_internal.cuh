@@ -28,6 +28,9 @@ int launch_append(const kv_pool* pool, int layer, const void* k, const void* v, 
                   const int64_t* slot_mapping, int num_tokens, cudaStream_t stream);
 int launch_copy_blocks(const kv_pool* pool, const int32_t* pairs, int num_pairs, int layer_begin,
                        int layer_end, cudaStream_t stream);
+size_t swap_bytes(const kv_pool* pool, int num_blocks, int layer_begin, int layer_end);
+int launch_swap(const kv_pool* pool, bool out, const int32_t* blocks, int num_blocks, int layer_begin,
+                int layer_end, void* host, cudaStream_t stream);
 
 struct AttnPlan {
     int partition;       // tokens per split-context partition
