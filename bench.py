@@ -55,19 +55,22 @@ def apply_overrides(w, args):
     return w
 
 
-def algorithmic_bytes(w) -> int:
+def algorithmic_bytes(w, window: int = 0) -> int:
     """Bytes one paged_decode_attention call must move at minimum (one layer):
-    K+V of every cached token, q, out (fp32), the used block-table entries, context_lens,
-    and for FP8 pools the two per-block scales."""
+    K+V of every attended token, q, out (fp32), the block-table entries of the attended
+    blocks, context_lens, and for FP8 pools the two per-block scales.  With a sliding
+    window only the last `window` tokens of each sequence are attended."""
     kv_elem = 1 if w.kv == "fp8" else 2
     H, d, B = w.num_heads, w.head_dim, w.block_size
     Hq = w.q_heads                                   # query heads (grouped-query: > H)
-    kv = sum(w.lens) * H * d * kv_elem * 2
+    spans = [(n - min(n, window), n) if window > 0 else (0, n) for n in w.lens]
+    nblk = [(-(-hi // B) - lo // B) if hi > lo else 0 for lo, hi in spans]
+    kv = sum(hi - lo for lo, hi in spans) * H * d * kv_elem * 2
     q = w.batch * Hq * d * 2
     out = w.batch * Hq * d * 4
-    tables = sum(-(-n // B) for n in w.lens) * 4
+    tables = sum(nblk) * 4
     lens = w.batch * 4
-    scales = sum(-(-n // B) for n in w.lens) * 8 if w.kv == "fp8" else 0
+    scales = sum(nblk) * 8 if w.kv == "fp8" else 0
     return kv + q + out + tables + lens + scales
 
 
@@ -312,7 +315,13 @@ def run_ours(args):
     out = torch.empty((L, w.batch, Hq, d), dtype=torch.float32, device=dev)
     max_ctx = max(w.lens)
     grouped = Hq != H
-    if grouped:
+    if args.window:
+        from paged_kv_cache_169_gb300 import abi as _abi
+        xa = _abi.kv_decode_args()
+        xa.num_q_heads, xa.batch, xa.max_context = Hq, w.batch, max_ctx
+        xa.window, xa.partition_tokens = args.window, args.partition
+        ws = torch.empty(_abi.paged_decode_workspace_size_ex(cache.handle, xa), dtype=torch.uint8, device=dev)
+    elif grouped:
         from paged_kv_cache_169_gb300 import abi as _abi
         ws = torch.empty(_abi.paged_decode_workspace_size_gqa(cache.handle, w.batch, Hq, max_ctx, args.partition),
                          dtype=torch.uint8, device=dev)
@@ -330,7 +339,12 @@ def run_ours(args):
                 cache.append(l, k_new[l], v_new[l], slots)
             if ev is not None:
                 ev[l][0].record(stream)
-            if grouped:
+            if args.window:
+                cache.attention_ex(l, q[l], bt, cl, max_ctx, w.scale, window=args.window,
+                                   k_new=None if args.unfused else k_new[l],
+                                   v_new=None if args.unfused else v_new[l], out=out[l],
+                                   partition_tokens=args.partition, workspace=ws)
+            elif grouped:
                 cache.attention_gqa(l, q[l], bt, cl, max_ctx, w.scale,
                                     k_new=None if args.unfused else k_new[l],
                                     v_new=None if args.unfused else v_new[l], out=out[l],
@@ -405,7 +419,7 @@ def run_ours(args):
         raise SystemExit(f"device error bits {err}")
 
     # ---- numbers
-    alg = algorithmic_bytes(w)
+    alg = algorithmic_bytes(w, args.window)
     step_bytes = alg * L
     # the timed call's own minimum traffic: the fused call also reads the new K/V and
     # writes them into the pool
@@ -416,7 +430,7 @@ def run_ours(args):
     peak, peak_src = measured_peak()
     achieved = call_bytes / (attn_ms_mean / 1e3) / 1e9
     src = os.path.join(ROOT, "paged_kv_cache_169_gb300", "csrc", "decode_attention.cu")
-    traffic = traffic_record(src) if args.workload == "llama13b" else None
+    traffic = traffic_record(src) if (args.workload == "llama13b" and not args.window) else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_rate(w, args.cpu_units)
@@ -432,6 +446,7 @@ def run_ours(args):
                                                              (1 if w.kv == "fp8" else 2) / 2 ** 30, 2),
                    "l2": "no flush: inputs (the KV pool) larger than L2",
                    "partition_tokens": args.partition or "auto", "parallelism": f"replica x{world}",
+                   "window": args.window or None,
                    "step": "kv_append + paged_decode_attention" if args.unfused
                            else "paged_decode_attention_append (fused)"},
         "pct_of_peak": 100.0 * value / world / peak,
@@ -458,6 +473,61 @@ def run_ours(args):
     return 0
 
 
+def run_swap(args):
+    """Block-swap bandwidth: one LLaMA-13B-shaped sequence (2048 tokens = 128 blocks, all 40
+    layers, K and V: 1.68 GB) moved to pinned host memory and back per step."""
+    import numpy as np
+    import torch
+
+    import workloads as W
+    from paged_kv_cache_169_gb300 import build as B
+    from paged_kv_cache_169_gb300.cache import PagedKVCache
+
+    B.build()
+    w = W.llama13b()
+    L = w.num_layers
+    cache = PagedKVCache(L, w.num_blocks, w.block_size, w.num_heads, w.head_dim, "f16")
+    for t in cache.k + cache.v:
+        t.zero_()
+    perm = W.free_order(w)
+    out_ids = torch.from_numpy(perm[:128].copy()).cuda()
+    in_ids = torch.from_numpy(perm[128:256].copy()).cuda()
+    host = cache.swap_out(out_ids)                       # allocates the pinned image
+    nbytes = host.numel()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        cache.swap_out(out_ids, host)
+        cache.swap_in(host, in_ids)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    t_out = t_in = 0.0
+    for _ in range(args.steps):
+        ev[0].record(stream)
+        cache.swap_out(out_ids, host)
+        ev[1].record(stream)
+        cache.swap_in(host, in_ids)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        t_out += ev[0].elapsed_time(ev[1])
+        t_in += ev[1].elapsed_time(ev[2])
+    err = cache.device_error()
+    if err:
+        raise SystemExit(f"device error bits {err}")
+    out_gbs = nbytes * args.steps / (t_out / 1e3) / 1e9
+    in_gbs = nbytes * args.steps / (t_in / 1e3) / 1e9
+    line = {"metric": "kv block swap GB/s (device <-> pinned host, one 13B-shaped sequence)",
+            "value": 2 * nbytes * args.steps / ((t_out + t_in) / 1e3) / 1e9, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": (t_out + t_in) / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "swap13b", "layers": L, "blocks": 128, "bytes_per_direction": nbytes},
+            "swap_out_gbs": out_gbs, "swap_in_gbs": in_gbs, "gpu_launches": 2 * args.steps}
+    print(json.dumps(line), flush=True)
+    cache.close()
+    del np
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -471,11 +541,14 @@ def main():
     ap.add_argument("--ref-units", type=int, default=768, help="oracle units per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="time kv_append + paged_decode_attention as two calls")
+    ap.add_argument("--window", type=int, default=0, help="sliding-window decode over the last N tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "swap13b":
+        return run_swap(args)
     return run_ours(args)
 
 
