@@ -83,9 +83,9 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel_src: str):
-    """DRAM bytes per launch from the committed ncu summary, only if the kernel source
-    is unchanged since the counters were taken."""
+def traffic_record(kernel_srcs):
+    """DRAM bytes per launch from the committed ncu summary, only if the kernel sources
+    (device code and its launch code) are unchanged since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "attention_llama13b_traffic.txt")
     try:
         rec = {}
@@ -93,7 +93,7 @@ def traffic_record(kernel_src: str):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 rec[k.strip()] = v.strip()
-        h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+        h = hashlib.sha256(b"".join(open(f, "rb").read() for f in kernel_srcs)).hexdigest()[:16]
         if rec.get("source_sha256_16") == h:
             return float(rec["dram_bytes_per_launch"])
     except Exception:
@@ -429,7 +429,8 @@ def run_ours(args):
     value = job_throughput(world, step_bytes, args.steps, elapsed_ms)
     peak, peak_src = measured_peak()
     achieved = call_bytes / (attn_ms_mean / 1e3) / 1e9
-    src = os.path.join(ROOT, "paged_kv_cache_169_gb300", "csrc", "decode_attention.cu")
+    src = [os.path.join(ROOT, "paged_kv_cache_169_gb300", "csrc", f)
+           for f in ("attention_kernel.cuh", "decode_attention.cu")]
     traffic = traffic_record(src) if (args.workload == "llama13b" and not args.window) else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -195,7 +195,7 @@ KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int ma
  *   max_context   host upper bound of context_lens (sizes the split-context workspace).
  *   scale         score multiplier, usually 1/sqrt(head_dim); finite and > 0.
  *   partition_tokens  0 = library choice; else tokens per split-context partition,
- *                 a multiple of 32 and at most 32*B.  Sequences longer than one
+ *                 a multiple of 32.  Sequences longer than one
  *                 partition are split, attended per partition and merged exactly
  *                 (log-sum-exp) by a second kernel.
  *   workspace     device, >= paged_decode_workspace_size(...) bytes, 256-byte aligned,

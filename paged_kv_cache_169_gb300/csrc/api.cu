@@ -24,11 +24,53 @@ bool valid_desc(const kv_pool_desc* d) {
 
 void free_pool(kv_pool* p) {
     if (!p) return;
+    std::free(p->tmaps_raw);
     std::free(p->k_layers);
     std::free(p->v_layers);
     std::free(p->k_scales);
     std::free(p->v_scales);
     delete p;
+}
+
+// Tensor maps of an fp16, head_dim 128 pool for the grouped-query tensor-core path:
+// each layer's K and V viewed as [rows][2][64] fp16 (rows = num_blocks*H*B, a row being one
+// token of one head), box {64, 2, min(B, 16)}, 128-byte swizzle.  Leaves p->tmaps null if
+// the driver's encoder is unavailable or refuses (the CUDA-core path then serves).
+void make_tensor_maps(kv_pool* p) {
+    const kv_pool_desc& d = p->desc;
+    if (d.dtype != KV_F16 || d.head_dim != 128) return;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return;
+    }
+    using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    Encode encode = reinterpret_cast<Encode>(fn);
+    const int L = d.num_layers;
+    void* raw = std::malloc(2 * L * sizeof(CUtensorMap) + 64);
+    if (!raw) return;
+    CUtensorMap* maps = reinterpret_cast<CUtensorMap*>((reinterpret_cast<uintptr_t>(raw) + 63) & ~uintptr_t(63));
+    const cuuint64_t dims[3] = {64, 2, static_cast<cuuint64_t>(d.num_blocks) * d.num_heads * d.block_size};
+    const cuuint64_t strides[2] = {128, 256};
+    const cuuint32_t box[3] = {64, 2, static_cast<cuuint32_t>(d.block_size < 16 ? d.block_size : 16)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    for (int l = 0; l < L; ++l) {
+        for (int kv = 0; kv < 2; ++kv) {
+            void* base = kv == 0 ? p->k_layers[l] : p->v_layers[l];
+            if (encode(&maps[2 * l + kv], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+                std::free(raw);
+                return;
+            }
+        }
+    }
+    p->tmaps = maps;
+    p->tmaps_raw = raw;
 }
 
 }  // namespace
@@ -95,6 +137,7 @@ int kv_pool_create(const kv_pool_desc* desc, void* const* k_layers, void* const*
         free_pool(p);
         return KV_ERR_CUDA;
     }
+    make_tensor_maps(p);
     *out = p;
     return KV_OK;
 }

@@ -44,6 +44,8 @@
 namespace kvp {
 
 struct AttnArgs {
+    CUtensorMap kmap;      // tensor-core path: the layer's K and V as swizzled tiles
+    CUtensorMap vmap;
     char* kpool;           // written only by the fused append (the new token's slot)
     char* vpool;
     const float* kscale;
@@ -108,15 +110,19 @@ template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_
 #endif
 
 // G_: query heads per KV head (grouped-query attention; 1 = one query per KV head).
-template <int D_, typename KV_, typename QT_, int G_ = 1>
+// MMA_: grouped-query tensor-core consumer (fp16, head_dim 128, G >= 2) fed by swizzled
+// tensor-map copies.
+template <int D_, typename KV_, typename QT_, int G_ = 1, bool MMA_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int G = G_;
+    static constexpr bool MMA = MMA_;
+    static_assert(!MMA || (sizeof(KV_) == 2 && D_ == 128 && G_ >= 2), "tensor-core path: fp16, d 128, G >= 2");
     using KV = KV_;
     using QT = QT_;
     static constexpr int ESZ = sizeof(KV);
     static constexpr bool FP8 = (ESZ == 1);
-    static constexpr int CT = G >= 4 ? 16 : Tune<ESZ>::CT;   // bounds G*CT/2 partial sums per lane
+    static constexpr int CT = (G >= 4 || MMA) ? 16 : Tune<ESZ>::CT;   // bounds G*CT/2 sums per lane
     static constexpr int TPL = CT / 2;                    // tokens per lane per chunk
     static constexpr int DPL = D / 16;                    // dims per lane
     static constexpr int CBMAX = CT / 8;                  // blocks per chunk at B = 8
@@ -127,24 +133,38 @@ struct Cfg {
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = KV_BYTES;
     static constexpr int Q_OFF = 2 * KV_BYTES;
-    static constexpr int SC_OFF = Q_OFF + Q_BYTES;
-    static constexpr int META_OFF = SC_OFF + SC_BYTES;
-    static constexpr int STAGE = round_up(META_OFF + (int)sizeof(Meta), 128);
+    // the tensor-core path keeps its 1024-aligned stages to exactly K and V (8 KiB): its
+    // query rows go to a region of their own, one slot per stage
+    static constexpr int Q_STAGE = MMA ? 0 : Q_BYTES;
+    static constexpr int QR_BYTES = MMA ? Q_BYTES : 0;
+    static constexpr int SC_OFF = Q_OFF + Q_STAGE;
+    // the tensor-core path's stages hold 128-byte-swizzled rows: 1024-byte aligned
+    static constexpr int STAGE = round_up(SC_OFF + SC_BYTES, MMA ? 1024 : 128);
     static constexpr int NC_AUTO = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
     // more query heads per warp need more registers: fewer consumer warps
-    static constexpr int NC = G == 1 ? (Tune<ESZ>::NC ? Tune<ESZ>::NC : NC_AUTO)
-                                     : (G == 2 ? 12 : (G == 4 ? 8 : 6));
+#if defined(KVP_MMA_NC)
+    static constexpr int NC_MMA = KVP_MMA_NC;      // tuning sweeps only
+#else
+    static constexpr int NC_MMA = 7;               // 8 warps: the register cap stays at 255
+#endif
+    static constexpr int NC = MMA ? NC_MMA
+                                  : G == 1 ? (Tune<ESZ>::NC ? Tune<ESZ>::NC : NC_AUTO)
+                                           : (G == 2 ? 12 : (G == 4 ? 8 : 6));
     // stages that fit beside the prefix table and the barriers
-    static constexpr int NSW_FIT = (227 * 1024 - 2 * kMaxBatch * 4 - 1024) / (NC * STAGE);
-    static constexpr int NSW = Tune<ESZ>::NSW ? Tune<ESZ>::NSW : (NSW_FIT > 4 ? 4 : NSW_FIT);
+    static constexpr int NSW_FIT =
+        (227 * 1024 - 2 * kMaxBatch * 4 - 1024 - (MMA ? 1024 : 0)) / (NC * (STAGE + (int)sizeof(Meta) + QR_BYTES));
+    static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > 4 ? 4 : NSW_FIT);
     static_assert(NSW >= 2, "at least double buffering");
     static constexpr int THREADS = (NC + 1) * 32;
-    static constexpr int BAR_OFF = NC * NSW * STAGE;
+    static constexpr int META_R = NC * NSW * STAGE;                   // one Meta per stage
+    static constexpr int QR_OFF = META_R + NC * NSW * (int)sizeof(Meta);   // MMA: one q slot per stage
+    static constexpr int BAR_OFF = QR_OFF + NC * NSW * QR_BYTES;
     static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
-    static constexpr int SMEM = PREFIX_OFF + 2 * kMaxBatch * 4;
+    static constexpr int ALIGN_SLACK = MMA ? 1024 : 0;           // to 1024-align the base
+    static constexpr int SMEM = PREFIX_OFF + 2 * kMaxBatch * 4 + ALIGN_SLACK;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(NC <= 32 && (CT == 16 || CT == 32), "launch shape");
-    static_assert(Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && META_OFF % 16 == 0, "alignment");
+    static_assert(Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && META_R % 16 == 0 && QR_OFF % 16 == 0, "alignment");
 };
 
 
@@ -280,36 +300,54 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
 // Split-context merge of the np partials of one (sequence, head), by one warp:
 // M = max m_p, L = sum l_p 2^(m_p - M), out = sum o_p 2^(m_p - M) / L.
 // The partials were written by other SMs; they are read through L2 (ld.global.cg).
-template <int D>
-__device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh, int np, int lane) {
-    constexpr int DW = D / 32;
-    const int64_t base = sh * a.max_parts;
+template <int D, int G>
+__device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, int np, int lane) {
+    // merges the np partials of the G query heads sh0 .. sh0+G-1 at once: 32/G lanes per
+    // head, so every lane's loads are independent and all heads' loads are in flight
+    // together (a merge sits on the critical path of its item)
+    constexpr int LPH = 32 / G;                     // lanes per query head
+    constexpr int DL = D / LPH;                     // dims per lane
+    constexpr int VEC = DL % 4 == 0 ? 4 : 2;
+    constexpr int UNR = G == 1 ? 4 : 2;
+    const int g = lane / LPH, q = lane % LPH;
+    const int64_t base = (sh0 + g) * a.max_parts;
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + base;
     float mx = -CUDART_INF_F;
-    for (int p = lane; p < np; p += 32) mx = fmaxf(mx, __ldcg(ml + p).x);
-    mx = warp_max(mx);
-    float L = 0.f, acc[DW];
+    for (int p = q; p < np; p += LPH) mx = fmaxf(mx, __ldcg(ml + p).x);
     #pragma unroll
-    for (int i = 0; i < DW; ++i) acc[i] = 0.f;
-    #pragma unroll 4
+    for (int off = LPH / 2; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
+    float L = 0.f, acc[DL];
+    #pragma unroll
+    for (int i = 0; i < DL; ++i) acc[i] = 0.f;
+    #pragma unroll UNR
     for (int p = 0; p < np; ++p) {
         const float2 v = __ldcg(ml + p);
         const float wgt = ex2_approx(v.x - mx);
         L = fmaf(v.y, wgt, L);
-        const float* o = a.part_o + (base + p) * D + lane * DW;
-        if constexpr (DW == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
-            acc[0] = fmaf(wgt, x.x, acc[0]); acc[1] = fmaf(wgt, x.y, acc[1]);
-            acc[2] = fmaf(wgt, x.z, acc[2]); acc[3] = fmaf(wgt, x.w, acc[3]);
-        } else {
-            const float2 x = __ldcg(reinterpret_cast<const float2*>(o));
-            acc[0] = fmaf(wgt, x.x, acc[0]); acc[1] = fmaf(wgt, x.y, acc[1]);
+        const float* o = a.part_o + (base + p) * D;
+        #pragma unroll
+        for (int i = 0; i < DL / VEC; ++i) {
+            if constexpr (VEC == 4) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(o) + i * LPH + q);
+                acc[4 * i] = fmaf(wgt, x.x, acc[4 * i]); acc[4 * i + 1] = fmaf(wgt, x.y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(wgt, x.z, acc[4 * i + 2]); acc[4 * i + 3] = fmaf(wgt, x.w, acc[4 * i + 3]);
+            } else {
+                const float2 x = __ldcg(reinterpret_cast<const float2*>(o) + i * LPH + q);
+                acc[2 * i] = fmaf(wgt, x.x, acc[2 * i]); acc[2 * i + 1] = fmaf(wgt, x.y, acc[2 * i + 1]);
+            }
         }
     }
     const float inv = 1.f / L;
-    float* out = a.out + sh * D + lane * DW;
+    float* out = a.out + (sh0 + g) * D;
     #pragma unroll
-    for (int i = 0; i < DW; ++i) out[i] = acc[i] * inv;
+    for (int i = 0; i < DL / VEC; ++i) {
+        if constexpr (VEC == 4) {
+            reinterpret_cast<float4*>(out)[i * LPH + q] =
+                make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+        } else {
+            reinterpret_cast<float2*>(out)[i * LPH + q] = make_float2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+        }
+    }
 }
 
 // Fused append: lane's D/32 elements of one new-token row (src, in_bytes per element)
@@ -363,11 +401,190 @@ __device__ __forceinline__ void patch_row(const char* src, int in_bytes, char* s
     }
 }
 
+// Byte offset inside a 128-byte-swizzled stage of element byte `off` of the logical
+// [token][256 B] layout (tensor-map copies swap 16-byte chunks within each 128-byte row
+// by the row's index mod 8).
+__device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Grouped-query consumer on the tensor cores (fp16, head_dim 128, G query heads per K/V
+// head).  Per 16-token chunk, with queries as the M dimension (G real rows of 16) and
+// tokens as N:
+//   S  = Q K^T        8 k-steps x 2 token tiles of mma.m16n8k16; K fragments by ldmatrix
+//   softmax           rows owned by the 4 lanes of a quad (lane/4 = query, lane%4 = tokens)
+//   O += P V          P re-used from the S accumulators as fp16 A fragments; V fragments
+//                     by ldmatrix.trans; 16 dim tiles of 8
+// fp32 accumulation and softmax, exact running max.
 template <typename C>
-__global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(AttnArgs a) {
+__device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, const int* s_ctx, int w, int lane) {
+    constexpr int NSW = C::NSW, D = C::D, G = C::G, CT = C::CT;
+    static_assert(CT == 16 && D == 128, "tensor-core consumer shape");
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    const int g = lane >> 2, t = lane & 3;          // accumulator row (query) / column pair
+    uint32_t qa[8][2];
+    float o[16][4];
+    float m = -CUDART_INF_F, l = 0.f;
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) { qa[i][0] = 0u; qa[i][1] = 0u; }
+    #pragma unroll
+    for (int j = 0; j < 16; ++j) { o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f; }
+
+    for (int j = 0;; ++j) {
+        const int st = j % NSW;
+        const uint32_t par = (j / NSW) & 1;
+        const uint32_t fb = smem_u32(&bars[w * NSW + st]);
+        if (!mbar_wait_bounded(fb, par, a.err)) {
+            mbar_wait_bounded(fb, par, a.err);      // let copies in flight land, then leave
+            break;
+        }
+        char* stg = smem + (w * NSW + st) * C::STAGE;
+        const Meta* mp = reinterpret_cast<const Meta*>(smem + C::META_R + (w * NSW + st) * sizeof(Meta));
+        const int flags = mp->flags;
+        if (flags & F_TERM) break;
+        const int nt = mp->ntok, lo = mp->lo, ms = mp->s, mh = mp->h, mpart = mp->p;
+        const uint32_t kbase = smem_u32(stg + C::K_OFF), vbase = smem_u32(stg + C::V_OFF);
+        if (flags & F_FIRST) {
+            m = -CUDART_INF_F;
+            l = 0.f;
+            #pragma unroll
+            for (int jj = 0; jj < 16; ++jj) { o[jj][0] = o[jj][1] = o[jj][2] = o[jj][3] = 0.f; }
+            // A fragments of the G query rows (staged with the item's first chunk)
+            const bool real = g < G && nt > 0;
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES + (real ? g : 0) * D * 2);
+            #pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                qa[k][0] = real ? qrow[8 * k + t] : 0u;
+                qa[k][1] = real ? qrow[8 * k + 4 + t] : 0u;
+            }
+        }
+        if (flags & F_PATCH) {
+            // the new token's row, into the swizzled stage and into the pool slot
+            const int r = mp->patch_row;
+            const int64_t sh = static_cast<int64_t>(ms) * a.H + mh;
+            const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + mh) * a.B + mp->patch_off;
+            const int e0 = lane * 4;
+            const uint2 kv = *reinterpret_cast<const uint2*>(a.k_new + (sh * D + e0) * 2);
+            const uint2 vv = *reinterpret_cast<const uint2*>(a.v_new + (sh * D + e0) * 2);
+            const uint32_t so = swz128(static_cast<uint32_t>(r * 256 + e0 * 2));
+            *reinterpret_cast<uint2*>(stg + C::K_OFF + so) = kv;
+            *reinterpret_cast<uint2*>(stg + C::V_OFF + so) = vv;
+            *reinterpret_cast<uint2*>(a.kpool + grow * C::ROW + e0 * 2) = kv;
+            *reinterpret_cast<uint2*>(a.vpool + grow * C::ROW + e0 * 2) = vv;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+        }
+        if (nt > 0) {
+            if (nt < CT || lo > 0) {
+                // rows outside [lo, nt) may hold anything (unused slots): zero their V so
+                // that p = 0 rows contribute exactly nothing to P V
+                #pragma unroll 1
+                for (int r = 0; r < CT; ++r)
+                    if ((r < lo || r >= nt) && lane < 16)
+                        *reinterpret_cast<uint4*>(stg + C::V_OFF + r * 256 + lane * 16) = make_uint4(0, 0, 0, 0);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            // S = Q K^T
+            float sacc[2][4];
+            #pragma unroll
+            for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+            const int mi = lane >> 3, mr = lane & 7;
+            #pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                // matrices: (tok 0-7, dims 16k..+7) (tok 0-7, +8..) (tok 8-15, 16k..) (tok 8-15, +8..)
+                const int tok = (mi >> 1) * 8 + mr, cp = 2 * k + (mi & 1);
+                uint32_t kb[4];
+                ldsm_x4(kbase + swz128(static_cast<uint32_t>(tok * 256 + (cp >> 3) * 128 + (cp & 7) * 16)), kb);
+                mma_16816(sacc[0], qa[k][0], 0u, qa[k][1], 0u, kb[0], kb[1]);
+                mma_16816(sacc[1], qa[k][0], 0u, qa[k][1], 0u, kb[2], kb[3]);
+            }
+            // row g: tokens 2t, 2t+1 (tile 0) and 8+2t, 9+2t (tile 1); log2-domain scores
+            float x[4] = {sacc[0][0] * a.qscale, sacc[0][1] * a.qscale, sacc[1][0] * a.qscale,
+                          sacc[1][1] * a.qscale};
+            const int tk[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+            float mx = -CUDART_INF_F;
+            #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[i] = (tk[i] >= lo && tk[i] < nt) ? x[i] : -CUDART_INF_F;
+                mx = fmaxf(mx, x[i]);
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+            const float m_new = fmaxf(m, mx);
+            const float corr = ex2_approx(m - m_new);
+            float pr[4], ps = 0.f;
+            #pragma unroll
+            for (int i = 0; i < 4; ++i) { pr[i] = ex2_approx(x[i] - m_new); ps += pr[i]; }
+            l = fmaf(l, corr, ps);
+            #pragma unroll
+            for (int jj = 0; jj < 16; ++jj) { o[jj][0] *= corr; o[jj][1] *= corr; }
+            m = m_new;
+            const uint32_t pa0 = pack_half2(pr[0], pr[1]), pa2 = pack_half2(pr[2], pr[3]);
+            // O += P V
+            #pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                // matrices: (tok 0-7, dims 16jj..) (tok 8-15, 16jj..) (tok 0-7, +8..) (tok 8-15, +8..)
+                const int tok = (mi & 1) * 8 + mr, cp = 2 * jj + (mi >> 1);
+                uint32_t vb[4];
+                ldsm_x4_t(vbase + swz128(static_cast<uint32_t>(tok * 256 + (cp >> 3) * 128 + (cp & 7) * 16)), vb);
+                mma_16816(o[2 * jj], pa0, 0u, pa2, 0u, vb[0], vb[1]);
+                mma_16816(o[2 * jj + 1], pa0, 0u, pa2, 0u, vb[2], vb[3]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars[C::NC * NSW + w * NSW + st]));
+        if (flags & F_LAST) {
+            float lr = l + __shfl_xor_sync(FULL, l, 1);
+            lr += __shfl_xor_sync(FULL, lr, 2);
+            const int64_t shk = static_cast<int64_t>(ms) * a.H + mh;
+            const int64_t sq = shk * G + g;
+            if (flags & F_SINGLE) {
+                if (g < G) {
+                    const float inv = nt > 0 ? 1.f / lr : 0.f;
+                    float* dst = a.out + sq * D + 2 * t;
+                    #pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        *reinterpret_cast<float2*>(dst + 8 * jj) =
+                            nt > 0 ? make_float2(o[jj][0] * inv, o[jj][1] * inv) : make_float2(0.f, 0.f);
+                }
+            } else {
+                if (g < G) {
+                    const int64_t idx = sq * a.max_parts + mpart;
+                    if (t == 0) {
+                        a.part_ml[2 * idx] = m;
+                        a.part_ml[2 * idx + 1] = lr;
+                    }
+                    float* dst = a.part_o + idx * D + 2 * t;
+                    #pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) *reinterpret_cast<float2*>(dst + 8 * jj) = make_float2(o[jj][0], o[jj][1]);
+                }
+                __syncwarp();
+                unsigned prev = 0;
+                if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + shk, 1u);
+                prev = __shfl_sync(FULL, prev, 0);
+                const int ctx_s = s_ctx[ms];
+                const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
+                if (prev == static_cast<unsigned>(np - 1)) {
+                    __syncwarp();
+                    merge_partials<D, G>(a, shk * G, np, lane);
+                }
+            }
+        }
+    }
+}
+
+template <typename C>
+__global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(const __grid_constant__ AttnArgs a) {
     constexpr int NC = C::NC, NSW = C::NSW, D = C::D, CT = C::CT, TPL = C::TPL, DPL = C::DPL;
     constexpr int CBMAX = C::CBMAX;
-    extern __shared__ __align__(128) char smem[];
+    extern __shared__ __align__(128) char smem_raw[];
+    // swizzled stages need a 1024-byte aligned base (the slack is part of C::SMEM)
+    char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) * (C::MMA ? 1 : 0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);   // full[NC*NSW], empty[NC*NSW]
     int* s_ctx = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
     int* s_end = s_ctx + kMaxBatch;
@@ -416,12 +633,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
         const int w = mine ? lane : 0;
         const int rpc = a.B < CT ? a.B : CT;           // token rows per copy (whole block if B <= CT)
         const uint32_t tile = static_cast<uint32_t>(rpc) * C::ROW;
-        unsigned pending = 0;                          // next item index (atomic in flight)
-        if (mine) pending = atomicAdd(a.counter, 1u);
-        auto take = [&]() {
-            const int idx = static_cast<int>(pending);
-            pending = atomicAdd(a.counter, 1u);
-            return decode_item<CT>(idx, n_items, s_ctx, s_end, a.batch, a.H, a.P, a.window, rpc);
+        // Items are claimed one at a time: the next one only while the current item's last
+        // two chunks are filled (its atomic then has a chunk's time to return), so no lane
+        // holds more than two items and the tail stays balanced when items are few.
+        unsigned pending = 0;                          // claimed next item (atomic in flight)
+        bool claimed = false;
+        auto claim = [&]() { pending = atomicAdd(a.counter, 1u); claimed = true; };
+        auto decode = [&](unsigned idx) {
+            return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, a.H, a.P, a.window, rpc);
         };
         int ids[CBMAX];
         auto load_ids = [&](const Item& it, int chunk) {
@@ -432,12 +651,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
             #pragma unroll
             for (int j = 0; j < CBMAX; ++j) ids[j] = j < ncp ? a.tables[row + (t0 + j * rpc) / a.B] : 0;
         };
-        Item cur{}, nxt{};
+        Item cur{};
         int c = 0, fills = 0;
         bool alive = mine;
         if (mine) {
-            cur = take();
-            if (cur.valid) nxt = take();
+            cur = decode(atomicAdd(a.counter, 1u));
+            if (cur.valid && cur.nchunks == 1) claim();
             load_ids(cur, 0);
         }
         bool failed = false;
@@ -448,7 +667,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
             if (alive) ready = mbar_test_wait(empty_bar(w, st), ((fills / NSW) & 1) ^ 1);
             if (ready) {
                 char* stg = stage_ptr(w, st);
-                Meta* meta = reinterpret_cast<Meta*>(stg + C::META_OFF);
+                Meta* meta = reinterpret_cast<Meta*>(smem + C::META_R + (w * NSW + st) * sizeof(Meta));
                 const uint32_t fb = full_bar(w, st);
                 if (!cur.valid) {
                     meta->flags = F_TERM;
@@ -496,20 +715,34 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
                         if (j < nblk) {
                             const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h) * a.B +
                                                   row0) * C::ROW;
-                            bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
-                            bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
+                            if constexpr (C::MMA) {
+                                // rpc token rows of one head as [rows][2][64], 128-byte swizzled
+                                const int row = static_cast<int>(toff / C::ROW);
+                                tma_load_3d(dst + C::K_OFF + j * tile, &a.kmap, 0, 0, row, fb);
+                                tma_load_3d(dst + C::V_OFF + j * tile, &a.vmap, 0, 0, row, fb);
+                            } else {
+                                bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
+                                bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
+                            }
                         }
                     }
                     if (with_q) {
                         const char* qsrc = static_cast<const char*>(a.q) +
                                            (static_cast<int64_t>(cur.s) * a.H + cur.h) * C::Q_BYTES;
-                        bulk_g2s(dst + C::Q_OFF, qsrc, C::Q_BYTES, fb);
+                        const uint32_t qdst = C::MMA ? smem_u32(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES)
+                                                     : dst + C::Q_OFF;
+                        bulk_g2s(qdst, qsrc, C::Q_BYTES, fb);
                     }
-                    if (++c == cur.nchunks) {
-                        cur = nxt;
+                    const int rem = cur.nchunks - 1 - c;      // chunks of cur still to fill
+                    if (rem == 1 && !claimed) claim();
+                    if (rem == 0) {
+                        if (!claimed) claim();
+                        cur = decode(pending);
+                        claimed = false;
                         c = 0;
-                        nxt = Item{};
-                        if (cur.valid) nxt = take();
+                        if (cur.valid && cur.nchunks == 1) claim();
+                    } else {
+                        ++c;
                     }
                     load_ids(cur, c);                  // used at this lane's next fill
                 }
@@ -539,6 +772,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
     }
 
     // ==================================================================== consumer
+    if constexpr (C::MMA) {
+        consumer_mma<C>(a, smem, s_ctx, warp, lane);
+        return;
+    }
     constexpr int G = C::G;
     const int w = warp;
     const int half = lane >> 4;                 // which token of each row pair
@@ -564,15 +801,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
             break;
         }
         const char* stg = stage_ptr(w, st);
+        const char* mst = smem + C::META_R + (w * NSW + st) * sizeof(Meta);
         struct { int s, h, p, ntok, flags; } meta;
         {
-            const int4 m0 = *reinterpret_cast<const int4*>(stg + C::META_OFF);
+            const int4 m0 = *reinterpret_cast<const int4*>(mst);
             meta.s = m0.x; meta.h = m0.y; meta.p = m0.z; meta.ntok = m0.w;
-            meta.flags = reinterpret_cast<const Meta*>(stg + C::META_OFF)->flags;
+            meta.flags = reinterpret_cast<const Meta*>(mst)->flags;
         }
         if (meta.flags & F_TERM) break;
         const int nt = meta.ntok;
-        const int lo = reinterpret_cast<const Meta*>(stg + C::META_OFF)->lo;
+        const int lo = reinterpret_cast<const Meta*>(mst)->lo;
         if (meta.flags & F_FIRST) {
             #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -585,7 +823,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
         }
         if (meta.flags & F_PATCH) {
             // this warp owns the stage now: put the new token into its row and its slot
-            const Meta* mp = reinterpret_cast<const Meta*>(stg + C::META_OFF);
+            const Meta* mp = reinterpret_cast<const Meta*>(mst);
             const int r = mp->patch_row;
             const int64_t sh = static_cast<int64_t>(meta.s) * a.H + meta.h;
             const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + meta.h) * a.B + mp->patch_off;
@@ -608,8 +846,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
             if constexpr (C::FP8) {
                 // per-block scales of this lane's token, loaded now and used after the dot
                 // products; the producer validated the ids
-                const int id = reinterpret_cast<const Meta*>(stg + C::META_OFF)
-                                   ->ids[tok_l / (a.B < CT ? a.B : CT)];
+                const int id = reinterpret_cast<const Meta*>(mst)->ids[tok_l / (a.B < CT ? a.B : CT)];
                 ks = __ldg(a.kscale + id);
                 vs = __ldg(a.vscale + id);
             }
@@ -713,17 +950,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(Attn
             }
             if (!(meta.flags & F_SINGLE)) {
                 // publish the partials, then take a ticket; the last partition merges
-                __threadfence();
                 __syncwarp();
                 unsigned prev = 0;
-                if (lane == 0) prev = atomicAdd(a.arrivals + shk, 1u);
+                if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + shk, 1u);
                 prev = __shfl_sync(FULL, prev, 0);
                 const int ctx_s = s_ctx[meta.s];
                 const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
                 if (prev == static_cast<unsigned>(np - 1)) {
-                    __threadfence();
-                    #pragma unroll 1
-                    for (int g = 0; g < G; ++g) merge_partials<D>(a, shk * G + g, np, lane);
+                    __syncwarp();
+                    merge_partials<D, G>(a, shk * G, np, lane);
                 }
             }
         }

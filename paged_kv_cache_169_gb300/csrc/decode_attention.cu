@@ -11,7 +11,12 @@ template <typename C>
 int consumers_of() { return C::NC; }
 
 template <int G>
-int consumers_for_g(const kv_pool_desc& d) {
+int consumers_for_g(const kv_pool* pool) {
+    const kv_pool_desc& d = pool->desc;
+    if constexpr (G > 1) {                         // grouped-query tensor-core configuration
+        if (d.dtype == KV_F16 && d.head_dim == 128 && pool->tmaps)
+            return consumers_of<Cfg<128, __half, __half, G, true>>();
+    }
     if constexpr (G == 1) {                        // fp32 pools have no grouped path
         if (d.dtype == KV_F32) return d.head_dim == 128 ? consumers_of<Cfg<128, float, float>>()
                                                         : consumers_of<Cfg<64, float, float>>();
@@ -22,12 +27,12 @@ int consumers_for_g(const kv_pool_desc& d) {
                              : consumers_of<Cfg<64, uint8_t, __half, G>>();
 }
 
-int consumers_for(const kv_pool_desc& d, int group) {
+int consumers_for(const kv_pool* pool, int group) {
     switch (group) {
-        case 2: return consumers_for_g<2>(d);
-        case 4: return consumers_for_g<4>(d);
-        case 8: return consumers_for_g<8>(d);
-        default: return consumers_for_g<1>(d);
+        case 2: return consumers_for_g<2>(pool);
+        case 4: return consumers_for_g<4>(pool);
+        case 8: return consumers_for_g<8>(pool);
+        default: return consumers_for_g<1>(pool);
     }
 }
 
@@ -47,8 +52,8 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     // a sliding window bounds the tokens read per sequence (window + up to 31 masked rows)
     const int span = (window > 0 && window + 32 < max_context) ? window + 32 : max_context;
     if (!valid_group(d, group)) return KV_ERR_INVALID_ARG;
-    const int cap = 32 * d.block_size;             // one producer lane per block of a partition
-    const int nc = consumers_for(d, group);
+    const int cap = 1 << 24;                       // block ids are fetched per chunk: no per-item cap
+    const int nc = consumers_for(pool, group);
     int P;
     if (partition_tokens > 0) {
         if (partition_tokens % kPartAlign != 0 || partition_tokens > cap) return KV_ERR_INVALID_ARG;
@@ -135,6 +140,10 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     a.num_blocks = d.num_blocks;
     a.qscale = scale * 1.4426950408889634f;        // log2(e): softmax evaluated with 2^x
     a.window = plan.window;
+    if (pool->tmaps) {                             // the layer's swizzled tile maps
+        a.kmap = pool->tmaps[2 * layer];
+        a.vmap = pool->tmaps[2 * layer + 1];
+    }
 
     if (group != 1) return launch_attention_grouped(group, pool, a, plan, counters, stream);
     if (d.dtype == KV_F32) {

@@ -12,7 +12,11 @@ int launch_g(const kv_pool* pool, const AttnArgs& a, const AttnPlan& plan, unsig
              cudaStream_t stream) {
     const kv_pool_desc& d = pool->desc;
     if (d.dtype == KV_F16) {
-        if (d.head_dim == 128) return launch_typed<Cfg<128, __half, __half, G>>(pool, a, plan, counters, stream);
+        if (d.head_dim == 128) {
+            // tensor cores when the pool has its swizzled tensor maps, else CUDA cores
+            if (pool->tmaps) return launch_typed<Cfg<128, __half, __half, G, true>>(pool, a, plan, counters, stream);
+            return launch_typed<Cfg<128, __half, __half, G>>(pool, a, plan, counters, stream);
+        }
         return launch_typed<Cfg<64, __half, __half, G>>(pool, a, plan, counters, stream);
     }
     if (d.dtype == KV_FP8_E4M3) {

@@ -1,6 +1,7 @@
 // Internal declarations shared by the kvpaged CUDA translation units.
 #pragma once
 
+#include <cuda.h>            // CUtensorMap (the encode entry point is fetched at run time)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -16,6 +17,11 @@ struct kv_pool {
     float** k_scales;    // FP8 pools only, else nullptr
     float** v_scales;
     int* d_err;          // device error bits (the library's only allocation)
+    // fp16, head_dim 128 pools: per layer a K and a V tensor map of the pool viewed as
+    // [rows = num_blocks*H*B][2][64] halves with a {64, 2, min(B,16)} box and 128-byte
+    // swizzle (the grouped-query tensor-core path); nullptr when unavailable
+    CUtensorMap* tmaps;  // [2 * num_layers], 64-byte aligned
+    void* tmaps_raw;
 };
 
 namespace kvp {
@@ -121,6 +127,45 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// 3-D tiled bulk tensor load global -> shared through a tensor map (param/const/global
+// address), completion counted on the mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// Four 8x8 b16 matrices from shared memory (lane L gives row L%8 of matrix L/8).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
+// D += A(16x16, fp16, row) * B(16x8, fp16, col) with fp32 accumulation.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Arrival ticket with acquire-release semantics at GPU scope: the partials this warp wrote
+// (ordered before the call by __syncwarp) are visible to whoever draws a later ticket, and
+// the caller sees every partial released before its own ticket.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
