@@ -37,6 +37,8 @@ def make_workload(name: str):
         w.lens = [n + w.steps for n in w.lens]       # context after the last of the 64 steps
     elif name == "gqa70b":
         w = W.gqa70b()
+    elif name == "longctx13b":
+        w = W.longctx13b()
     elif name.startswith("ragged"):
         # ragged_f16_b16 | ragged_fp8_b8 ...
         _, dt, b = name.split("_")

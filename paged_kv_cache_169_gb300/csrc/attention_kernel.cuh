@@ -57,7 +57,9 @@ struct AttnArgs {
     float* part_ml;        // [batch*H*max_parts][2]  (m in log2 units, l)
     float* part_o;         // [batch*H*max_parts][D]  unnormalised
     unsigned* counter;
-    unsigned* arrivals;    // [batch*H] partitions finished per (sequence, head)
+    unsigned* arrivals;    // [batch*H] partitions (or partition groups) finished per (sequence, head)
+    unsigned* grp_arrivals;  // [batch*H][n_grp] partitions finished per group of kMergeFan
+    int n_grp;             // ceil(max_parts / kMergeFan) when max_parts > kMergeFan, else 0
     const char* k_new;     // fused append: [batch][H][D] new-token K (nullptr: no append)
     const char* v_new;
     int in_bytes;          // element size of k_new / v_new (2 or 4)
@@ -300,31 +302,35 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
 // Split-context merge of the np partials of one (sequence, head), by one warp:
 // M = max m_p, L = sum l_p 2^(m_p - M), out = sum o_p 2^(m_p - M) / L.
 // The partials were written by other SMs; they are read through L2 (ld.global.cg).
-template <int D, int G>
-__device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, int np, int lane) {
-    // merges the np partials of the G query heads sh0 .. sh0+G-1 at once: 32/G lanes per
-    // head, so every lane's loads are independent and all heads' loads are in flight
-    // together (a merge sits on the critical path of its item)
+template <int D, int G, bool FINAL>
+__device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, int first, int count, int stride,
+                                               int lane) {
+    // merges partials first, first+stride, ... (count of them) of the G query heads
+    // sh0 .. sh0+G-1 at once: 32/G lanes per head, so every lane's loads are independent
+    // and all heads' loads are in flight together (a merge sits on the critical path).
+    // FINAL writes the normalised output; otherwise the merged, still unnormalised
+    // partial (with its m, l) replaces partial `first`.
     constexpr int LPH = 32 / G;                     // lanes per query head
     constexpr int DL = D / LPH;                     // dims per lane
     constexpr int VEC = DL % 4 == 0 ? 4 : 2;
     constexpr int UNR = G == 1 ? 4 : 2;
     const int g = lane / LPH, q = lane % LPH;
-    const int64_t base = (sh0 + g) * a.max_parts;
+    const int64_t base = (sh0 + g) * a.max_parts + first;
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + base;
     float mx = -CUDART_INF_F;
-    for (int p = q; p < np; p += LPH) mx = fmaxf(mx, __ldcg(ml + p).x);
+    for (int k = q; k < count; k += LPH) mx = fmaxf(mx, __ldcg(ml + static_cast<int64_t>(k) * stride).x);
     #pragma unroll
     for (int off = LPH / 2; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
     float L = 0.f, acc[DL];
     #pragma unroll
     for (int i = 0; i < DL; ++i) acc[i] = 0.f;
     #pragma unroll UNR
-    for (int p = 0; p < np; ++p) {
-        const float2 v = __ldcg(ml + p);
+    for (int k = 0; k < count; ++k) {
+        const int64_t row = static_cast<int64_t>(k) * stride;
+        const float2 v = __ldcg(ml + row);
         const float wgt = ex2_approx(v.x - mx);
         L = fmaf(v.y, wgt, L);
-        const float* o = a.part_o + (base + p) * D;
+        const float* o = a.part_o + (base + row) * D;
         #pragma unroll
         for (int i = 0; i < DL / VEC; ++i) {
             if constexpr (VEC == 4) {
@@ -337,8 +343,12 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
             }
         }
     }
-    const float inv = 1.f / L;
-    float* out = a.out + (sh0 + g) * D;
+    const float inv = FINAL ? 1.f / L : 1.f;
+    float* out = FINAL ? a.out + (sh0 + g) * D : a.part_o + base * D;
+    if (!FINAL) {
+        __syncwarp();                                  // every lane has read partial `first`
+        if (q == 0) reinterpret_cast<float2*>(a.part_ml)[base] = make_float2(mx, L);
+    }
     #pragma unroll
     for (int i = 0; i < DL / VEC; ++i) {
         if constexpr (VEC == 4) {
@@ -348,6 +358,36 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
             reinterpret_cast<float2*>(out)[i * LPH + q] = make_float2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
         }
     }
+}
+
+// Partition p of (sequence, KV head) shk has written its partials: publish them and take
+// a ticket.  Up to kMergeFan partitions merge in one step, by the warp that finishes last.
+// Longer splits merge in two levels, which shortens the merge that ends the split: the
+// last finisher of each group of kMergeFan partitions folds the group into the group's
+// first slot, and the last group to fold merges the ceil(np / kMergeFan) groups.
+template <int D, int G>
+__device__ __forceinline__ void finish_partition(const AttnArgs& a, int64_t shk, int p, int np, int lane) {
+    __syncwarp();
+    int count = np, stride = 1;
+    if (np > kMergeFan) {
+        const int grp = p / kMergeFan;
+        const int gsz = min(kMergeFan, np - grp * kMergeFan);
+        unsigned prev = 0;
+        if (lane == 0) prev = atom_add_acq_rel_gpu(a.grp_arrivals + shk * a.n_grp + grp, 1u);
+        prev = __shfl_sync(FULL, prev, 0);
+        if (prev != static_cast<unsigned>(gsz - 1)) return;
+        __syncwarp();
+        merge_partials<D, G, false>(a, shk * G, grp * kMergeFan, gsz, 1, lane);
+        __syncwarp();
+        count = (np + kMergeFan - 1) / kMergeFan;
+        stride = kMergeFan;
+    }
+    unsigned prev = 0;
+    if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + shk, 1u);
+    prev = __shfl_sync(FULL, prev, 0);
+    if (prev != static_cast<unsigned>(count - 1)) return;
+    __syncwarp();
+    merge_partials<D, G, true>(a, shk * G, 0, count, stride, lane);
 }
 
 // Fused append: lane's D/32 elements of one new-token row (src, in_bytes per element)
@@ -563,16 +603,9 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                     #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) *reinterpret_cast<float2*>(dst + 8 * jj) = make_float2(o[jj][0], o[jj][1]);
                 }
-                __syncwarp();
-                unsigned prev = 0;
-                if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + shk, 1u);
-                prev = __shfl_sync(FULL, prev, 0);
                 const int ctx_s = s_ctx[ms];
                 const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
-                if (prev == static_cast<unsigned>(np - 1)) {
-                    __syncwarp();
-                    merge_partials<D, G>(a, shk * G, np, lane);
-                }
+                finish_partition<D, G>(a, shk, mpart, np, lane);
             }
         }
     }
@@ -950,16 +983,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             }
             if (!(meta.flags & F_SINGLE)) {
                 // publish the partials, then take a ticket; the last partition merges
-                __syncwarp();
-                unsigned prev = 0;
-                if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + shk, 1u);
-                prev = __shfl_sync(FULL, prev, 0);
                 const int ctx_s = s_ctx[meta.s];
                 const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
-                if (prev == static_cast<unsigned>(np - 1)) {
-                    __syncwarp();
-                    merge_partials<D, G>(a, shk * G, np, lane);
-                }
+                finish_partition<D, G>(a, shk, meta.p, np, lane);
             }
         }
     }

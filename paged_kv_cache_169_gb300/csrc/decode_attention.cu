@@ -53,21 +53,32 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     const int span = (window > 0 && window + 32 < max_context) ? window + 32 : max_context;
     if (!valid_group(d, group)) return KV_ERR_INVALID_ARG;
     const int cap = 1 << 24;                       // block ids are fetched per chunk: no per-item cap
+    constexpr int kAutoPartMax = 1024;             // library choice: at most 1024 tokens per item
     const int nc = consumers_for(pool, group);
     int P;
     if (partition_tokens > 0) {
         if (partition_tokens % kPartAlign != 0 || partition_tokens > cap) return KV_ERR_INVALID_ARG;
         P = partition_tokens;
     } else if (partition_tokens == 0) {
-        // work items are (sequence, KV head, partition): aim at >= 8 per consumer warp
+        // work items are (sequence, KV head, partition), handed out dynamically
         const int64_t units = static_cast<int64_t>(batch > 0 ? batch : 1) * d.num_heads;
-        const int64_t target = 8ll * pool->num_sms * nc;
-        int64_t parts = (target + units - 1) / units;
+        const int64_t warps = static_cast<int64_t>(pool->num_sms) * nc;
+        int64_t parts;
+        if (group == 1) {
+            // about 8 items per consumer warp, so the dynamic hand-out evens out the tail
+            parts = (8 * warps + units - 1) / units;
+        } else {
+            // an item of a grouped launch also stages G query rows and writes (and merges)
+            // G partial rows: fewer, longer items, about one round of them
+            parts = warps / units;
+        }
         if (parts < 1) parts = 1;
         int64_t p = (span + parts - 1) / parts;
         p = (p + kPartAlign - 1) / kPartAlign * kPartAlign;
         if (p < kPartAlign) p = kPartAlign;
-        if (p > cap) p = cap;
+        // the longest item bounds the tail when contexts are ragged (the host sees only
+        // the longest context)
+        if (p > kAutoPartMax) p = kAutoPartMax;
         P = static_cast<int>(p);
     } else {
         return KV_ERR_INVALID_ARG;
@@ -80,7 +91,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     size_t ws = 256;                                // kMaxSub work counters
     if (plan->max_parts > 1) {
         const size_t n = static_cast<size_t>(batch) * d.num_heads * group * plan->max_parts;
-        ws += align256(static_cast<size_t>(batch) * d.num_heads * sizeof(unsigned));   // arrivals
+        ws += plan->arrivals_bytes(batch, d.num_heads);
         ws += align256(n * 2 * sizeof(float));
         ws += align256(n * d.head_dim * sizeof(float));
     }
@@ -105,8 +116,7 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     const int group = plan.group;
     char* ws = static_cast<char*>(workspace);
     unsigned* counters = reinterpret_cast<unsigned*>(ws);
-    const size_t arrivals_bytes =
-        plan.max_parts > 1 ? align256(static_cast<size_t>(batch) * d.num_heads * sizeof(unsigned)) : 0;
+    const size_t arrivals_bytes = plan.arrivals_bytes(batch, d.num_heads);
     // work counters and per-(sequence, KV head) arrival counters start at zero every call
     if (cudaMemsetAsync(counters, 0, 256 + arrivals_bytes, stream) != cudaSuccess) return KV_ERR_CUDA;
 
@@ -125,6 +135,8 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     if (plan.max_parts > 1) {
         const size_t n = static_cast<size_t>(batch) * d.num_heads * group * plan.max_parts;
         a.arrivals = reinterpret_cast<unsigned*>(ws + 256);
+        a.grp_arrivals = reinterpret_cast<unsigned*>(ws + 256 + align256(static_cast<size_t>(batch) * d.num_heads * 4));
+        a.n_grp = merge_groups(plan.max_parts);
         a.part_ml = reinterpret_cast<float*>(ws + 256 + arrivals_bytes);
         a.part_o = reinterpret_cast<float*>(ws + 256 + arrivals_bytes + align256(n * 2 * sizeof(float)));
     }

@@ -38,6 +38,11 @@ size_t swap_bytes(const kv_pool* pool, int num_blocks, int layer_begin, int laye
 int launch_swap(const kv_pool* pool, bool out, const int32_t* blocks, int num_blocks, int layer_begin,
                 int layer_end, void* host, cudaStream_t stream);
 
+// Split-context partials merge in one step up to this many partitions per (sequence,
+// head); longer splits merge in two levels (groups of kMergeFan, then the groups).
+constexpr int kMergeFan = 16;
+inline int merge_groups(int max_parts) { return max_parts > kMergeFan ? (max_parts + kMergeFan - 1) / kMergeFan : 0; }
+
 struct AttnPlan {
     int partition;       // tokens per split-context partition
     int max_parts;       // ceil(max_context / partition)
@@ -45,6 +50,13 @@ struct AttnPlan {
     int group;           // query heads per KV head
     int window;          // > 0: sliding window of the last `window` tokens
     size_t ws_bytes;     // workspace bytes
+    // zero-initialised counters after the 256 work-counter bytes: the per-(sequence, head)
+    // arrivals, then the per-partition-group arrivals
+    size_t arrivals_bytes(int batch, int heads) const {
+        if (max_parts <= 1) return 0;
+        const size_t units = static_cast<size_t>(batch) * heads;
+        return ((units * 4 + 255) & ~size_t(255)) + ((units * merge_groups(max_parts) * 4 + 255) & ~size_t(255));
+    }
 };
 // group: query heads per KV head (1, or 2/4/8 for fp16 and FP8 pools)
 bool valid_group(const kv_pool_desc& d, int group);

@@ -287,3 +287,37 @@ def test_other_head_dims_and_dtypes(dtype, d):
         vs = [OF.decode(OF.quantize(v, np.float32(0.01))) * float(np.float32(0.01)) for v in vs]
     assert max_abs(out, OA.decode_attention(q, ks, vs, w.scale)) <= tol_for(w.dtype)
     assert cache.device_error() == 0
+
+
+# ------------------------------------------------------------------ long splits
+
+@pytest.mark.parametrize("G", [1, 8])
+def test_two_level_merge_of_long_splits(G):
+    """With 32-token partitions these contexts split into 15, 16, 17, 32, 33, 257 and 282
+    partitions: one-step merges up to 16, two-level merges beyond (groups of 16, the
+    last group ragged, and more than 16 groups at the top)."""
+    B, Hkv, d = 16, 2, 128
+    lens = [15 * 32, 16 * 32, 16 * 32 + 1, 32 * 32, 33 * 32 - 5, 257 * 32, 9000]
+    nb = sum(-(-n // B) for n in lens) + 4
+    w = W.Workload("long_splits", 160 + G, 1, Hkv, d, B, "f16", len(lens), lens, nb, 1 / math.sqrt(d),
+                   num_q_heads=G * Hkv)
+    cache = PagedKVCache(1, nb, B, Hkv, d, "f16")
+    poison(cache)
+    alloc = BlockAllocator(nb, B, W.free_order(w))
+    seqs = [alloc.new_seq() for _ in lens]
+    ks = [W.host_tokens(w, s, n, "k") for s, n in enumerate(lens)]
+    vs = [W.host_tokens(w, s, n, "v") for s, n in enumerate(lens)]
+    prefill(cache, alloc, seqs, ks, vs)
+    bt, cl, _ = tables_for(alloc, seqs, max(-(-n // B) for n in lens))
+    q = W.host_queries(w)
+    want = OA.decode_attention_gqa(q, ks, vs, w.scale) if G > 1 else OA.decode_attention(q, ks, vs, w.scale)
+    qt = torch.from_numpy(q).cuda()
+    for P in (32, 64, 0):
+        if G > 1:
+            out = cache.attention_gqa(0, qt, bt, cl, max(lens), w.scale, partition_tokens=P)
+        else:
+            out = cache.attention(0, qt, bt, cl, max(lens), w.scale, partition_tokens=P)
+        out = out.cpu().numpy()
+        assert np.all(np.isfinite(out))
+        assert max_abs(out, want) <= tol_for("f16"), (P, max_abs(out, want))
+    assert cache.device_error() == 0

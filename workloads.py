@@ -24,6 +24,9 @@ pages "KV缓存机制解析" §3.1 and "KV Cache与PagedAttention" §1.1):
             d 128, fp16 (and an FP8-E4M3 pool variant), B in {8, 16, 32}.
   gqa70b    80 layers, 64 query heads over 8 K/V heads (LLaMA-2-70B shape), d 128, fp16,
             B 16, batch 32, every length 4096.
+  longctx13b  8 layers of the LLaMA-13B shape (40 heads, d 128, fp16, B 16) with only 2
+            sequences of 32768 tokens: few (sequence, head) units, so one sequence's
+            context is split into many partitions.
 """
 
 from __future__ import annotations
@@ -110,6 +113,11 @@ def gqa70b(num_layers: int = 80) -> Workload:
     return Workload("gqa70b", seed=6, num_layers=num_layers, num_heads=8, head_dim=128, block_size=16,
                     dtype="f16", batch=32, lens=[4096] * 32, num_blocks=32 * 256,
                     scale=1.0 / math.sqrt(128), num_q_heads=64)
+
+
+def longctx13b(num_layers: int = 8) -> Workload:
+    return Workload("longctx13b", seed=7, num_layers=num_layers, num_heads=40, head_dim=128, block_size=16,
+                    dtype="f16", batch=2, lens=[32768] * 2, num_blocks=2 * 2048, scale=1.0 / math.sqrt(128))
 
 
 PROMPT_LEN_PARALLEL = 1030
