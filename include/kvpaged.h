@@ -113,6 +113,15 @@ KV_API int kv_pool_destroy(kv_pool* pool);
 /* Copy of the descriptor the pool was created with. */
 KV_API int kv_pool_get_desc(const kv_pool* pool, kv_pool_desc* desc);
 
+/* Fast paths the pool was set up with, as bit flags in *flags.
+ *   KV_FEATURE_TENSOR_MAPS  fp16 pool with head_dim 128: every layer has 128-byte-swizzled
+ *                           tensor maps of its K and V pools, and grouped-query decode
+ *                           (2, 4 or 8 query heads per KV head) runs its scores and P V on
+ *                           the tensor cores.  Without it the same calls run on the CUDA
+ *                           cores with identical semantics. */
+#define KV_FEATURE_TENSOR_MAPS 1u
+KV_API int kv_pool_features(const kv_pool* pool, unsigned* flags);
+
 /* Read (and if clear != 0, reset) the pool's device error bits.  Enqueues a copy on
  * `stream` and synchronises that stream.  Returns KV_ERR_DEVICE if any bit is set
  * (bits in *code), else KV_OK with *code = 0. */

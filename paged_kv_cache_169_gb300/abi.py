@@ -16,6 +16,7 @@ KV_OK, KV_ERR_INVALID_ARG, KV_ERR_NO_BLOCKS, KV_ERR_STATE = 0, -1, -2, -3
 KV_ERR_CUDA, KV_ERR_DEVICE, KV_ERR_UNSUPPORTED = -4, -5, -6
 KV_F32, KV_F16, KV_FP8_E4M3 = 0, 1, 2
 KV_DEVERR_SLOT, KV_DEVERR_BLOCK_ID, KV_DEVERR_CONTEXT, KV_DEVERR_TIMEOUT = 1, 2, 4, 8
+KV_FEATURE_TENSOR_MAPS = 1
 
 
 class KvError(RuntimeError):
@@ -51,6 +52,7 @@ _SIGS = {
                                  C.POINTER(_VP), C.POINTER(_VP), C.POINTER(_VP)]),
     "kv_pool_destroy": (C.c_int, [_VP]),
     "kv_pool_get_desc": (C.c_int, [_VP, C.POINTER(kv_pool_desc)]),
+    "kv_pool_features": (C.c_int, [_VP, C.POINTER(C.c_uint)]),
     "kv_get_device_error": (C.c_int, [_VP, _VP, C.c_int, C.POINTER(C.c_int)]),
     "kv_append": (C.c_int, [_VP, C.c_int, _VP, _VP, C.c_int, _VP, C.c_int, _VP]),
     "kv_copy_blocks": (C.c_int, [_VP, _VP, C.c_int, C.c_int, C.c_int, _VP]),
@@ -156,6 +158,13 @@ def kv_pool_get_desc(pool: int) -> kv_pool_desc:
     d = kv_pool_desc()
     _check("kv_pool_get_desc", load().kv_pool_get_desc(pool, C.byref(d)))
     return d
+
+
+def kv_pool_features(pool: int) -> int:
+    """Bit flags of the pool's fast paths (KV_FEATURE_*)."""
+    f = C.c_uint(0)
+    _check("kv_pool_features", load().kv_pool_features(pool, C.byref(f)))
+    return f.value
 
 
 def kv_get_device_error(pool: int, stream: int = 0, clear: bool = True) -> int:

@@ -54,9 +54,12 @@ void make_tensor_maps(kv_pool* p) {
     void* raw = std::malloc(2 * L * sizeof(CUtensorMap) + 64);
     if (!raw) return;
     CUtensorMap* maps = reinterpret_cast<CUtensorMap*>((reinterpret_cast<uintptr_t>(raw) + 63) & ~uintptr_t(63));
-    const cuuint64_t dims[3] = {64, 2, static_cast<cuuint64_t>(d.num_blocks) * d.num_heads * d.block_size};
-    const cuuint64_t strides[2] = {128, 256};
-    const cuuint32_t box[3] = {64, 2, static_cast<cuuint32_t>(d.block_size < 16 ? d.block_size : 16)};
+    // a token row of one head (128 halves) seen as two 64-half halves: the copied tile of
+    // up to 16 rows lands half-major ([2][rows][64]), so 8 consecutive tokens of one half
+    // are 8 consecutive 128-byte lines and their swizzled 16-byte pieces hit distinct banks
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(d.num_blocks) * d.num_heads * d.block_size, 2};
+    const cuuint64_t strides[2] = {256, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(d.block_size < 16 ? d.block_size : 16), 2};
     const cuuint32_t estr[3] = {1, 1, 1};
     for (int l = 0; l < L; ++l) {
         for (int kv = 0; kv < 2; ++kv) {
@@ -152,6 +155,12 @@ int kv_pool_destroy(kv_pool* pool) {
 int kv_pool_get_desc(const kv_pool* pool, kv_pool_desc* desc) {
     if (!pool || !desc) return KV_ERR_INVALID_ARG;
     *desc = pool->desc;
+    return KV_OK;
+}
+
+int kv_pool_features(const kv_pool* pool, unsigned* flags) {
+    if (!pool || !flags) return KV_ERR_INVALID_ARG;
+    *flags = pool->tmaps ? KV_FEATURE_TENSOR_MAPS : 0u;
     return KV_OK;
 }
 

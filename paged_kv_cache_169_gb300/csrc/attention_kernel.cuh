@@ -465,6 +465,14 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     static_assert(CT == 16 && D == 128, "tensor-core consumer shape");
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     const int g = lane >> 2, t = lane & 3;          // accumulator row (query) / column pair
+    // byte x (0..255) of token row tok in a chunk: copies of rpc rows (8 or 16), each laid
+    // out half-major [2][rpc][64 halves], 128-byte swizzled
+    const int rs = (a.B < CT ? a.B : CT) == 8 ? 3 : 4;
+    auto tile_off = [rs](int tok, int x) -> uint32_t {
+        const int rpc = 1 << rs;
+        return swz128(static_cast<uint32_t>(((tok >> rs) << (rs + 8)) + ((((x >> 7) << rs) + (tok & (rpc - 1))) << 7) +
+                                            (x & 127)));
+    };
     uint32_t qa[8][2];
     float o[16][4];
     float m = -CUDART_INF_F, l = 0.f;
@@ -510,7 +518,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             const int e0 = lane * 4;
             const uint2 kv = *reinterpret_cast<const uint2*>(a.k_new + (sh * D + e0) * 2);
             const uint2 vv = *reinterpret_cast<const uint2*>(a.v_new + (sh * D + e0) * 2);
-            const uint32_t so = swz128(static_cast<uint32_t>(r * 256 + e0 * 2));
+            const uint32_t so = tile_off(r, e0 * 2);
             *reinterpret_cast<uint2*>(stg + C::K_OFF + so) = kv;
             *reinterpret_cast<uint2*>(stg + C::V_OFF + so) = vv;
             *reinterpret_cast<uint2*>(a.kpool + grow * C::ROW + e0 * 2) = kv;
@@ -525,7 +533,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 #pragma unroll 1
                 for (int r = 0; r < CT; ++r)
                     if ((r < lo || r >= nt) && lane < 16)
-                        *reinterpret_cast<uint4*>(stg + C::V_OFF + r * 256 + lane * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(stg + C::V_OFF + tile_off(r, lane * 16)) = make_uint4(0, 0, 0, 0);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
             }
@@ -539,7 +547,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 // matrices: (tok 0-7, dims 16k..+7) (tok 0-7, +8..) (tok 8-15, 16k..) (tok 8-15, +8..)
                 const int tok = (mi >> 1) * 8 + mr, cp = 2 * k + (mi & 1);
                 uint32_t kb[4];
-                ldsm_x4(kbase + swz128(static_cast<uint32_t>(tok * 256 + (cp >> 3) * 128 + (cp & 7) * 16)), kb);
+                ldsm_x4(kbase + tile_off(tok, cp * 16), kb);
                 mma_16816(sacc[0], qa[k][0], 0u, qa[k][1], 0u, kb[0], kb[1]);
                 mma_16816(sacc[1], qa[k][0], 0u, qa[k][1], 0u, kb[2], kb[3]);
             }
@@ -571,7 +579,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 // matrices: (tok 0-7, dims 16jj..) (tok 8-15, 16jj..) (tok 0-7, +8..) (tok 8-15, +8..)
                 const int tok = (mi & 1) * 8 + mr, cp = 2 * jj + (mi >> 1);
                 uint32_t vb[4];
-                ldsm_x4_t(vbase + swz128(static_cast<uint32_t>(tok * 256 + (cp >> 3) * 128 + (cp & 7) * 16)), vb);
+                ldsm_x4_t(vbase + tile_off(tok, cp * 16), vb);
                 mma_16816(o[2 * jj], pa0, 0u, pa2, 0u, vb[0], vb[1]);
                 mma_16816(o[2 * jj + 1], pa0, 0u, pa2, 0u, vb[2], vb[3]);
             }
@@ -749,10 +757,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                             const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h) * a.B +
                                                   row0) * C::ROW;
                             if constexpr (C::MMA) {
-                                // rpc token rows of one head as [rows][2][64], 128-byte swizzled
+                                // rpc token rows of one head as [2][rows][64], 128-byte swizzled
                                 const int row = static_cast<int>(toff / C::ROW);
-                                tma_load_3d(dst + C::K_OFF + j * tile, &a.kmap, 0, 0, row, fb);
-                                tma_load_3d(dst + C::V_OFF + j * tile, &a.vmap, 0, 0, row, fb);
+                                tma_load_3d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, 0, fb);
+                                tma_load_3d(dst + C::V_OFF + j * tile, &a.vmap, 0, row, 0, fb);
                             } else {
                                 bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
                                 bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
