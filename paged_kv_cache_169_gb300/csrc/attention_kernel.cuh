@@ -365,29 +365,47 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
 // Longer splits merge in two levels, which shortens the merge that ends the split: the
 // last finisher of each group of kMergeFan partitions folds the group into the group's
 // first slot, and the last group to fold merges the ceil(np / kMergeFan) groups.
+// The ticket's atomic is issued at the end of the item and read one chunk later
+// (ticket_resolve), so its round trip overlaps the next chunk instead of stalling the warp.
+struct Ticket {
+    unsigned prev;          // lane 0: the atomic's result (in flight until read)
+    int64_t shk;
+    int p, np;
+    bool pending;
+};
+
+__device__ __forceinline__ void ticket_issue(const AttnArgs& a, Ticket& tk, int64_t shk, int p, int np, int lane) {
+    __syncwarp();                                      // every lane's partial is written
+    unsigned* ctr = np > kMergeFan ? a.grp_arrivals + shk * a.n_grp + p / kMergeFan : a.arrivals + shk;
+    if (lane == 0) tk.prev = atom_add_acq_rel_gpu(ctr, 1u);
+    tk.shk = shk;
+    tk.p = p;
+    tk.np = np;
+    tk.pending = true;
+}
+
 template <int D, int G>
-__device__ __forceinline__ void finish_partition(const AttnArgs& a, int64_t shk, int p, int np, int lane) {
-    __syncwarp();
-    int count = np, stride = 1;
-    if (np > kMergeFan) {
-        const int grp = p / kMergeFan;
-        const int gsz = min(kMergeFan, np - grp * kMergeFan);
-        unsigned prev = 0;
-        if (lane == 0) prev = atom_add_acq_rel_gpu(a.grp_arrivals + shk * a.n_grp + grp, 1u);
-        prev = __shfl_sync(FULL, prev, 0);
+__device__ __forceinline__ void ticket_resolve(const AttnArgs& a, Ticket& tk, int lane) {
+    if (!tk.pending) return;
+    tk.pending = false;
+    unsigned prev = __shfl_sync(FULL, tk.prev, 0);
+    int count = tk.np, stride = 1;
+    if (tk.np > kMergeFan) {
+        const int grp = tk.p / kMergeFan;
+        const int gsz = min(kMergeFan, tk.np - grp * kMergeFan);
         if (prev != static_cast<unsigned>(gsz - 1)) return;
         __syncwarp();
-        merge_partials<D, G, false>(a, shk * G, grp * kMergeFan, gsz, 1, lane);
+        merge_partials<D, G, false>(a, tk.shk * G, grp * kMergeFan, gsz, 1, lane);
         __syncwarp();
-        count = (np + kMergeFan - 1) / kMergeFan;
+        count = (tk.np + kMergeFan - 1) / kMergeFan;
         stride = kMergeFan;
+        unsigned p2 = 0;
+        if (lane == 0) p2 = atom_add_acq_rel_gpu(a.arrivals + tk.shk, 1u);
+        prev = __shfl_sync(FULL, p2, 0);
     }
-    unsigned prev = 0;
-    if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + shk, 1u);
-    prev = __shfl_sync(FULL, prev, 0);
     if (prev != static_cast<unsigned>(count - 1)) return;
     __syncwarp();
-    merge_partials<D, G, true>(a, shk * G, 0, count, stride, lane);
+    merge_partials<D, G, true>(a, tk.shk * G, 0, count, stride, lane);
 }
 
 // Fused append: lane's D/32 elements of one new-token row (src, in_bytes per element)
@@ -480,6 +498,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     for (int i = 0; i < 8; ++i) { qa[i][0] = 0u; qa[i][1] = 0u; }
     #pragma unroll
     for (int j = 0; j < 16; ++j) { o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f; }
+    Ticket tk{};
 
     for (int j = 0;; ++j) {
         const int st = j % NSW;
@@ -586,6 +605,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars[C::NC * NSW + w * NSW + st]));
+        ticket_resolve<D, G>(a, tk, lane);            // the previous item's ticket
         if (flags & F_LAST) {
             float lr = l + __shfl_xor_sync(FULL, l, 1);
             lr += __shfl_xor_sync(FULL, lr, 2);
@@ -613,10 +633,11 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 }
                 const int ctx_s = s_ctx[ms];
                 const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
-                finish_partition<D, G>(a, shk, mpart, np, lane);
+                ticket_issue(a, tk, shk, mpart, np, lane);
             }
         }
     }
+    ticket_resolve<D, G>(a, tk, lane);
 }
 
 template <typename C>
@@ -832,6 +853,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         #pragma unroll
         for (int i = 0; i < DPL / 2; ++i) { q2[g][i] = make_float2(0.f, 0.f); acc[g][i] = make_float2(0.f, 0.f); }
     }
+    Ticket tk{};
 
     for (int j = 0;; ++j) {
         const int st = j % NSW;
@@ -956,6 +978,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(w, st));
+        ticket_resolve<D, G>(a, tk, lane);            // the previous item's ticket
         if (meta.flags & F_LAST) {
             const int64_t shk = static_cast<int64_t>(meta.s) * a.H + meta.h;   // (sequence, KV head)
             #pragma unroll
@@ -993,10 +1016,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 // publish the partials, then take a ticket; the last partition merges
                 const int ctx_s = s_ctx[meta.s];
                 const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
-                finish_partition<D, G>(a, shk, meta.p, np, lane);
+                ticket_issue(a, tk, shk, meta.p, np, lane);
             }
         }
     }
+    ticket_resolve<D, G>(a, tk, lane);
 }
 
 template <typename C>
