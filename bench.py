@@ -540,7 +540,8 @@ def main():
     ap.add_argument("--workload", default="llama13b")
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library choice)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a smaller case)")
-    ap.add_argument("--cpu-units", type=int, default=38400, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--cpu-units", type=int, default=153600,
+                    help="oracle sample size for cpu_baseline ((sequence, head) units; ~4 s on 16 cores)")
     ap.add_argument("--ref-units", type=int, default=768, help="oracle units per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="time kv_append + paged_decode_attention as two calls")
