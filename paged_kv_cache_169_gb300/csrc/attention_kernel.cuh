@@ -78,6 +78,11 @@ namespace {
 constexpr int kMaxBatch = 1024;    // sequences per launch (prefix table in shared memory)
 constexpr int kMaxSub = 64;        // launches per call -> batch <= 65536
 constexpr int kPartAlign = 32;     // partition sizes are multiples of this
+#if defined(KVP_CLAIM_LEAD)
+constexpr int kClaimLead = KVP_CLAIM_LEAD;   // tuning sweeps only
+#else
+constexpr int kClaimLead = 6;      // claim the next item this many fills before it is needed
+#endif
 constexpr unsigned FULL = 0xffffffffu;
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_TERM = 4, F_SINGLE = 8, F_PATCH = 16 };
@@ -718,7 +723,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         bool alive = mine;
         if (mine) {
             cur = decode(atomicAdd(a.counter, 1u));
-            if (cur.valid && cur.nchunks == 1) claim();
+            if (cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
             load_ids(cur, 0);
         }
         bool failed = false;
@@ -796,13 +801,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                         bulk_g2s(qdst, qsrc, C::Q_BYTES, fb);
                     }
                     const int rem = cur.nchunks - 1 - c;      // chunks of cur still to fill
-                    if (rem == 1 && !claimed) claim();
+                    if (rem <= kClaimLead && !claimed) claim();
                     if (rem == 0) {
                         if (!claimed) claim();
                         cur = decode(pending);
                         claimed = false;
                         c = 0;
-                        if (cur.valid && cur.nchunks == 1) claim();
+                        if (cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
                     } else {
                         ++c;
                     }
