@@ -204,7 +204,7 @@ KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int ma
  *   max_context   host upper bound of context_lens (sizes the split-context workspace).
  *   scale         score multiplier, usually 1/sqrt(head_dim); finite and > 0.
  *   partition_tokens  0 = library choice (about 8 work items per consumer warp, one
- *                 round for grouped-query launches, at most 1024 tokens); else tokens
+ *                 round for grouped-query launches, 256 to 1024 tokens); else tokens
  *                 per split-context partition, a multiple of 32.  Sequences longer
  *                 than one partition are split, attended per partition and merged
  *                 exactly (log-sum-exp) in the same launch by the warp that finishes

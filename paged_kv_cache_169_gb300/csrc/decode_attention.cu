@@ -53,7 +53,8 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     const int span = (window > 0 && window + 32 < max_context) ? window + 32 : max_context;
     if (!valid_group(d, group)) return KV_ERR_INVALID_ARG;
     const int cap = 1 << 24;                       // block ids are fetched per chunk: no per-item cap
-    constexpr int kAutoPartMax = 1024;             // library choice: at most 1024 tokens per item
+    constexpr int kAutoPartMax = 1024;             // library choice: 256 .. 1024 tokens per item
+    constexpr int kAutoPartMin = 256;
     const int nc = consumers_for(pool, group);
     int P;
     if (partition_tokens > 0) {
@@ -75,7 +76,9 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
         if (parts < 1) parts = 1;
         int64_t p = (span + parts - 1) / parts;
         p = (p + kPartAlign - 1) / kPartAlign * kPartAlign;
-        if (p < kPartAlign) p = kPartAlign;
+        // every item also pays a claim, a query copy, a partial and its share of a merge:
+        // below 256 tokens that costs more than the finer balance gains
+        if (p < kAutoPartMin) p = kAutoPartMin;
         // the longest item bounds the tail when contexts are ragged (the host sees only
         // the longest context)
         if (p > kAutoPartMax) p = kAutoPartMax;
