@@ -127,6 +127,14 @@ KV_API int kv_pool_features(const kv_pool* pool, unsigned* flags);
  * (bits in *code), else KV_OK with *code = 0. */
 KV_API int kv_get_device_error(kv_pool* pool, kv_stream_t stream, int clear, int* code);
 
+/* Self-test of the kernels' bounded waits (no counterpart on the pages).  Launches one warp
+ * on `stream` that waits on a shared-memory mbarrier nothing arrives at, through the same
+ * bounded wait every kernel wait uses, with a limit of limit_ns nanoseconds instead of the
+ * kernels' one second.  The wait gives up, sets KV_DEVERR_TIMEOUT in the pool's error word
+ * and the kernel returns normally: the context stays usable.  limit_ns in [1, 1e9], else
+ * KV_ERR_INVALID_ARG.  Asynchronous; read the bit with kv_get_device_error. */
+KV_API int kv_selftest_wait_timeout(kv_pool* pool, uint64_t limit_ns, kv_stream_t stream);
+
 /* ---------------------------------------------------------------- append */
 
 /* Write num_tokens new tokens' K and V into their slots for one layer.

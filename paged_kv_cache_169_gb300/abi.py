@@ -54,6 +54,7 @@ _SIGS = {
     "kv_pool_get_desc": (C.c_int, [_VP, C.POINTER(kv_pool_desc)]),
     "kv_pool_features": (C.c_int, [_VP, C.POINTER(C.c_uint)]),
     "kv_get_device_error": (C.c_int, [_VP, _VP, C.c_int, C.POINTER(C.c_int)]),
+    "kv_selftest_wait_timeout": (C.c_int, [_VP, C.c_uint64, _VP]),
     "kv_append": (C.c_int, [_VP, C.c_int, _VP, _VP, C.c_int, _VP, C.c_int, _VP]),
     "kv_copy_blocks": (C.c_int, [_VP, _VP, C.c_int, C.c_int, C.c_int, _VP]),
     "kv_swap_bytes": (C.c_size_t, [_VP, C.c_int, C.c_int, C.c_int]),
@@ -165,6 +166,11 @@ def kv_pool_features(pool: int) -> int:
     f = C.c_uint(0)
     _check("kv_pool_features", load().kv_pool_features(pool, C.byref(f)))
     return f.value
+
+
+def kv_selftest_wait_timeout(pool: int, limit_ns: int, stream: int = 0) -> None:
+    """Launch the bounded-wait self-test (a wait that must time out after limit_ns)."""
+    _check("kv_selftest_wait_timeout", load().kv_selftest_wait_timeout(pool, limit_ns, stream))
 
 
 def kv_get_device_error(pool: int, stream: int = 0, clear: bool = True) -> int:

@@ -164,6 +164,11 @@ int kv_pool_features(const kv_pool* pool, unsigned* flags) {
     return KV_OK;
 }
 
+int kv_selftest_wait_timeout(kv_pool* pool, uint64_t limit_ns, kv_stream_t stream) {
+    if (!pool || limit_ns < 1 || limit_ns > 1000000000ull) return KV_ERR_INVALID_ARG;
+    return kvp::launch_selftest_wait(pool, limit_ns, static_cast<cudaStream_t>(stream));
+}
+
 int kv_get_device_error(kv_pool* pool, kv_stream_t stream, int clear, int* code) {
     if (!pool || !code) return KV_ERR_INVALID_ARG;
     int h = 0;

@@ -234,4 +234,24 @@ int launch_swap(const kv_pool* pool, bool out, const int32_t* blocks, int num_bl
     return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
+namespace {
+// One warp waits on an mbarrier that nothing arrives at, through the same bounded wait the
+// attention kernel uses: the wait gives up after limit_ns, sets KV_DEVERR_TIMEOUT and the
+// kernel returns normally.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    mbar_wait_bounded(smem_u32(&bar), 0, err, limit_ns);
+}
+}  // namespace
+
+int launch_selftest_wait(const kv_pool* pool, uint64_t limit_ns, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns, pool->d_err);
+    return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 }  // namespace kvp

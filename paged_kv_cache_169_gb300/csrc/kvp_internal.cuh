@@ -117,7 +117,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for completion of the phase with the given parity, for at most ~1 s.
 // On time-out: set KV_DEVERR_TIMEOUT in *err and return false (no trap, no hang).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     #pragma unroll 1
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity)) return true;
@@ -125,12 +126,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     #pragma unroll 1
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(err, KV_DEVERR_TIMEOUT);
             return false;
         }
     }
 }
+
+int launch_selftest_wait(const kv_pool* pool, uint64_t limit_ns, cudaStream_t stream);
 
 // 1-D bulk copy global -> shared (the issuing CTA's own shared memory), completion
 // counted in bytes on the mbarrier.  dst, src 16-byte aligned, bytes a multiple of 16.

@@ -44,6 +44,15 @@ def test_status_strings(lib):
     assert abi.kv_version() >= 100
 
 
+def test_selftest_entry_validates_before_any_device_call(lib):
+    with pytest.raises(abi.KvError) as e:
+        abi.kv_selftest_wait_timeout(0, 1000)
+    assert e.value.status == abi.KV_ERR_INVALID_ARG
+    assert abi.KV_FEATURE_TENSOR_MAPS == 1
+    with pytest.raises(abi.KvError):
+        abi.kv_pool_features(0)
+
+
 def test_pool_create_rejects_bad_descriptors_without_a_gpu(lib):
     bad = [dict(head_dim=96), dict(block_size=12), dict(num_heads=0), dict(num_layers=0),
            dict(num_blocks=0), dict(dtype=7)]
