@@ -35,8 +35,10 @@ def make_workload(name: str):
     elif name == "llama7b":
         w = W.llama7b()
         w.lens = [n + w.steps for n in w.lens]       # context after the last of the 64 steps
-    elif name == "gqa70b":
+    elif name in ("gqa70b", "gqa70b_fp8"):
         w = W.gqa70b()
+        if name.endswith("fp8"):
+            w.kv = "fp8"
     elif name == "longctx13b":
         w = W.longctx13b()
     elif name.startswith("ragged"):

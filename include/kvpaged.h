@@ -118,7 +118,10 @@ KV_API int kv_pool_get_desc(const kv_pool* pool, kv_pool_desc* desc);
  *                           tensor maps of its K and V pools, and grouped-query decode
  *                           (2, 4 or 8 query heads per KV head) runs its scores and P V on
  *                           the tensor cores.  Without it the same calls run on the CUDA
- *                           cores with identical semantics. */
+ *                           cores with identical semantics.  (FP8 pools with head_dim 128
+ *                           need no tensor maps: their grouped-query decode dequantises
+ *                           each tile to fp16 in shared memory and runs on the tensor
+ *                           cores too.) */
 #define KV_FEATURE_TENSOR_MAPS 1u
 KV_API int kv_pool_features(const kv_pool* pool, unsigned* flags);
 

@@ -117,14 +117,15 @@ template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_
 #endif
 
 // G_: query heads per KV head (grouped-query attention; 1 = one query per KV head).
-// MMA_: grouped-query tensor-core consumer (fp16, head_dim 128, G >= 2) fed by swizzled
-// tensor-map copies.
+// MMA_: grouped-query tensor-core consumer (head_dim 128, G >= 2).  fp16 pools are fed by
+// swizzled tensor-map copies; FP8 pools by plain bulk copies, each tile dequantised to a
+// swizzled fp16 scratch in shared memory before the mma.
 template <int D_, typename KV_, typename QT_, int G_ = 1, bool MMA_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int G = G_;
     static constexpr bool MMA = MMA_;
-    static_assert(!MMA || (sizeof(KV_) == 2 && D_ == 128 && G_ >= 2), "tensor-core path: fp16, d 128, G >= 2");
+    static_assert(!MMA || (sizeof(KV_) <= 2 && D_ == 128 && G_ >= 2), "tensor-core path: fp16 or FP8, d 128, G >= 2");
     using KV = KV_;
     using QT = QT_;
     static constexpr int ESZ = sizeof(KV);
@@ -140,13 +141,16 @@ struct Cfg {
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = KV_BYTES;
     static constexpr int Q_OFF = 2 * KV_BYTES;
-    // the tensor-core path keeps its 1024-aligned stages to exactly K and V (8 KiB): its
-    // query rows go to a region of their own, one slot per stage
+    // the fp16 tensor-core path keeps its 1024-aligned stages to exactly K and V (8 KiB):
+    // its query rows go to a region of their own, one slot per stage.  The FP8 tensor-core
+    // path reads its query rows from global memory once per item and keeps a per-warp fp16
+    // scratch (K, then V, of one chunk) instead.
+    static constexpr bool SWZ_STAGE = MMA && !FP8;        // stages hold swizzled tensor-map tiles
     static constexpr int Q_STAGE = MMA ? 0 : Q_BYTES;
-    static constexpr int QR_BYTES = MMA ? Q_BYTES : 0;
+    static constexpr int QR_BYTES = SWZ_STAGE ? Q_BYTES : 0;
+    static constexpr int SCR_BYTES = (MMA && FP8) ? CT * D * 2 : 0;
     static constexpr int SC_OFF = Q_OFF + Q_STAGE;
-    // the tensor-core path's stages hold 128-byte-swizzled rows: 1024-byte aligned
-    static constexpr int STAGE = round_up(SC_OFF + SC_BYTES, MMA ? 1024 : 128);
+    static constexpr int STAGE = round_up(SC_OFF + SC_BYTES, SWZ_STAGE ? 1024 : 128);
     static constexpr int NC_AUTO = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
     // more query heads per warp need more registers: fewer consumer warps
 #if defined(KVP_MMA_NC)
@@ -159,13 +163,16 @@ struct Cfg {
                                            : (G == 2 ? 12 : (G == 4 ? 8 : 6));
     // stages that fit beside the prefix table and the barriers
     static constexpr int NSW_FIT =
-        (227 * 1024 - 2 * kMaxBatch * 4 - 1024 - (MMA ? 1024 : 0)) / (NC * (STAGE + (int)sizeof(Meta) + QR_BYTES));
-    static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > 4 ? 4 : NSW_FIT);
+        (227 * 1024 - 2 * kMaxBatch * 4 - 1024 - (MMA ? 2048 : 0) - NC * SCR_BYTES) /
+        (NC * (STAGE + (int)sizeof(Meta) + QR_BYTES));
+    static constexpr int NSW_CAP = (MMA && FP8) ? 6 : 4;   // FP8 stages are half as large
+    static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > NSW_CAP ? NSW_CAP : NSW_FIT);
     static_assert(NSW >= 2, "at least double buffering");
     static constexpr int THREADS = (NC + 1) * 32;
     static constexpr int META_R = NC * NSW * STAGE;                   // one Meta per stage
     static constexpr int QR_OFF = META_R + NC * NSW * (int)sizeof(Meta);   // MMA: one q slot per stage
-    static constexpr int BAR_OFF = QR_OFF + NC * NSW * QR_BYTES;
+    static constexpr int SCR_OFF = round_up(QR_OFF + NC * NSW * QR_BYTES, 1024);   // FP8 MMA scratch
+    static constexpr int BAR_OFF = SCR_OFF + NC * SCR_BYTES;
     static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
     static constexpr int ALIGN_SLACK = MMA ? 1024 : 0;           // to 1024-align the base
     static constexpr int SMEM = PREFIX_OFF + 2 * kMaxBatch * 4 + ALIGN_SLACK;
@@ -488,13 +495,35 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     static_assert(CT == 16 && D == 128, "tensor-core consumer shape");
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     const int g = lane >> 2, t = lane & 3;          // accumulator row (query) / column pair
-    // byte x (0..255) of token row tok in a chunk: copies of rpc rows (8 or 16), each laid
-    // out half-major [2][rpc][64 halves], 128-byte swizzled
-    const int rs = (a.B < CT ? a.B : CT) == 8 ? 3 : 4;
+    // byte x (0..255) of fp16 token row tok in a chunk: copies of rpc rows (8 or 16), each
+    // laid out half-major [2][rpc][64 halves], 128-byte swizzled.  fp16 stages are laid out
+    // by the tensor-map copies (rpc = min(B, 16)); the FP8 path's dequantised scratch is
+    // one 16-row copy.
+    const int rs = (C::FP8 || (a.B < CT ? a.B : CT) == 16) ? 4 : 3;
     auto tile_off = [rs](int tok, int x) -> uint32_t {
         const int rpc = 1 << rs;
         return swz128(static_cast<uint32_t>(((tok >> rs) << (rs + 8)) + ((((x >> 7) << rs) + (tok & (rpc - 1))) << 7) +
                                             (x & 127)));
+    };
+    char* scr = smem + C::SCR_OFF + w * C::SCR_BYTES;      // FP8 only: fp16 K, then V, of a chunk
+    // FP8: the 16 rows x 128 codes at src become fp16 rows of the scratch (exact: every
+    // E4M3 value is an fp16 value); the block scales are applied to S and P instead
+    auto dequant = [&](const char* src) {
+        #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int task = lane + 32 * i;                 // 16 rows x 8 pieces of 16 codes
+            const int r = task >> 3, c = (task & 7) * 16;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + c);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h[8];
+            #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                h[2 * k] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w4[k] & 0xffffu));
+                h[2 * k + 1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w4[k] >> 16));
+            }
+            *reinterpret_cast<uint4*>(scr + tile_off(r, 2 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(scr + tile_off(r, 2 * c + 16)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
     };
     uint32_t qa[8][2];
     float o[16][4];
@@ -518,23 +547,38 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
         const int flags = mp->flags;
         if (flags & F_TERM) break;
         const int nt = mp->ntok, lo = mp->lo, ms = mp->s, mh = mp->h, mpart = mp->p;
-        const uint32_t kbase = smem_u32(stg + C::K_OFF), vbase = smem_u32(stg + C::V_OFF);
+        uint32_t kbase = smem_u32(stg + C::K_OFF), vbase = smem_u32(stg + C::V_OFF);
         if (flags & F_FIRST) {
             m = -CUDART_INF_F;
             l = 0.f;
             #pragma unroll
             for (int jj = 0; jj < 16; ++jj) { o[jj][0] = o[jj][1] = o[jj][2] = o[jj][3] = 0.f; }
-            // A fragments of the G query rows (staged with the item's first chunk)
+            // A fragments of the G query rows (fp16: staged with the item's first chunk;
+            // FP8: read from global memory once per item)
             const bool real = g < G && nt > 0;
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES + (real ? g : 0) * D * 2);
+            const uint32_t* qrow = C::FP8
+                ? reinterpret_cast<const uint32_t*>(static_cast<const char*>(a.q) +
+                                                    ((static_cast<int64_t>(ms) * a.H + mh) * G + (real ? g : 0)) * D * 2)
+                : reinterpret_cast<const uint32_t*>(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES +
+                                                    (real ? g : 0) * D * 2);
             #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 qa[k][0] = real ? qrow[8 * k + t] : 0u;
                 qa[k][1] = real ? qrow[8 * k + 4 + t] : 0u;
             }
         }
-        if (flags & F_PATCH) {
+        if (C::FP8 && (flags & F_PATCH)) {
+            // the new token, quantised with its block's scale, into the stage row and the slot
+            const int r = mp->patch_row;
+            const int64_t sh = static_cast<int64_t>(ms) * a.H + mh;
+            const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + mh) * a.B + mp->patch_off;
+            patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, stg + C::K_OFF + r * C::ROW,
+                         a.kpool + grow * C::ROW, __ldg(a.kscale + mp->patch_id), lane);
+            patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, stg + C::V_OFF + r * C::ROW,
+                         a.vpool + grow * C::ROW, __ldg(a.vscale + mp->patch_id), lane);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+        } else if (flags & F_PATCH) {
             // the new token's row, into the swizzled stage and into the pool slot
             const int r = mp->patch_row;
             const int64_t sh = static_cast<int64_t>(ms) * a.H + mh;
@@ -551,7 +595,20 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             __syncwarp();
         }
         if (nt > 0) {
-            if (nt < CT || lo > 0) {
+            // FP8: per-block scales of this thread's score columns (tokens 2t, 2t+1 and
+            // 8+2t, 9+2t) and the K tile dequantised into the scratch
+            float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
+            if constexpr (C::FP8) {
+                const int id0 = mp->ids[0], id1 = mp->ids[(a.B < CT ? a.B : CT) == 8 ? 1 : 0];
+                ks0 = __ldg(a.kscale + id0);
+                ks1 = __ldg(a.kscale + id1);
+                vs0 = __ldg(a.vscale + id0);
+                vs1 = __ldg(a.vscale + id1);
+                dequant(stg + C::K_OFF);
+                __syncwarp();
+                kbase = smem_u32(scr);
+            }
+            if (!C::FP8 && (nt < CT || lo > 0)) {
                 // rows outside [lo, nt) may hold anything (unused slots): zero their V so
                 // that p = 0 rows contribute exactly nothing to P V
                 #pragma unroll 1
@@ -576,8 +633,8 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 mma_16816(sacc[1], qa[k][0], 0u, qa[k][1], 0u, kb[2], kb[3]);
             }
             // row g: tokens 2t, 2t+1 (tile 0) and 8+2t, 9+2t (tile 1); log2-domain scores
-            float x[4] = {sacc[0][0] * a.qscale, sacc[0][1] * a.qscale, sacc[1][0] * a.qscale,
-                          sacc[1][1] * a.qscale};
+            const float qk0 = a.qscale * ks0, qk1 = a.qscale * ks1;   // ks = 1 for fp16 pools
+            float x[4] = {sacc[0][0] * qk0, sacc[0][1] * qk0, sacc[1][0] * qk1, sacc[1][1] * qk1};
             const int tk[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
             float mx = -CUDART_INF_F;
             #pragma unroll
@@ -596,7 +653,21 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             #pragma unroll
             for (int jj = 0; jj < 16; ++jj) { o[jj][0] *= corr; o[jj][1] *= corr; }
             m = m_new;
-            const uint32_t pa0 = pack_half2(pr[0], pr[1]), pa2 = pack_half2(pr[2], pr[3]);
+            const uint32_t pa0 = pack_half2(pr[0] * vs0, pr[1] * vs0), pa2 = pack_half2(pr[2] * vs1, pr[3] * vs1);
+            if constexpr (C::FP8) {
+                // V into the scratch once every lane is done reading K from it; rows outside
+                // [lo, nt) are zeroed so that their p = 0 contributes exactly nothing
+                __syncwarp();
+                dequant(stg + C::V_OFF);
+                if (nt < CT || lo > 0) {
+                    #pragma unroll 1
+                    for (int r = 0; r < CT; ++r)
+                        if ((r < lo || r >= nt) && lane < 16)
+                            *reinterpret_cast<uint4*>(scr + tile_off(r, lane * 16)) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+                vbase = smem_u32(scr);
+            }
             // O += P V
             #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
@@ -652,6 +723,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
     extern __shared__ __align__(128) char smem_raw[];
     // swizzled stages need a 1024-byte aligned base (the slack is part of C::SMEM)
     char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) * (C::MMA ? 1 : 0);
+    static_assert(!C::MMA || (C::STAGE % 1024 == 0 || !C::SWZ_STAGE), "swizzled stages 1024-aligned");
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);   // full[NC*NSW], empty[NC*NSW]
     int* s_ctx = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
     int* s_end = s_ctx + kMaxBatch;
@@ -751,7 +823,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                             ids[j] = 0;
                         }
                     }
-                    const bool with_q = (c == 0) && nt > 0;
+                    const bool with_q = (c == 0) && nt > 0 && (C::Q_STAGE > 0 || C::QR_BYTES > 0);
                     const uint32_t bytes = nblk * 2 * tile + (with_q ? C::Q_BYTES : 0);
                     meta->s = cur.s;
                     meta->h = cur.h;
@@ -782,7 +854,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                         if (j < nblk) {
                             const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h) * a.B +
                                                   row0) * C::ROW;
-                            if constexpr (C::MMA) {
+                            if constexpr (C::SWZ_STAGE) {
                                 // rpc token rows of one head as [2][rows][64], 128-byte swizzled
                                 const int row = static_cast<int>(toff / C::ROW);
                                 tma_load_3d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, 0, fb);
@@ -796,8 +868,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                     if (with_q) {
                         const char* qsrc = static_cast<const char*>(a.q) +
                                            (static_cast<int64_t>(cur.s) * a.H + cur.h) * C::Q_BYTES;
-                        const uint32_t qdst = C::MMA ? smem_u32(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES)
-                                                     : dst + C::Q_OFF;
+                        const uint32_t qdst = C::QR_BYTES ? smem_u32(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES)
+                                                          : dst + C::Q_OFF;
                         bulk_g2s(qdst, qsrc, C::Q_BYTES, fb);
                     }
                     const int rem = cur.nchunks - 1 - c;      // chunks of cur still to fill

@@ -190,6 +190,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Two E4M3 bytes (low byte = first element) -> two floats, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2_bits(uint16_t v) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    return h2;
+}
+
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));

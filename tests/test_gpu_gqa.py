@@ -45,7 +45,7 @@ def _oracle_values(dtype, ks, vs):
 
 @pytest.mark.parametrize("G", [2, 4, 8])
 @pytest.mark.parametrize("dtype,d,B", [("f16", 128, 16), ("f16", 128, 8), ("f16", 128, 32), ("f16", 64, 8),
-                                       ("fp8", 128, 16), ("fp8", 64, 32)])
+                                       ("fp8", 128, 16), ("fp8", 128, 8), ("fp8", 128, 32), ("fp8", 64, 32)])
 def test_gqa_against_oracle(G, dtype, d, B):
     lens = [0, 1, 15, 16, 17, 100, 513, 1400, 2200]
     w, cache, alloc, seqs, ks, vs = _setup(G, 2, d, B, dtype, 80 + G, lens)
