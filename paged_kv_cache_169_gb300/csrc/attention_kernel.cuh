@@ -494,7 +494,10 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     constexpr int NSW = C::NSW, D = C::D, G = C::G, CT = C::CT;
     static_assert(CT == 16 && D == 128, "tensor-core consumer shape");
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-    const int g = lane >> 2, t = lane & 3;          // accumulator row (query) / column pair
+    // S^T = K Q^T and O^T += V^T P^T: the 16 tokens of a chunk (and 16 dims of an output
+    // tile) are the mma's M side, the query heads (padded to 8) its N side, so no mma row
+    // is padding.  Lane (g, t): token rows g and g+8, query columns 2t and 2t+1.
+    const int g = lane >> 2, t = lane & 3;
     // byte x (0..255) of fp16 token row tok in a chunk: copies of rpc rows (8 or 16), each
     // laid out half-major [2][rpc][64 halves], 128-byte swizzled.  fp16 stages are laid out
     // by the tensor-map copies (rpc = min(B, 16)); the FP8 path's dequantised scratch is
@@ -525,13 +528,13 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             *reinterpret_cast<uint4*>(scr + tile_off(r, 2 * c + 16)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
     };
-    uint32_t qa[8][2];
-    float o[16][4];
-    float m = -CUDART_INF_F, l = 0.f;
+    uint32_t qa[8][2];                 // B fragments of Q^T: query g, dims 16k+2t.. and 16k+8+2t..
+    float ot[8][4];                    // O^T tile i: dims 16i+g / 16i+g+8, queries 2t / 2t+1
+    float m2[2] = {-CUDART_INF_F, -CUDART_INF_F}, l2[2] = {0.f, 0.f};   // queries 2t, 2t+1
     #pragma unroll
     for (int i = 0; i < 8; ++i) { qa[i][0] = 0u; qa[i][1] = 0u; }
     #pragma unroll
-    for (int j = 0; j < 16; ++j) { o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f; }
+    for (int i = 0; i < 8; ++i) { ot[i][0] = ot[i][1] = ot[i][2] = ot[i][3] = 0.f; }
     Ticket tk{};
 
     for (int j = 0;; ++j) {
@@ -549,11 +552,11 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
         const int nt = mp->ntok, lo = mp->lo, ms = mp->s, mh = mp->h, mpart = mp->p;
         uint32_t kbase = smem_u32(stg + C::K_OFF), vbase = smem_u32(stg + C::V_OFF);
         if (flags & F_FIRST) {
-            m = -CUDART_INF_F;
-            l = 0.f;
+            m2[0] = m2[1] = -CUDART_INF_F;
+            l2[0] = l2[1] = 0.f;
             #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) { o[jj][0] = o[jj][1] = o[jj][2] = o[jj][3] = 0.f; }
-            // A fragments of the G query rows (fp16: staged with the item's first chunk;
+            for (int i = 0; i < 8; ++i) { ot[i][0] = ot[i][1] = ot[i][2] = ot[i][3] = 0.f; }
+            // B fragments of the G query rows (fp16: staged with the item's first chunk;
             // FP8: read from global memory once per item)
             const bool real = g < G && nt > 0;
             const uint32_t* qrow = C::FP8
@@ -618,42 +621,44 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
             }
-            // S = Q K^T
-            float sacc[2][4];
-            #pragma unroll
-            for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+            // S^T = K Q^T, the even and odd k-steps in two accumulators (shorter chains)
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
             const int mi = lane >> 3, mr = lane & 7;
             #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                // matrices: (tok 0-7, dims 16k..+7) (tok 0-7, +8..) (tok 8-15, 16k..) (tok 8-15, +8..)
-                const int tok = (mi >> 1) * 8 + mr, cp = 2 * k + (mi & 1);
-                uint32_t kb[4];
-                ldsm_x4(kbase + tile_off(tok, cp * 16), kb);
-                mma_16816(sacc[0], qa[k][0], 0u, qa[k][1], 0u, kb[0], kb[1]);
-                mma_16816(sacc[1], qa[k][0], 0u, qa[k][1], 0u, kb[2], kb[3]);
+                // A = K: (tok 0-7, dims 16k..) (tok 8-15, 16k..) (tok 0-7, +8..) (tok 8-15, +8..)
+                const int tok = (mi & 1) * 8 + mr, cp = 2 * k + (mi >> 1);
+                uint32_t kf[4];
+                ldsm_x4(kbase + tile_off(tok, cp * 16), kf);
+                if (k & 1) mma_16816(sb, kf[0], kf[1], kf[2], kf[3], qa[k][0], qa[k][1]);
+                else mma_16816(sa, kf[0], kf[1], kf[2], kf[3], qa[k][0], qa[k][1]);
             }
-            // row g: tokens 2t, 2t+1 (tile 0) and 8+2t, 9+2t (tile 1); log2-domain scores
-            const float qk0 = a.qscale * ks0, qk1 = a.qscale * ks1;   // ks = 1 for fp16 pools
-            float x[4] = {sacc[0][0] * qk0, sacc[0][1] * qk0, sacc[1][0] * qk1, sacc[1][1] * qk1};
-            const int tk[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
-            float mx = -CUDART_INF_F;
+            // log2-domain scores of tokens g (x0: query 2t, x1: 2t+1) and g+8 (x2, x3)
+            const float qk0 = a.qscale * ks0, qk1 = a.qscale * ks1;   // K scales; 1 for fp16 pools
+            const bool v0 = g >= lo && g < nt, v1 = g + 8 >= lo && g + 8 < nt;
+            float x[4] = {v0 ? (sa[0] + sb[0]) * qk0 : -CUDART_INF_F, v0 ? (sa[1] + sb[1]) * qk0 : -CUDART_INF_F,
+                          v1 ? (sa[2] + sb[2]) * qk1 : -CUDART_INF_F, v1 ? (sa[3] + sb[3]) * qk1 : -CUDART_INF_F};
+            // column maxima over the 16 tokens: the 8 lanes of equal t hold them
+            float mxa = fmaxf(x[0], x[2]), mxb = fmaxf(x[1], x[3]);
             #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                x[i] = (tk[i] >= lo && tk[i] < nt) ? x[i] : -CUDART_INF_F;
-                mx = fmaxf(mx, x[i]);
+            for (int off = 4; off < 32; off <<= 1) {
+                mxa = fmaxf(mxa, __shfl_xor_sync(FULL, mxa, off));
+                mxb = fmaxf(mxb, __shfl_xor_sync(FULL, mxb, off));
             }
-            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
-            const float m_new = fmaxf(m, mx);
-            const float corr = ex2_approx(m - m_new);
-            float pr[4], ps = 0.f;
+            const float ma = fmaxf(m2[0], mxa), mb = fmaxf(m2[1], mxb);
+            const float ca = ex2_approx(m2[0] - ma), cb = ex2_approx(m2[1] - mb);
+            const float p0 = ex2_approx(x[0] - ma), p1 = ex2_approx(x[1] - mb);
+            const float p2 = ex2_approx(x[2] - ma), p3 = ex2_approx(x[3] - mb);
+            l2[0] = fmaf(l2[0], ca, p0 + p2);        // this lane's tokens only; summed at the end
+            l2[1] = fmaf(l2[1], cb, p1 + p3);
+            m2[0] = ma;
+            m2[1] = mb;
             #pragma unroll
-            for (int i = 0; i < 4; ++i) { pr[i] = ex2_approx(x[i] - m_new); ps += pr[i]; }
-            l = fmaf(l, corr, ps);
-            #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) { o[jj][0] *= corr; o[jj][1] *= corr; }
-            m = m_new;
-            const uint32_t pa0 = pack_half2(pr[0] * vs0, pr[1] * vs0), pa2 = pack_half2(pr[2] * vs1, pr[3] * vs1);
+            for (int i = 0; i < 8; ++i) { ot[i][0] *= ca; ot[i][2] *= ca; ot[i][1] *= cb; ot[i][3] *= cb; }
+            // P^T as the B operand: the 8x8 blocks (tokens x queries) this lane holds a row
+            // pair of, transposed in registers (V scales folded in; 1 for fp16 pools)
+            const uint32_t pb0 = movmatrix_t(pack_half2(p0 * vs0, p1 * vs0));
+            const uint32_t pb1 = movmatrix_t(pack_half2(p2 * vs1, p3 * vs1));
             if constexpr (C::FP8) {
                 // V into the scratch once every lane is done reading K from it; rows outside
                 // [lo, nt) are zeroed so that their p = 0 contributes exactly nothing
@@ -668,45 +673,55 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 __syncwarp();
                 vbase = smem_u32(scr);
             }
-            // O += P V
+            // O^T += V^T P^T, one 16-dim tile per mma
             #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                // matrices: (tok 0-7, dims 16jj..) (tok 8-15, 16jj..) (tok 0-7, +8..) (tok 8-15, +8..)
-                const int tok = (mi & 1) * 8 + mr, cp = 2 * jj + (mi >> 1);
-                uint32_t vb[4];
-                ldsm_x4_t(vbase + tile_off(tok, cp * 16), vb);
-                mma_16816(o[2 * jj], pa0, 0u, pa2, 0u, vb[0], vb[1]);
-                mma_16816(o[2 * jj + 1], pa0, 0u, pa2, 0u, vb[2], vb[3]);
+            for (int i = 0; i < 8; ++i) {
+                // A = V^T: (dims 16i.., tok 0-7) (dims 16i+8.., tok 0-7) (16i.., tok 8-15) (16i+8.., tok 8-15)
+                const int tok = (mi >> 1) * 8 + mr, cp = 2 * i + (mi & 1);
+                uint32_t vf[4];
+                ldsm_x4_t(vbase + tile_off(tok, cp * 16), vf);
+                mma_16816(ot[i], vf[0], vf[1], vf[2], vf[3], pb0, pb1);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars[C::NC * NSW + w * NSW + st]));
         ticket_resolve<D, G>(a, tk, lane);            // the previous item's ticket
         if (flags & F_LAST) {
-            float lr = l + __shfl_xor_sync(FULL, l, 1);
-            lr += __shfl_xor_sync(FULL, lr, 2);
+            float la = l2[0], lb = l2[1];
+            #pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                la += __shfl_xor_sync(FULL, la, off);
+                lb += __shfl_xor_sync(FULL, lb, off);
+            }
             const int64_t shk = static_cast<int64_t>(ms) * a.H + mh;
-            const int64_t sq = shk * G + g;
-            if (flags & F_SINGLE) {
-                if (g < G) {
-                    const float inv = nt > 0 ? 1.f / lr : 0.f;
-                    float* dst = a.out + sq * D + 2 * t;
+            #pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {              // query 2t + h2
+                const int q = 2 * t + h2;
+                if (q >= G) continue;
+                const int64_t sq = shk * G + q;
+                if (flags & F_SINGLE) {
+                    const float inv = nt > 0 ? 1.f / (h2 ? lb : la) : 0.f;
+                    float* dst = a.out + sq * D + g;
                     #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj)
-                        *reinterpret_cast<float2*>(dst + 8 * jj) =
-                            nt > 0 ? make_float2(o[jj][0] * inv, o[jj][1] * inv) : make_float2(0.f, 0.f);
-                }
-            } else {
-                if (g < G) {
-                    const int64_t idx = sq * a.max_parts + mpart;
-                    if (t == 0) {
-                        a.part_ml[2 * idx] = m;
-                        a.part_ml[2 * idx + 1] = lr;
+                    for (int i = 0; i < 8; ++i) {
+                        dst[16 * i] = ot[i][h2] * inv;
+                        dst[16 * i + 8] = ot[i][2 + h2] * inv;
                     }
-                    float* dst = a.part_o + idx * D + 2 * t;
+                } else {
+                    const int64_t idx = sq * a.max_parts + mpart;
+                    if (g == 0) {
+                        a.part_ml[2 * idx] = m2[h2];
+                        a.part_ml[2 * idx + 1] = h2 ? lb : la;
+                    }
+                    float* dst = a.part_o + idx * D + g;
                     #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) *reinterpret_cast<float2*>(dst + 8 * jj) = make_float2(o[jj][0], o[jj][1]);
+                    for (int i = 0; i < 8; ++i) {
+                        dst[16 * i] = ot[i][h2];
+                        dst[16 * i + 8] = ot[i][2 + h2];
+                    }
                 }
+            }
+            if (!(flags & F_SINGLE)) {
                 const int ctx_s = s_ctx[ms];
                 const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
                 ticket_issue(a, tk, shk, mpart, np, lane);

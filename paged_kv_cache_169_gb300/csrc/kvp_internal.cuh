@@ -165,6 +165,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
 }
 
 // D += A(16x16, fp16, row) * B(16x8, fp16, col) with fp32 accumulation.
+// Transpose of an 8x8 b16 matrix held one row pair per lane (lane 4r + c: row r, cols 2c, 2c+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
     asm volatile(
