@@ -130,7 +130,10 @@ struct Cfg {
     using QT = QT_;
     static constexpr int ESZ = sizeof(KV);
     static constexpr bool FP8 = (ESZ == 1);
-    static constexpr int CT = (G >= 4 || MMA) ? 16 : Tune<ESZ>::CT;   // bounds G*CT/2 sums per lane
+    // G*CT/2 sums per lane bound the CUDA-core consumer; the tensor-core consumer takes 16
+    // tokens per step (FP8: two steps per 32-token chunk, so a chunk moves as many bytes
+    // as an fp16 one)
+    static constexpr int CT = MMA ? (ESZ == 1 ? 32 : 16) : (G >= 4 ? 16 : Tune<ESZ>::CT);
     static constexpr int TPL = CT / 2;                    // tokens per lane per chunk
     static constexpr int DPL = D / 16;                    // dims per lane
     static constexpr int CBMAX = CT / 8;                  // blocks per chunk at B = 8
@@ -148,7 +151,7 @@ struct Cfg {
     static constexpr bool SWZ_STAGE = MMA && !FP8;        // stages hold swizzled tensor-map tiles
     static constexpr int Q_STAGE = MMA ? 0 : Q_BYTES;
     static constexpr int QR_BYTES = SWZ_STAGE ? Q_BYTES : 0;
-    static constexpr int SCR_BYTES = (MMA && FP8) ? CT * D * 2 : 0;
+    static constexpr int SCR_BYTES = (MMA && FP8) ? 16 * D * 2 : 0;
     static constexpr int SC_OFF = Q_OFF + Q_STAGE;
     static constexpr int STAGE = round_up(SC_OFF + SC_BYTES, SWZ_STAGE ? 1024 : 128);
     static constexpr int NC_AUTO = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
@@ -492,7 +495,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 template <typename C>
 __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, const int* s_ctx, int w, int lane) {
     constexpr int NSW = C::NSW, D = C::D, G = C::G, CT = C::CT;
-    static_assert(CT == 16 && D == 128, "tensor-core consumer shape");
+    static_assert((CT == 16 || (C::FP8 && CT == 32)) && D == 128, "tensor-core consumer shape");
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     // S^T = K Q^T and O^T += V^T P^T: the 16 tokens of a chunk (and 16 dims of an output
     // tile) are the mma's M side, the query heads (padded to 8) its N side, so no mma row
@@ -597,17 +600,23 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
         }
-        if (nt > 0) {
-            // FP8: per-block scales of this thread's score columns (tokens 2t, 2t+1 and
-            // 8+2t, 9+2t) and the K tile dequantised into the scratch
+        // 16 tokens per step (a 32-token FP8 chunk takes two); a step with no token in
+        // [lo, nt) is skipped whole
+        #pragma unroll 1
+        for (int t16 = 0; t16 < CT; t16 += 16) {
+          if (t16 >= nt || t16 + 16 <= lo) continue;
+          {
+            // FP8: per-block scales of this lane's token rows (t16 + g and t16 + g + 8) and
+            // this step's K rows dequantised into the scratch
             float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
             if constexpr (C::FP8) {
-                const int id0 = mp->ids[0], id1 = mp->ids[(a.B < CT ? a.B : CT) == 8 ? 1 : 0];
+                const int rpc = a.B < CT ? a.B : CT;
+                const int id0 = mp->ids[t16 / rpc], id1 = mp->ids[(t16 + 8) / rpc];
                 ks0 = __ldg(a.kscale + id0);
                 ks1 = __ldg(a.kscale + id1);
                 vs0 = __ldg(a.vscale + id0);
                 vs1 = __ldg(a.vscale + id1);
-                dequant(stg + C::K_OFF);
+                dequant(stg + C::K_OFF + t16 * C::ROW);
                 __syncwarp();
                 kbase = smem_u32(scr);
             }
@@ -635,7 +644,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             }
             // log2-domain scores of tokens g (x0: query 2t, x1: 2t+1) and g+8 (x2, x3)
             const float qk0 = a.qscale * ks0, qk1 = a.qscale * ks1;   // K scales; 1 for fp16 pools
-            const bool v0 = g >= lo && g < nt, v1 = g + 8 >= lo && g + 8 < nt;
+            const bool v0 = t16 + g >= lo && t16 + g < nt, v1 = t16 + g + 8 >= lo && t16 + g + 8 < nt;
             float x[4] = {v0 ? (sa[0] + sb[0]) * qk0 : -CUDART_INF_F, v0 ? (sa[1] + sb[1]) * qk0 : -CUDART_INF_F,
                           v1 ? (sa[2] + sb[2]) * qk1 : -CUDART_INF_F, v1 ? (sa[3] + sb[3]) * qk1 : -CUDART_INF_F};
             // column maxima over the 16 tokens: the 8 lanes of equal t hold them
@@ -663,11 +672,11 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 // V into the scratch once every lane is done reading K from it; rows outside
                 // [lo, nt) are zeroed so that their p = 0 contributes exactly nothing
                 __syncwarp();
-                dequant(stg + C::V_OFF);
-                if (nt < CT || lo > 0) {
+                dequant(stg + C::V_OFF + t16 * C::ROW);
+                if (t16 + 16 > nt || t16 < lo) {
                     #pragma unroll 1
-                    for (int r = 0; r < CT; ++r)
-                        if ((r < lo || r >= nt) && lane < 16)
+                    for (int r = 0; r < 16; ++r)
+                        if ((t16 + r < lo || t16 + r >= nt) && lane < 16)
                             *reinterpret_cast<uint4*>(scr + tile_off(r, lane * 16)) = make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
@@ -682,6 +691,8 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 ldsm_x4_t(vbase + tile_off(tok, cp * 16), vf);
                 mma_16816(ot[i], vf[0], vf[1], vf[2], vf[3], pb0, pb1);
             }
+            if constexpr (C::FP8) __syncwarp();       // the next step rewrites the scratch
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars[C::NC * NSW + w * NSW + st]));
