@@ -803,7 +803,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         // holds more than two items and the tail stays balanced when items are few.
         unsigned pending = 0;                          // claimed next item (atomic in flight)
         bool claimed = false;
-        auto claim = [&]() { pending = atomicAdd(a.counter, 1u); claimed = true; };
+        // the first item of every lane is fixed (CTA-major), so the first copies need no
+        // atomic round trip; claimed items are numbered after them
+        const unsigned first_claim = gridDim.x * NC;
+        auto claim = [&]() { pending = atomicAdd(a.counter, 1u) + first_claim; claimed = true; };
         auto decode = [&](unsigned idx) {
             return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, a.H, a.P, a.window, rpc);
         };
@@ -820,7 +823,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         int c = 0, fills = 0;
         bool alive = mine;
         if (mine) {
-            cur = decode(atomicAdd(a.counter, 1u));
+            cur = decode(blockIdx.x * NC + lane);
             if (cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
             load_ids(cur, 0);
         }
@@ -1157,6 +1160,7 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
             sa.part_ml = args.part_ml + 2 * pofs;
             sa.part_o = args.part_o + pofs * C::D;
             sa.arrivals = args.arrivals + static_cast<int64_t>(s0) * args.H;
+            if (args.grp_arrivals) sa.grp_arrivals = args.grp_arrivals + static_cast<int64_t>(s0) * args.H * args.n_grp;
         }
         sa.counter = counters + sub;
         const int64_t upper = static_cast<int64_t>(sa.batch) * args.H * args.max_parts;

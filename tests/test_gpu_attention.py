@@ -243,10 +243,13 @@ def test_edge_lengths_and_errors():
 
 
 def test_large_batch_uses_several_launches():
-    """More than 1024 sequences: the batch is split across launches with separate counters."""
+    """More than 1024 sequences: the batch is split across launches with separate counters.
+    A few long sequences in every launch split into more than 16 partitions, so the
+    two-level merge's group counters of each launch are exercised too."""
     B, H, d = 8, 1, 64
     rng = np.random.default_rng(9)
     lens = rng.integers(0, 70, 2100).tolist()
+    lens[5], lens[1024 + 5], lens[2048 + 5] = 900, 1000, 700   # same slot in every launch
     nb = sum(-(-n // B) for n in lens) + 1
     w = W.Workload("bigbatch", 91, 1, H, d, B, "f16", len(lens), lens, nb, 0.125)
     cache = PagedKVCache(1, nb, B, H, d, "f16")
@@ -260,6 +263,10 @@ def test_large_batch_uses_several_launches():
     q = W.host_queries(w)
     out = cache.attention(0, torch.from_numpy(q).cuda(), bt, cl, max(lens), w.scale, partition_tokens=32)
     assert max_abs(out.cpu().numpy(), OA.decode_attention(q, ks, vs, w.scale)) <= tol_for("f16")
+    # grouped queries (2 per K/V head) over the same cache and launches
+    q2 = np.concatenate([q, q[:, :, ::-1]], axis=1).copy()
+    out2 = cache.attention_gqa(0, torch.from_numpy(q2).cuda(), bt, cl, max(lens), w.scale, partition_tokens=32)
+    assert max_abs(out2.cpu().numpy(), OA.decode_attention_gqa(q2, ks, vs, w.scale)) <= tol_for("f16")
     assert cache.device_error() == 0
 
 
