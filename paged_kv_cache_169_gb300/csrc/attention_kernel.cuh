@@ -803,8 +803,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         // holds more than two items and the tail stays balanced when items are few.
         unsigned pending = 0;                          // claimed next item (atomic in flight)
         bool claimed = false;
-        // the first item of every lane is fixed (CTA-major), so the first copies need no
-        // atomic round trip; claimed items are numbered after them
+        // the first item of every lane is fixed, so the first copies need no atomic round
+        // trip; claimed items are numbered after them.  Lane-major order spreads a job with
+        // fewer items than consumer warps evenly over the SMs.
         const unsigned first_claim = gridDim.x * NC;
         auto claim = [&]() { pending = atomicAdd(a.counter, 1u) + first_claim; claimed = true; };
         auto decode = [&](unsigned idx) {
@@ -823,7 +824,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         int c = 0, fills = 0;
         bool alive = mine;
         if (mine) {
-            cur = decode(blockIdx.x * NC + lane);
+            cur = decode(lane * gridDim.x + blockIdx.x);
             if (cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
             load_ids(cur, 0);
         }
