@@ -24,6 +24,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak); seq-steps/s"
+# kv_decode_args.flags: KV_DECODE_WORKSPACE_ZEROED = 1, KV_DECODE_PDL = 2
+LAUNCH_FLAGS = {"none": 0, "zeroed": 1, "pdl": 3}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -319,7 +321,11 @@ def run_ours(args):
     out = torch.empty((L, w.batch, Hq, d), dtype=torch.float32, device=dev)
     max_ctx = max(w.lens)
     grouped = Hq != H
-    if args.window:
+    flags = LAUNCH_FLAGS[args.launch_flags]
+    if flags & 1:
+        # zero-filled once; every decode launch leaves its counters zero again
+        ws = cache.zeroed_workspace(w.batch, max_ctx, args.partition, num_q_heads=Hq, window=args.window)
+    elif args.window:
         from paged_kv_cache_169_gb300 import abi as _abi
         xa = _abi.kv_decode_args()
         xa.num_q_heads, xa.batch, xa.max_context = Hq, w.batch, max_ctx
@@ -343,11 +349,11 @@ def run_ours(args):
                 cache.append(l, k_new[l], v_new[l], slots)
             if ev is not None:
                 ev[l][0].record(stream)
-            if args.window:
+            if args.window or flags:
                 cache.attention_ex(l, q[l], bt, cl, max_ctx, w.scale, window=args.window,
                                    k_new=None if args.unfused else k_new[l],
                                    v_new=None if args.unfused else v_new[l], out=out[l],
-                                   partition_tokens=args.partition, workspace=ws)
+                                   partition_tokens=args.partition, workspace=ws, flags=flags)
             elif grouped:
                 cache.attention_gqa(l, q[l], bt, cl, max_ctx, w.scale,
                                     k_new=None if args.unfused else k_new[l],
@@ -451,7 +457,7 @@ def run_ours(args):
                                                              (1 if w.kv == "fp8" else 2) / 2 ** 30, 2),
                    "l2": "no flush: inputs (the KV pool) larger than L2",
                    "partition_tokens": args.partition or "auto", "parallelism": f"replica x{world}",
-                   "window": args.window or None,
+                   "window": args.window or None, "launch_flags": args.launch_flags,
                    "step": "kv_append + paged_decode_attention" if args.unfused
                            else "paged_decode_attention_append (fused)"},
         "pct_of_peak": 100.0 * value / world / peak,
@@ -569,13 +575,20 @@ def run_decode_steps(args):
     q, kn, vn = (torch.randn(shape, generator=g, device=dev).half() for _ in range(3))
     out = torch.empty(shape, dtype=torch.float32, device=dev)
     max_ctx = max(init) + S
-    ws = cache.workspace(w.batch, max_ctx, args.partition)
+    flags = LAUNCH_FLAGS[args.launch_flags]
+    ws = (cache.zeroed_workspace(w.batch, max_ctx, args.partition) if flags & 1
+          else cache.workspace(w.batch, max_ctx, args.partition))
     stream = torch.cuda.Stream(dev)
 
     def loop():
         for i in range(S):
-            cache.attention_append(0, q[i], kn[i], vn[i], bt, lens[i], max_ctx, w.scale, out=out[i],
-                                   partition_tokens=args.partition, workspace=ws, stream=stream)
+            if flags:
+                cache.attention_ex(0, q[i], bt, lens[i], max_ctx, w.scale, k_new=kn[i], v_new=vn[i],
+                                   out=out[i], partition_tokens=args.partition, workspace=ws, stream=stream,
+                                   flags=flags)
+            else:
+                cache.attention_append(0, q[i], kn[i], vn[i], bt, lens[i], max_ctx, w.scale, out=out[i],
+                                       partition_tokens=args.partition, workspace=ws, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -634,6 +647,7 @@ def run_decode_steps(args):
         "vs_baseline": None, "dtype": "f32-accum/f16", "data": "synthetic",
         "config": {"workload": "decode7b", "layers": 1, "batch": w.batch, "heads": H, "head_dim": d,
                    "block_size": BS, "decode_steps_per_replay": S, "context_before": [min(init), max(init)],
+                   "launch_flags": args.launch_flags,
                    "l2": "flushed (256 MB write) between timed replays", "step": "64 fused calls, one CUDA graph"},
         "seq_steps_per_s": w.batch * S / (graph_ms / 1e3),
         "eager": {"ms_per_64_steps": eager_ms, "GB/s": step_bytes / (eager_ms / 1e3) / 1e9},
@@ -703,15 +717,22 @@ def run_parallel(args):
     q, kn, vn = (torch.randn(shape, generator=g, device=dev).half() for _ in range(3))
     out = torch.empty(shape, dtype=torch.float32, device=dev)
     max_ctx = prompt + S
-    ws = cache.workspace(C, max_ctx, args.partition)
+    flags = LAUNCH_FLAGS[args.launch_flags]
+    ws = (cache.zeroed_workspace(C, max_ctx, args.partition) if flags & 1
+          else cache.workspace(C, max_ctx, args.partition))
     stream = torch.cuda.Stream(dev)
 
     def loop():
         for i in range(S):
             if cows[i] is not None:
                 cache.copy_blocks(cows[i], stream=stream)
-            cache.attention_append(0, q[i], kn[i], vn[i], bt[i], cl[i], max_ctx, w.scale, out=out[i],
-                                   partition_tokens=args.partition, workspace=ws, stream=stream)
+            if flags:
+                cache.attention_ex(0, q[i], bt[i], cl[i], max_ctx, w.scale, k_new=kn[i], v_new=vn[i],
+                                   out=out[i], partition_tokens=args.partition, workspace=ws, stream=stream,
+                                   flags=flags)
+            else:
+                cache.attention_append(0, q[i], kn[i], vn[i], bt[i], cl[i], max_ctx, w.scale, out=out[i],
+                                       partition_tokens=args.partition, workspace=ws, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -741,7 +762,7 @@ def run_parallel(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32-accum/f16", "data": "synthetic",
         "config": {"workload": "parallel", "layers": 1, "candidates": C, "prompt": prompt, "decode_steps": S,
-                   "heads": H, "head_dim": d, "block_size": BS, "cow_copies": n_cow,
+                   "heads": H, "head_dim": d, "block_size": BS, "cow_copies": n_cow, "launch_flags": args.launch_flags,
                    "blocks_in_use": w.num_blocks - len(alloc.free_list()),
                    "l2": "flushed (256 MB write) before each timed 128-step run",
                    "step": "128 x (block copies + fused append + attention), one run per timed step"},
@@ -772,6 +793,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="time kv_append + paged_decode_attention as two calls")
     ap.add_argument("--window", type=int, default=0, help="sliding-window decode over the last N tokens")
+    ap.add_argument("--launch-flags", choices=sorted(LAUNCH_FLAGS), default="pdl",
+                    help="zeroed: a zero-filled workspace kept across calls (no clearing copy per call); "
+                         "pdl: zeroed + programmatic dependent launch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -282,7 +282,22 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *                only to the last W tokens of its sequence (all of them when shorter), as the
  *                rolling-window cache of [KV缓存机制解析] §8 keeps the most recent tokens.
  *                Blocks lying wholly before position context_len - W are never read, so the
- *                host may release them (kv_alloc_seq_trim) and leave their table entries -1. */
+ *                host may release them (kv_alloc_seq_trim) and leave their table entries -1.
+ *   flags        0, or a sum of:
+ *     KV_DECODE_WORKSPACE_ZEROED  the workspace's counters are already zero, so the call
+ *                does not clear them (one cudaMemsetAsync less per call).  True for a
+ *                workspace zero-filled once after allocation and used since only by decode
+ *                calls of this library that left no device error bit: every launch leaves
+ *                its counters zero when it completes.  After a device error, zero-fill the
+ *                workspace again before passing this flag.
+ *     KV_DECODE_PDL  launch with programmatic dependent launch: the kernel may be scheduled
+ *                while the previous kernel on the stream is still finishing; it reads no
+ *                global memory (inputs, pool or workspace) before that kernel has completed
+ *                and its writes are visible.  Saves the launch gap between back-to-back
+ *                kernels (with KV_DECODE_WORKSPACE_ZEROED no clearing copy sits between
+ *                two consecutive decode calls).  Also valid inside stream capture. */
+#define KV_DECODE_WORKSPACE_ZEROED 1u
+#define KV_DECODE_PDL 2u
 typedef struct {
     int layer;
     const void* q;
@@ -302,6 +317,7 @@ typedef struct {
     void* workspace;
     size_t workspace_bytes;
     kv_stream_t stream;
+    unsigned flags;
 } kv_decode_args;
 
 /* Workspace bytes for paged_decode_attention_ex with these arguments (0 on invalid ones). */

@@ -17,6 +17,7 @@ KV_ERR_CUDA, KV_ERR_DEVICE, KV_ERR_UNSUPPORTED = -4, -5, -6
 KV_F32, KV_F16, KV_FP8_E4M3 = 0, 1, 2
 KV_DEVERR_SLOT, KV_DEVERR_BLOCK_ID, KV_DEVERR_CONTEXT, KV_DEVERR_TIMEOUT = 1, 2, 4, 8
 KV_FEATURE_TENSOR_MAPS = 1
+KV_DECODE_WORKSPACE_ZEROED, KV_DECODE_PDL = 1, 2
 
 
 class KvError(RuntimeError):
@@ -36,7 +37,8 @@ class kv_decode_args(C.Structure):
                 ("out", C.c_void_p), ("block_tables", C.c_void_p), ("max_blocks_per_seq", C.c_int),
                 ("context_lens", C.c_void_p), ("batch", C.c_int), ("max_context", C.c_int),
                 ("window", C.c_int), ("scale", C.c_float), ("partition_tokens", C.c_int),
-                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("stream", C.c_void_p)]
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("stream", C.c_void_p),
+                ("flags", C.c_uint)]
 
 
 class kv_alloc_stats_t(C.Structure):

@@ -179,9 +179,11 @@ class PagedKVCache:
                      context_lens: torch.Tensor, max_context: int, scale: float, window: int = 0,
                      k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
                      out: torch.Tensor | None = None, partition_tokens: int = 0,
-                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                     workspace: torch.Tensor | None = None, stream=None, flags: int = 0) -> torch.Tensor:
         """Every decode option in one call (paged_decode_attention_ex): grouped-query heads
-        (q [batch, Hq, d]), optional fused append, and a sliding window of ``window`` tokens."""
+        (q [batch, Hq, d]), optional fused append, and a sliding window of ``window`` tokens.
+        ``flags``: abi.KV_DECODE_WORKSPACE_ZEROED (the workspace's counters are zero: a
+        zero-filled workspace used only by decode calls since) and/or abi.KV_DECODE_PDL."""
         batch, hq = q.shape[0], q.shape[1]
         if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
             raise ValueError("block_tables and context_lens must be int32")
@@ -203,8 +205,18 @@ class PagedKVCache:
             workspace = self._ws
         a.workspace, a.workspace_bytes = _dev_ptr(workspace, "workspace"), workspace.numel()
         a.stream = _stream(stream)
+        a.flags = flags
         abi.paged_decode_attention_ex(self.handle, a)
         return out
+
+    def zeroed_workspace(self, batch: int, max_context: int, partition_tokens: int = 0,
+                         num_q_heads: int = 0, window: int = 0) -> torch.Tensor:
+        """A new zero-filled workspace for attention_ex(..., flags=KV_DECODE_WORKSPACE_ZEROED)."""
+        a = abi.kv_decode_args()
+        a.num_q_heads, a.batch, a.max_context = num_q_heads, batch, max_context
+        a.window, a.partition_tokens = window, partition_tokens
+        n = abi.paged_decode_workspace_size_ex(self.handle, a)
+        return torch.zeros(n, dtype=torch.uint8, device=self.k[0].device)
 
     def device_error(self, clear: bool = True, stream=None) -> int:
         return abi.kv_get_device_error(self.handle, _stream(stream), clear)

@@ -348,10 +348,12 @@ int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* x) {
         }
     }
     if (!(x->scale > 0.f) || !(x->scale < 3.0e38f)) return KV_ERR_INVALID_ARG;
+    if (x->flags & ~(KV_DECODE_WORKSPACE_ZEROED | KV_DECODE_PDL)) return KV_ERR_INVALID_ARG;
     kvp::AttnPlan plan;
     int rc = kvp::plan_attention(pool, x->batch, x->max_context, x->partition_tokens, &plan, group, x->window);
     if (rc != KV_OK) return rc;
     if (x->workspace_bytes < plan.ws_bytes) return KV_ERR_INVALID_ARG;
+    plan.flags = x->flags;
     return kvp::launch_attention_append(pool, x->layer, x->q, x->k_new, x->v_new,
                                         x->k_new ? kvp::elem_bytes(x->in_dtype) : 0, x->out, x->block_tables,
                                         x->max_blocks_per_seq, x->context_lens, x->batch, x->max_context,

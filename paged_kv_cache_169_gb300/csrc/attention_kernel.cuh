@@ -56,7 +56,8 @@ struct AttnArgs {
     const int32_t* lens;
     float* part_ml;        // [batch*H*max_parts][2]  (m in log2 units, l)
     float* part_o;         // [batch*H*max_parts][D]  unnormalised
-    unsigned* counter;
+    unsigned* counter;     // work items claimed so far (this launch)
+    unsigned* exit_counter;  // producer warps that have finished (this launch)
     unsigned* arrivals;    // [batch*H] partitions (or partition groups) finished per (sequence, head)
     unsigned* grp_arrivals;  // [batch*H][n_grp] partitions finished per group of kMergeFan
     int n_grp;             // ceil(max_parts / kMergeFan) when max_parts > kMergeFan, else 0
@@ -77,6 +78,7 @@ namespace {
 
 constexpr int kMaxBatch = 1024;    // sequences per launch (prefix table in shared memory)
 constexpr int kMaxSub = 64;        // launches per call -> batch <= 65536
+static_assert(2 * kMaxSub * sizeof(unsigned) <= kCounterBytes, "work + exit counters");
 constexpr int kPartAlign = 32;     // partition sizes are multiples of this
 #if defined(KVP_CLAIM_LEAD)
 constexpr int kClaimLead = KVP_CLAIM_LEAD;   // tuning sweeps only
@@ -409,6 +411,7 @@ __device__ __forceinline__ void ticket_resolve(const AttnArgs& a, Ticket& tk, in
         const int grp = tk.p / kMergeFan;
         const int gsz = min(kMergeFan, tk.np - grp * kMergeFan);
         if (prev != static_cast<unsigned>(gsz - 1)) return;
+        if (lane == 0) a.grp_arrivals[tk.shk * a.n_grp + grp] = 0;   // left zero for the next call
         __syncwarp();
         merge_partials<D, G, false>(a, tk.shk * G, grp * kMergeFan, gsz, 1, lane);
         __syncwarp();
@@ -419,6 +422,7 @@ __device__ __forceinline__ void ticket_resolve(const AttnArgs& a, Ticket& tk, in
         prev = __shfl_sync(FULL, p2, 0);
     }
     if (prev != static_cast<unsigned>(count - 1)) return;
+    if (lane == 0) a.arrivals[tk.shk] = 0;                             // left zero for the next call
     __syncwarp();
     merge_partials<D, G, true>(a, tk.shk * G, 0, count, stride, lane);
 }
@@ -755,6 +759,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
     int* s_end = s_ctx + kMaxBatch;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    if (tid == 0) {
+        for (int i = 0; i < 2 * NC * NSW; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        fence_mbar_init();
+    }
+    // Programmatic dependent launch: nothing above read global memory.  Wait for the
+    // kernels this launch depends on (a no-op when it was launched without that
+    // attribute), then let the next launch on the stream begin scheduling: its CTAs start
+    // as this launch's CTAs exit and wait here in turn.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // ---- prologue: clamp lengths, items per sequence, inclusive prefix
     for (int s = tid; s < a.batch; s += C::THREADS) {
         int c = a.lens[s];
@@ -764,10 +778,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         }
         s_ctx[s] = c;
         s_end[s] = a.H * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), a.P);
-    }
-    if (tid == 0) {
-        for (int i = 0; i < 2 * NC * NSW; ++i) mbar_init(smem_u32(&bars[i]), 1);
-        fence_mbar_init();
     }
     __syncthreads();
     if (warp == 0) {
@@ -935,6 +945,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             for (int st = 0; st < NSW && st < fills; ++st) {
                 const int last = fills - 1 - ((fills - 1 - st) % NSW);
                 mbar_wait_bounded(full_bar(w, st), (last / NSW) & 1, a.err);
+            }
+        }
+        // The last producer warp of the launch to finish (all claims made and read) leaves
+        // the work and exit counters zero for the next call on this workspace.
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(a.exit_counter, 1u) == gridDim.x - 1) {
+                *reinterpret_cast<volatile unsigned*>(a.counter) = 0u;
+                *reinterpret_cast<volatile unsigned*>(a.exit_counter) = 0u;
             }
         }
         return;
@@ -1164,14 +1183,32 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
             if (args.grp_arrivals) sa.grp_arrivals = args.grp_arrivals + static_cast<int64_t>(s0) * args.H * args.n_grp;
         }
         sa.counter = counters + sub;
+        sa.exit_counter = counters + kMaxSub + sub;
         const int64_t upper = static_cast<int64_t>(sa.batch) * args.H * args.max_parts;
         int64_t grid = (upper + C::NC - 1) / C::NC;
         if (grid > pool->num_sms) grid = pool->num_sms;
         if (grid < 1) grid = 1;
-        attention_partition_kernel<C><<<static_cast<int>(grid), C::THREADS, C::SMEM, stream>>>(sa);
+        if (plan.flags & KV_DECODE_PDL) {
+            // may begin while the previous kernel on the stream finishes (see the kernel)
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(grid));
+            cfg.blockDim = dim3(C::THREADS);
+            cfg.dynamicSmemBytes = C::SMEM;
+            cfg.stream = stream;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaLaunchKernelEx(&cfg, attention_partition_kernel<C>, sa) != cudaSuccess) {
+                cudaGetLastError();
+                return KV_ERR_CUDA;
+            }
+        } else {
+            attention_partition_kernel<C><<<static_cast<int>(grid), C::THREADS, C::SMEM, stream>>>(sa);
+        }
         if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
     }
-    (void)plan;
     return KV_OK;
 }
 

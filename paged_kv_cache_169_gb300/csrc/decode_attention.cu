@@ -92,7 +92,8 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     plan->consumers = nc;
     plan->group = group;
     plan->window = window;
-    size_t ws = 256;                                // kMaxSub work counters
+    plan->flags = 0;
+    size_t ws = kCounterBytes;                      // work and exit counters
     if (plan->max_parts > 1) {
         const size_t n = static_cast<size_t>(batch) * d.num_heads * group * plan->max_parts;
         ws += plan->arrivals_bytes(batch, d.num_heads);
@@ -121,8 +122,12 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     char* ws = static_cast<char*>(workspace);
     unsigned* counters = reinterpret_cast<unsigned*>(ws);
     const size_t arrivals_bytes = plan.arrivals_bytes(batch, d.num_heads);
-    // work counters and per-(sequence, KV head) arrival counters start at zero every call
-    if (cudaMemsetAsync(counters, 0, 256 + arrivals_bytes, stream) != cudaSuccess) return KV_ERR_CUDA;
+    // the counters must be zero when the kernel starts; every launch leaves them zero when
+    // it completes without a device error, so a caller that keeps the workspace for decode
+    // calls may say so (KV_DECODE_WORKSPACE_ZEROED) and skip this clearing
+    if (!(plan.flags & KV_DECODE_WORKSPACE_ZEROED) &&
+        cudaMemsetAsync(counters, 0, kCounterBytes + arrivals_bytes, stream) != cudaSuccess)
+        return KV_ERR_CUDA;
 
     AttnArgs a{};
     a.kpool = static_cast<char*>(pool->k_layers[layer]);
@@ -138,11 +143,12 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     a.lens = context_lens;
     if (plan.max_parts > 1) {
         const size_t n = static_cast<size_t>(batch) * d.num_heads * group * plan.max_parts;
-        a.arrivals = reinterpret_cast<unsigned*>(ws + 256);
-        a.grp_arrivals = reinterpret_cast<unsigned*>(ws + 256 + align256(static_cast<size_t>(batch) * d.num_heads * 4));
+        a.arrivals = reinterpret_cast<unsigned*>(ws + kCounterBytes);
+        a.grp_arrivals =
+            reinterpret_cast<unsigned*>(ws + kCounterBytes + align256(static_cast<size_t>(batch) * d.num_heads * 4));
         a.n_grp = merge_groups(plan.max_parts);
-        a.part_ml = reinterpret_cast<float*>(ws + 256 + arrivals_bytes);
-        a.part_o = reinterpret_cast<float*>(ws + 256 + arrivals_bytes + align256(n * 2 * sizeof(float)));
+        a.part_ml = reinterpret_cast<float*>(ws + kCounterBytes + arrivals_bytes);
+        a.part_o = reinterpret_cast<float*>(ws + kCounterBytes + arrivals_bytes + align256(n * 2 * sizeof(float)));
     }
     a.err = pool->d_err;
     a.batch = batch;

@@ -43,7 +43,12 @@ int launch_swap(const kv_pool* pool, bool out, const int32_t* blocks, int num_bl
 constexpr int kMergeFan = 16;
 inline int merge_groups(int max_parts) { return max_parts > kMergeFan ? (max_parts + kMergeFan - 1) / kMergeFan : 0; }
 
+// Start of every decode workspace: kMaxSub work counters, then kMaxSub exit counters
+// (u32 each); the arrival counters and the partials follow.
+constexpr size_t kCounterBytes = 512;
+
 struct AttnPlan {
+    unsigned flags = 0;  // KV_DECODE_* of the call (kv_decode_args.flags)
     int partition;       // tokens per split-context partition
     int max_parts;       // ceil(max_context / partition)
     int consumers;       // consumer warps per CTA
