@@ -122,26 +122,38 @@ template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_
 // MMA_: grouped-query tensor-core consumer (head_dim 128, G >= 2).  fp16 pools are fed by
 // swizzled tensor-map copies; FP8 pools by plain bulk copies, each tile dequantised to a
 // swizzled fp16 scratch in shared memory before the mma.
-template <int D_, typename KV_, typename QT_, int G_ = 1, bool MMA_ = false>
+// HP_ = 2 (one query per KV head only): a work item covers two adjacent heads.  Their
+// (block, head) tiles are adjacent in the pool, so one bulk copy brings both: half as many
+// copies per byte, which is what limits pools with small tiles (FP8, and fp16 with B = 8).
+// The two half-warps take one head each.  BR_ is then the block size (8 or 16), fixed at
+// compile time because each copy holds whole blocks of both heads.
+template <int D_, typename KV_, typename QT_, int G_ = 1, bool MMA_ = false, int HP_ = 1, int BR_ = 0>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int G = G_;
     static constexpr bool MMA = MMA_;
+    static constexpr int HP = HP_;
+    static constexpr int BR = BR_;
+    static constexpr int GE = G_ * HP_;                   // output rows per work item
     static_assert(!MMA || (sizeof(KV_) <= 2 && D_ == 128 && G_ >= 2), "tensor-core path: fp16 or FP8, d 128, G >= 2");
+    static_assert(HP == 1 || (HP == 2 && G == 1 && !MMA && (BR == 8 || BR == 16)), "head pairs: one query per head");
     using KV = KV_;
     using QT = QT_;
     static constexpr int ESZ = sizeof(KV);
     static constexpr bool FP8 = (ESZ == 1);
     // G*CT/2 sums per lane bound the CUDA-core consumer; the tensor-core consumer takes 16
     // tokens per step (FP8: two steps per 32-token chunk, so a chunk moves as many bytes
-    // as an fp16 one)
-    static constexpr int CT = MMA ? (ESZ == 1 ? 32 : 16) : (G >= 4 ? 16 : Tune<ESZ>::CT);
-    static constexpr int TPL = CT / 2;                    // tokens per lane per chunk
+    // as an fp16 one).  Head pairs: a chunk of CT tokens of two heads (fp16: 8, FP8: 16),
+    // as many bytes as the single-head chunk.
+    static constexpr int CT = MMA ? (ESZ == 1 ? 32 : 16)
+                                  : HP == 2 ? 16 / ESZ : (G >= 4 ? 16 : Tune<ESZ>::CT);
+    static_assert(HP == 1 || BR <= CT, "head pairs: whole blocks per copy");
+    static constexpr int TPL = CT * HP / 2;               // tokens per lane per chunk
     static constexpr int DPL = D / 16;                    // dims per lane
-    static constexpr int CBMAX = CT / 8;                  // blocks per chunk at B = 8
+    static constexpr int CBMAX = CT >= 8 ? CT / 8 : 1;    // blocks per chunk at B = 8
     static constexpr int ROW = D * ESZ;                   // bytes of one token row of one head
-    static constexpr int KV_BYTES = CT * ROW;             // bytes of K (or V) per chunk
-    static constexpr int Q_BYTES = G * D * sizeof(QT);     // the G query rows of one KV head
+    static constexpr int KV_BYTES = CT * ROW * HP;        // bytes of K (or V) per chunk
+    static constexpr int Q_BYTES = GE * D * sizeof(QT);   // the query rows of one item
     static constexpr int SC_BYTES = 0;
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = KV_BYTES;
@@ -182,7 +194,7 @@ struct Cfg {
     static constexpr int ALIGN_SLACK = MMA ? 1024 : 0;           // to 1024-align the base
     static constexpr int SMEM = PREFIX_OFF + 2 * kMaxBatch * 4 + ALIGN_SLACK;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    static_assert(NC <= 32 && (CT == 16 || CT == 32), "launch shape");
+    static_assert(NC <= 32 && (CT == 8 || CT == 16 || CT == 32), "launch shape");
     static_assert(Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && META_R % 16 == 0 && QR_OFF % 16 == 0, "alignment");
 };
 
@@ -208,6 +220,17 @@ __device__ __forceinline__ float warp_max(float v) {
 __device__ __forceinline__ float warp_sum(float v) {
     #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+    return v;
+}
+// over the 16 lanes of each half-warp
+__device__ __forceinline__ float half_max(float v) {
+    #pragma unroll
+    for (int o = 8; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+    return v;
+}
+__device__ __forceinline__ float half_sum(float v) {
+    #pragma unroll
+    for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
     return v;
 }
 
@@ -758,6 +781,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
     int* s_ctx = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
     int* s_end = s_ctx + kMaxBatch;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int HU = a.H / C::HP;                 // work units (single heads or head pairs) per sequence
 
     if (tid == 0) {
         for (int i = 0; i < 2 * NC * NSW; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -777,7 +801,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             c = c < 0 ? 0 : a.ctx_limit;
         }
         s_ctx[s] = c;
-        s_end[s] = a.H * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), a.P);
+        s_end[s] = HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), a.P);
     }
     __syncthreads();
     if (warp == 0) {
@@ -807,7 +831,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         const bool mine = lane < NC;
         const int w = mine ? lane : 0;
         const int rpc = a.B < CT ? a.B : CT;           // token rows per copy (whole block if B <= CT)
-        const uint32_t tile = static_cast<uint32_t>(rpc) * C::ROW;
+        // bytes per copy: rpc rows of each of the item's HP heads (adjacent in the pool)
+        const uint32_t tile = static_cast<uint32_t>(rpc) * C::ROW * C::HP;
         // Items are claimed one at a time: the next one only while the current item's last
         // two chunks are filled (its atomic then has a chunk's time to return), so no lane
         // holds more than two items and the tail stays balanced when items are few.
@@ -819,7 +844,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         const unsigned first_claim = gridDim.x * NC;
         auto claim = [&]() { pending = atomicAdd(a.counter, 1u) + first_claim; claimed = true; };
         auto decode = [&](unsigned idx) {
-            return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, a.H, a.P, a.window, rpc);
+            return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, HU, a.P, a.window, rpc);
         };
         int ids[CBMAX];
         auto load_ids = [&](const Item& it, int chunk) {
@@ -892,7 +917,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                     #pragma unroll
                     for (int j = 0; j < CBMAX; ++j) {
                         if (j < nblk) {
-                            const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h) * a.B +
+                            const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h * C::HP) * a.B +
                                                   row0) * C::ROW;
                             if constexpr (C::SWZ_STAGE) {
                                 // rpc token rows of one head as [2][rows][64], 128-byte swizzled
@@ -907,7 +932,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                     }
                     if (with_q) {
                         const char* qsrc = static_cast<const char*>(a.q) +
-                                           (static_cast<int64_t>(cur.s) * a.H + cur.h) * C::Q_BYTES;
+                                           (static_cast<int64_t>(cur.s) * HU + cur.h) * C::Q_BYTES;
                         const uint32_t qdst = C::QR_BYTES ? smem_u32(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES)
                                                           : dst + C::Q_OFF;
                         bulk_g2s(qdst, qsrc, C::Q_BYTES, fb);
@@ -964,12 +989,21 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         consumer_mma<C>(a, smem, s_ctx, warp, lane);
         return;
     }
-    constexpr int G = C::G;
+    constexpr int G = C::G, HP = C::HP, GE = C::GE, BR = C::BR;
     const int w = warp;
-    const int half = lane >> 4;                 // which token of each row pair
+    // single heads: the half-warps take alternate tokens (half = which token of each row
+    // pair); head pairs: half-warp e takes head e of the pair, every token of the chunk
+    const int half = lane >> 4;
     const int sub = lane & 15;                  // which DPL-element slice of the row
-    const int tok_l = 2 * (lane & (TPL - 1)) + half;     // token whose score this lane holds
-    const bool primary = (lane & 15) < TPL;              // one holder per token when CT = 16
+    const int tok_l = HP == 2 ? (lane & (TPL - 1)) : 2 * (lane & (TPL - 1)) + half;   // token whose score this lane holds
+    const bool primary = (lane & 15) < TPL;              // one holder per token when TPL < 16
+    // stage byte offset of token row t (of the lane's head, from its K/V base): with head
+    // pairs each copy holds BR rows of head 0, then BR rows of head 1
+    auto tok_off = [](int t) -> int {
+        if constexpr (HP == 2) return (t / BR) * 2 * BR * C::ROW + (t % BR) * C::ROW;
+        else return t * C::ROW;
+    };
+    const int head_off = HP == 2 ? half * BR * C::ROW : half * C::ROW;
     float2 q2[G][DPL / 2], acc[G][DPL / 2];
     float m[G], lsum[G];
     #pragma unroll
@@ -1007,25 +1041,31 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 lsum[g] = 0.f;
                 #pragma unroll
                 for (int i = 0; i < DPL / 2; ++i) acc[g][i] = make_float2(0.f, 0.f);
-                if (nt > 0) load_q<C>(stg + C::Q_OFF + g * D * sizeof(typename C::QT), sub, a.qscale, q2[g]);
+                if (nt > 0) load_q<C>(stg + C::Q_OFF + (HP == 2 ? half : g) * D * sizeof(typename C::QT), sub,
+                                      a.qscale, q2[g]);
             }
         }
         if (meta.flags & F_PATCH) {
             // this warp owns the stage now: put the new token into its row and its slot
             const Meta* mp = reinterpret_cast<const Meta*>(mst);
             const int r = mp->patch_row;
-            const int64_t sh = static_cast<int64_t>(meta.s) * a.H + meta.h;
-            const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + meta.h) * a.B + mp->patch_off;
             float ksc = 1.f, vsc = 1.f;
             if constexpr (C::FP8) {
                 ksc = __ldg(a.kscale + mp->patch_id);
                 vsc = __ldg(a.vscale + mp->patch_id);
             }
             char* srow = const_cast<char*>(stg);
-            patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, srow + C::K_OFF + r * C::ROW,
-                         a.kpool + grow * C::ROW, ksc, lane);
-            patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, srow + C::V_OFF + r * C::ROW,
-                         a.vpool + grow * C::ROW, vsc, lane);
+            #pragma unroll
+            for (int e = 0; e < HP; ++e) {          // every head of the item
+                const int head = meta.h * HP + e;
+                const int64_t sh = static_cast<int64_t>(meta.s) * a.H + head;
+                const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + head) * a.B + mp->patch_off;
+                const int so = tok_off(r) + (HP == 2 ? e * BR * C::ROW : 0);
+                patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, srow + C::K_OFF + so,
+                             a.kpool + grow * C::ROW, ksc, lane);
+                patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, srow + C::V_OFF + so,
+                             a.vpool + grow * C::ROW, vsc, lane);
+            }
             // the stage is refilled by the TMA engine later: order these generic writes first
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
@@ -1039,13 +1079,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 ks = __ldg(a.kscale + id);
                 vs = __ldg(a.vscale + id);
             }
-            const char* K = stg + C::K_OFF + half * C::ROW;
-            const char* V = stg + C::V_OFF + half * C::ROW;
+            const char* K = stg + C::K_OFF + head_off;
+            const char* V = stg + C::V_OFF + head_off;
             float part[G][TPL];
             #pragma unroll
-            for (int i = 0; i < TPL; ++i) {          // token 2i + half; one K load serves G queries
+            for (int i = 0; i < TPL; ++i) {          // token 2i + half (pairs: i); one K load serves G queries
                 float2 kx[DPL / 2];
-                load_row<C>(K + 2 * i * C::ROW, sub, kx);
+                load_row<C>(K + tok_off(HP == 2 ? i : 2 * i), sub, kx);
                 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     float2 d2 = make_float2(0.f, 0.f);
@@ -1074,7 +1114,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 if constexpr (C::FP8) x *= ks;
                 x = (tok_l < nt && tok_l >= lo) ? x : -CUDART_INF_F;
                 if (__any_sync(FULL, x > m[g] + 8.f)) {   // raise the running max only when needed
-                    const float m_new = fmaxf(m[g], warp_max(x));
+                    const float m_new = fmaxf(m[g], HP == 2 ? half_max(x) : warp_max(x));
                     const float corr = ex2_approx(m[g] - m_new);
                     lsum[g] *= corr;
                     #pragma unroll
@@ -1086,13 +1126,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 pv[g] = pr * vs;
             }
             #pragma unroll
-            for (int i = 0; i < TPL; ++i) {          // token 2i + half, its p from lane i (+16)
+            for (int i = 0; i < TPL; ++i) {          // token 2i + half (pairs: i), its p from lane i (+16)
                 float pt[G];
                 #pragma unroll
                 for (int g = 0; g < G; ++g) pt[g] = __shfl_sync(FULL, pv[g], i + (lane & 16));
-                if ((nt == CT && lo == 0) || (2 * i + half < nt && 2 * i + half >= lo)) {
+                const int ti = HP == 2 ? i : 2 * i + half;
+                if ((nt == CT && lo == 0) || (ti < nt && ti >= lo)) {
                     float2 vx[DPL / 2];
-                    load_row<C>(V + 2 * i * C::ROW, sub, vx);
+                    load_row<C>(V + tok_off(HP == 2 ? i : 2 * i), sub, vx);
                     #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float2 p2 = make_float2(pt[g], pt[g]);
@@ -1104,21 +1145,25 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(w, st));
-        ticket_resolve<D, G>(a, tk, lane);            // the previous item's ticket
+        ticket_resolve<D, GE>(a, tk, lane);           // the previous item's ticket
         if (meta.flags & F_LAST) {
-            const int64_t shk = static_cast<int64_t>(meta.s) * a.H + meta.h;   // (sequence, KV head)
+            const int64_t shk = static_cast<int64_t>(meta.s) * HU + meta.h;   // (sequence, work unit)
             #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float l = warp_sum(lsum[g]);
+                const float l = HP == 2 ? half_sum(lsum[g]) : warp_sum(lsum[g]);
                 float2 o[DPL / 2];
                 #pragma unroll
-                for (int i = 0; i < DPL / 2; ++i) {   // the two halves saw different tokens
-                    o[i].x = acc[g][i].x + __shfl_xor_sync(FULL, acc[g][i].x, 16);
-                    o[i].y = acc[g][i].y + __shfl_xor_sync(FULL, acc[g][i].y, 16);
+                for (int i = 0; i < DPL / 2; ++i) {
+                    if constexpr (HP == 2) {
+                        o[i] = acc[g][i];              // each half holds its own head
+                    } else {                           // the two halves saw different tokens
+                        o[i].x = acc[g][i].x + __shfl_xor_sync(FULL, acc[g][i].x, 16);
+                        o[i].y = acc[g][i].y + __shfl_xor_sync(FULL, acc[g][i].y, 16);
+                    }
                 }
-                const int64_t sq = shk * G + g;        // (sequence, query head)
+                const int64_t sq = shk * GE + (HP == 2 ? half : g);   // (sequence, query head)
                 if (meta.flags & F_SINGLE) {
-                    if (half == 0) {
+                    if (HP == 2 || half == 0) {
                         float2* dst = reinterpret_cast<float2*>(a.out + sq * D + sub * DPL);
                         const float inv = nt > 0 ? 1.f / l : 0.f;   // empty sequence -> zeros
                         #pragma unroll
@@ -1127,11 +1172,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                     }
                 } else {
                     const int64_t idx = sq * a.max_parts + meta.p;
-                    if (lane == 0) {
+                    if (HP == 2 ? sub == 0 : lane == 0) {
                         a.part_ml[2 * idx] = m[g];
                         a.part_ml[2 * idx + 1] = l;
                     }
-                    if (half == 0) {
+                    if (HP == 2 || half == 0) {
                         float2* dst = reinterpret_cast<float2*>(a.part_o + idx * D + sub * DPL);
                         #pragma unroll
                         for (int i = 0; i < DPL / 2; ++i) dst[i] = o[i];
@@ -1146,7 +1191,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             }
         }
     }
-    ticket_resolve<D, G>(a, tk, lane);
+    ticket_resolve<D, GE>(a, tk, lane);
 }
 
 template <typename C>
@@ -1184,7 +1229,7 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
         }
         sa.counter = counters + sub;
         sa.exit_counter = counters + kMaxSub + sub;
-        const int64_t upper = static_cast<int64_t>(sa.batch) * args.H * args.max_parts;
+        const int64_t upper = static_cast<int64_t>(sa.batch) * (args.H / C::HP) * args.max_parts;
         int64_t grid = (upper + C::NC - 1) / C::NC;
         if (grid > pool->num_sms) grid = pool->num_sms;
         if (grid < 1) grid = 1;

@@ -28,7 +28,32 @@ int consumers_for_g(const kv_pool* pool) {
                              : consumers_of<Cfg<64, uint8_t, __half, G>>();
 }
 
+}  // namespace
+
+// Block rows of the head-pair configuration (Cfg HP = 2) this pool runs single-query
+// decode with, or 0 for one head per work item.  Pools whose (block, head) tiles are
+// small pay for every copy: FP8 pools with B = 8 or 16, fp16 pools with B = 8 (head_dim
+// 128, an even number of heads).  KVP_NO_HEAD_PAIRS (tuning builds only) turns it off.
+int head_pair_rows(const kv_pool_desc& d, int group) {
+#if defined(KVP_NO_HEAD_PAIRS)
+    (void)d; (void)group;
+    return 0;
+#else
+    if (group != 1 || d.head_dim != 128 || d.num_heads % 2 != 0) return 0;
+    if (d.dtype == KV_FP8_E4M3 && (d.block_size == 8 || d.block_size == 16)) return d.block_size;
+    if (d.dtype == KV_F16 && d.block_size == 8) return 8;
+    return 0;
+#endif
+}
+
+namespace {
+
 int consumers_for(const kv_pool* pool, int group) {
+    if (const int br = head_pair_rows(pool->desc, group)) {
+        if (pool->desc.dtype == KV_F16) return consumers_of<Cfg<128, __half, __half, 1, false, 2, 8>>();
+        return br == 8 ? consumers_of<Cfg<128, uint8_t, __half, 1, false, 2, 8>>()
+                       : consumers_of<Cfg<128, uint8_t, __half, 1, false, 2, 16>>();
+    }
     switch (group) {
         case 2: return consumers_for_g<2>(pool);
         case 4: return consumers_for_g<4>(pool);
@@ -62,8 +87,9 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
         if (partition_tokens % kPartAlign != 0 || partition_tokens > cap) return KV_ERR_INVALID_ARG;
         P = partition_tokens;
     } else if (partition_tokens == 0) {
-        // work items are (sequence, KV head, partition), handed out dynamically
-        const int64_t units = static_cast<int64_t>(batch > 0 ? batch : 1) * d.num_heads;
+        // work items are (sequence, KV head or head pair, partition), handed out dynamically
+        const int64_t units = static_cast<int64_t>(batch > 0 ? batch : 1) * d.num_heads /
+                              (head_pair_rows(d, group) ? 2 : 1);
         const int64_t warps = static_cast<int64_t>(pool->num_sms) * nc;
         int64_t parts;
         if (group == 1) {
@@ -171,6 +197,12 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     if (d.dtype == KV_F32) {
         if (d.head_dim == 128) return launch_typed<Cfg<128, float, float>>(pool, a, plan, counters, stream);
         return launch_typed<Cfg<64, float, float>>(pool, a, plan, counters, stream);
+    }
+    if (const int br = head_pair_rows(d, 1)) {      // two heads per work item
+        if (d.dtype == KV_F16)
+            return launch_typed<Cfg<128, __half, __half, 1, false, 2, 8>>(pool, a, plan, counters, stream);
+        if (br == 8) return launch_typed<Cfg<128, uint8_t, __half, 1, false, 2, 8>>(pool, a, plan, counters, stream);
+        return launch_typed<Cfg<128, uint8_t, __half, 1, false, 2, 16>>(pool, a, plan, counters, stream);
     }
     if (d.dtype == KV_F16) {
         if (d.head_dim == 128) return launch_typed<Cfg<128, __half, __half>>(pool, a, plan, counters, stream);

@@ -143,11 +143,11 @@ def test_parallel_sampling_cow_and_attention():
 
 # ------------------------------------------------------------------ ragged (fp16 / fp8), small
 
-def _ragged_small(B, dtype, seed):
+def _ragged_small(B, dtype, seed, H=4):
     rng = np.random.default_rng(seed)
     lens = np.floor(np.exp(rng.uniform(0, math.log(3000), 24))).astype(int).tolist()
     lens[:5] = [1, B, B + 1, 32, 33]
-    H, d = 4, 128
+    d = 128
     nb = sum(-(-n // B) for n in lens) + 9
     w = W.Workload("ragged_small", seed, 1, H, d, B, "f16", len(lens), lens, nb, 1 / math.sqrt(d))
     cache = PagedKVCache(1, nb, B, H, d, dtype)
@@ -175,8 +175,11 @@ def _ragged_small(B, dtype, seed):
 
 @pytest.mark.parametrize("B", [8, 16, 32])
 @pytest.mark.parametrize("dtype", ["f16", "fp8"])
-def test_ragged_small_against_full_oracle(B, dtype):
-    w, cache, alloc, seqs, ks, vs = _ragged_small(B, dtype, 50 + B)
+@pytest.mark.parametrize("H", [4, 3])
+def test_ragged_small_against_full_oracle(B, dtype, H):
+    """An even head count takes the head-pair launch shape for FP8 pools with B 8 or 16 and
+    fp16 pools with B 8; an odd one keeps one head per work item."""
+    w, cache, alloc, seqs, ks, vs = _ragged_small(B, dtype, 50 + B, H)
     max_blocks = max(-(-n // B) for n in w.lens)
     bt, cl, lens = tables_for(alloc, seqs, max_blocks)
     q = W.host_queries(w)
