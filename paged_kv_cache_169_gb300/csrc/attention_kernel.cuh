@@ -541,21 +541,20 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     char* scr = smem + C::SCR_OFF + w * C::SCR_BYTES;      // FP8 only: fp16 K, then V, of a chunk
     // FP8: the 16 rows x 128 codes at src become fp16 rows of the scratch (exact: every
     // E4M3 value is an fp16 value); the block scales are applied to S and P instead
+    // Lane tasks: 16 rows x 16 pieces of 8 codes.  A half-warp reads one 128-byte row and
+    // each quarter-warp writes 8 distinct 16-byte chunks of one 128-byte scratch line, so
+    // neither the loads nor the stores conflict on banks.
     auto dequant = [&](const char* src) {
         #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int task = lane + 32 * i;                 // 16 rows x 8 pieces of 16 codes
-            const int r = task >> 3, c = (task & 7) * 16;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + c);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint32_t h[8];
-            #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                h[2 * k] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w4[k] & 0xffffu));
-                h[2 * k + 1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w4[k] >> 16));
-            }
-            *reinterpret_cast<uint4*>(scr + tile_off(r, 2 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(scr + tile_off(r, 2 * c + 16)) = make_uint4(h[4], h[5], h[6], h[7]);
+        for (int i = 0; i < 8; ++i) {
+            const int task = lane + 32 * i;
+            const int r = task >> 4, c = (task & 15) * 8;
+            const uint2 v = *reinterpret_cast<const uint2*>(src + r * 128 + c);
+            const uint32_t h0 = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.x & 0xffffu));
+            const uint32_t h1 = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.x >> 16));
+            const uint32_t h2 = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.y & 0xffffu));
+            const uint32_t h3 = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.y >> 16));
+            *reinterpret_cast<uint4*>(scr + tile_off(r, 2 * c)) = make_uint4(h0, h1, h2, h3);
         }
     };
     uint32_t qa[8][2];                 // B fragments of Q^T: query g, dims 16k+2t.. and 16k+8+2t..
