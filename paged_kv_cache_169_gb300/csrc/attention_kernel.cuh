@@ -330,8 +330,11 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
     r.s = s;
     r.h = rr / np;
     r.p = rr - r.h * np;
-    r.tok0 = first + r.p * P;
-    r.ntok = min(P, ctx - r.tok0);
+    // the np partitions of a context split it evenly (each a multiple of kPartAlign tokens,
+    // at most P): items of one sequence have about one size, which evens out the finish
+    const int ps = np > 1 ? ((ctx - first + np - 1) / np + kPartAlign - 1) / kPartAlign * kPartAlign : P;
+    r.tok0 = first + r.p * ps;
+    r.ntok = min(ps, ctx - r.tok0);
     r.lo = r.p == 0 ? attend_start(ctx, window) - first : 0;
     r.nchunks = r.ntok > 0 ? (r.ntok + CT - 1) / CT : 1;
     r.single = np == 1;
