@@ -67,6 +67,7 @@ struct AttnArgs {
     int window;            // > 0: attend only to the last `window` tokens of each sequence
     int* err;
     int batch, H, B, max_blocks, ctx_limit, P, max_parts, num_blocks;
+    int P_fine, s_fine;    // sequences s >= s_fine split into partitions of P_fine tokens (< P)
     float qscale;          // scale * log2(e)
 };
 
@@ -202,6 +203,10 @@ struct Cfg {
 
 __device__ __forceinline__ int nparts_of(int ctx, int P) { return ctx <= P ? 1 : (ctx + P - 1) / P; }
 
+// Partition size of sequence s: the sequences handed out last (s >= s_fine) take finer
+// partitions, so the last round of work items is short and the launch ends evenly.
+__device__ __forceinline__ int part_of(const AttnArgs& a, int s) { return s >= a.s_fine ? a.P_fine : a.P; }
+
 // Sliding window: the first attended token, and the first token actually read — rounded
 // down to a whole copy unit (rpc rows) so every copy stays inside blocks the window still
 // holds.  Rows in [first, start) are read but masked.
@@ -312,7 +317,8 @@ struct __align__(16) Item {
 // (s, h, p) of compact item index `it` (items ordered by sequence, head, partition).
 template <int CT>
 __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ctx, const int* s_end,
-                                            int batch, int H, int P, int window, int rpc) {
+                                            int batch, int H, int P_coarse, int s_fine, int P_fine, int window,
+                                            int rpc) {
     Item r{};
     r.valid = it < n_items;
     if (!r.valid) return r;
@@ -322,6 +328,7 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
         if (s_end[mid] > it) hi = mid; else lo = mid + 1;
     }
     const int s = lo;
+    const int P = s >= s_fine ? P_fine : P_coarse;
     const int start = s ? s_end[s - 1] : 0;
     const int ctx = s_ctx[s];
     const int first = attend_first(ctx, window, rpc);
@@ -763,7 +770,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             }
             if (!(flags & F_SINGLE)) {
                 const int ctx_s = s_ctx[ms];
-                const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
+                const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), part_of(a, ms));
                 ticket_issue(a, tk, shk, mpart, np, lane);
             }
         }
@@ -803,7 +810,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             c = c < 0 ? 0 : a.ctx_limit;
         }
         s_ctx[s] = c;
-        s_end[s] = HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), a.P);
+        s_end[s] = HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), part_of(a, s));
     }
     __syncthreads();
     if (warp == 0) {
@@ -846,7 +853,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         const unsigned first_claim = gridDim.x * NC;
         auto claim = [&]() { pending = atomicAdd(a.counter, 1u) + first_claim; claimed = true; };
         auto decode = [&](unsigned idx) {
-            return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, HU, a.P, a.window, rpc);
+            return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, HU, a.P, a.s_fine,
+                                   a.P_fine, a.window, rpc);
         };
         int ids[CBMAX];
         auto load_ids = [&](const Item& it, int chunk) {
@@ -1188,7 +1196,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             if (!(meta.flags & F_SINGLE)) {
                 // publish the partials, then take a ticket; the last partition merges
                 const int ctx_s = s_ctx[meta.s];
-                const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), a.P);
+                const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT),
+                                         part_of(a, meta.s));
                 ticket_issue(a, tk, shk, meta.p, np, lane);
             }
         }
@@ -1229,6 +1238,7 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
             sa.arrivals = args.arrivals + static_cast<int64_t>(s0) * args.H;
             if (args.grp_arrivals) sa.grp_arrivals = args.grp_arrivals + static_cast<int64_t>(s0) * args.H * args.n_grp;
         }
+        sa.s_fine = args.s_fine - s0 > 0 ? args.s_fine - s0 : 0;
         sa.counter = counters + sub;
         sa.exit_counter = counters + kMaxSub + sub;
         const int64_t upper = static_cast<int64_t>(sa.batch) * (args.H / C::HP) * args.max_parts;

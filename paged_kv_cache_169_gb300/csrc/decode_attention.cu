@@ -114,7 +114,27 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
         return KV_ERR_INVALID_ARG;
     }
     plan->partition = P;
-    plan->max_parts = span <= P ? 1 : (span + P - 1) / P;
+    plan->fine_partition = P;
+    plan->fine_from = batch;
+    if (partition_tokens == 0 && P >= 512) {
+        // A launch of several rounds of work items ends with the last round: items claimed
+        // last finish up to an item's time apart.  With long items (512 tokens and more)
+        // the sequences handed out last, about one round of items' worth of tokens, take
+        // half-size partitions (measured: ragged 256 sequences +1 % fp16, +4 % FP8; with
+        // 256-token items it gained nothing and the doubled split count of long contexts
+        // cost 3 %).
+        const int hu = d.num_heads / (head_pair_rows(d, group) ? 2 : 1);
+        const int64_t warps = static_cast<int64_t>(pool->num_sms) * nc;
+        const int64_t items = static_cast<int64_t>(batch) * hu * ((span + P - 1) / P);
+        if (items >= 2 * warps) {
+            const int64_t per_seq = static_cast<int64_t>(span) * hu;
+            const int64_t n_fine = (warps * P + per_seq - 1) / per_seq;
+            plan->fine_from = static_cast<int>(batch - (n_fine < batch ? n_fine : batch));
+            plan->fine_partition = (P / 2 + kPartAlign - 1) / kPartAlign * kPartAlign;
+        }
+    }
+    const int pmin = plan->fine_from < batch ? plan->fine_partition : P;
+    plan->max_parts = span <= pmin ? 1 : (span + pmin - 1) / pmin;
     plan->consumers = nc;
     plan->group = group;
     plan->window = window;
@@ -184,6 +204,8 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     const int64_t lim_tables = static_cast<int64_t>(max_blocks) * d.block_size;
     a.ctx_limit = static_cast<int>(lim_tables < max_context ? lim_tables : max_context);
     a.P = plan.partition;
+    a.P_fine = plan.fine_partition;
+    a.s_fine = plan.fine_from;
     a.max_parts = plan.max_parts;
     a.num_blocks = d.num_blocks;
     a.qscale = scale * 1.4426950408889634f;        // log2(e): softmax evaluated with 2^x

@@ -50,12 +50,14 @@ constexpr size_t kCounterBytes = 512;
 struct AttnPlan {
     unsigned flags = 0;  // KV_DECODE_* of the call (kv_decode_args.flags)
     int partition;       // tokens per split-context partition
-    int max_parts;       // ceil(max_context / partition)
+    int fine_partition;  // tokens per partition of the sequences from fine_from on
+    int fine_from;       // first sequence with the finer partitions (batch: none)
+    int max_parts;       // ceil(max_context / smallest partition)
     int consumers;       // consumer warps per CTA
     int group;           // query heads per KV head
     int window;          // > 0: sliding window of the last `window` tokens
     size_t ws_bytes;     // workspace bytes
-    // zero-initialised counters after the 256 work-counter bytes: the per-(sequence, head)
+    // zero-initialised counters after the kCounterBytes of work counters: the per-(sequence, head)
     // arrivals, then the per-partition-group arrivals
     size_t arrivals_bytes(int batch, int heads) const {
         if (max_parts <= 1) return 0;

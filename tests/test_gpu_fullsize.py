@@ -138,3 +138,42 @@ def test_ragged_full_size_sampled(B, dtype):
     assert cache.device_error() == 0
     del cache
     torch.cuda.empty_cache()
+
+
+def test_finer_partitions_for_the_sequences_handed_out_last():
+    """A long launch of long items (library partitioning picks 576 tokens here: 128
+    sequences of 12k-16k tokens, 4 heads) gives the sequences handed out last half-size
+    partitions.  The plan shows it (a larger split count, hence a larger workspace than an
+    explicit 576-token partition).  Outputs agree with the explicit partitioning to fp32
+    rounding, and with the float64 oracle on sampled (sequence, head) pairs, the last
+    sequences included."""
+    B, H, d, batch = 16, 4, 128, 128
+    rng = np.random.default_rng(77)
+    lens = rng.integers(12000, 16385, batch).tolist()
+    lens[-1] = 16384
+    nbs = [-(-n // B) for n in lens]
+    w = W.Workload("fine_tail", 77, 1, H, d, B, "f16", batch, lens, sum(nbs), 1 / np.sqrt(d))
+    cache = PagedKVCache(1, w.num_blocks, B, H, d, "f16")
+    W.device_fill_normal(cache.k[0], 7701)
+    W.device_fill_normal(cache.v[0], 7702)
+    tables = W.shuffled_tables(w, nbs)
+    bt = torch.from_numpy(tables).cuda()
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    max_ctx = max(lens)
+    assert cache.workspace_bytes(batch, max_ctx, 0) > cache.workspace_bytes(batch, max_ctx, 576)
+    q = W.host_queries(w)
+    qt = torch.from_numpy(q).cuda()
+    auto = cache.attention(0, qt, bt, cl, max_ctx, w.scale, partition_tokens=0).cpu().numpy()
+    fixed = cache.attention(0, qt, bt, cl, max_ctx, w.scale, partition_tokens=576).cpu().numpy()
+    assert max_abs(auto, fixed) <= 1e-5
+    samples = [(int(rng.integers(batch)), int(rng.integers(H))) for _ in range(6)]
+    samples += [(batch - 1, H - 1), (batch - 2, 0), (batch - 5, 1), (0, 0)]
+    worst = 0.0
+    for s, h in samples:
+        K = _snapshot(cache.k[0], tables[s], nbs[s], h)[:lens[s]]
+        V = _snapshot(cache.v[0], tables[s], nbs[s], h)[:lens[s]]
+        worst = max(worst, max_abs(auto[s, h], OA.decode_attention_one(q[s, h], K, V, w.scale)))
+    assert worst <= tol_for("f16"), worst
+    assert cache.device_error() == 0
+    del cache
+    torch.cuda.empty_cache()
