@@ -300,6 +300,47 @@ __device__ __forceinline__ void load_row(const char* row, int sub, float2 (&x)[C
     }
 }
 
+// c.x += lo(a)·lo(b), c.y += hi(a)·hi(b): fp16 operands, fp32 accumulation.  The product
+// of two fp16 values is exact in fp32, so this equals widening both operands first.
+__device__ __forceinline__ float2 hfma2_f32(uint32_t a, uint32_t b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %4;\n\tfma.rn.f32.f16 %1, ah, bh, %5;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(a), "r"(b), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// The lane's DPL consecutive elements of one fp16 or FP8 token row as DPL/2 fp16 pairs
+// (E4M3 -> fp16 is exact).
+template <typename C>
+__device__ __forceinline__ void load_row_h(const char* row, int sub, uint32_t (&x)[C::DPL / 2]) {
+    const char* p = row + sub * C::DPL * C::ESZ;
+    if constexpr (C::ESZ == 2) {
+        if constexpr (C::DPL == 8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p);
+            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+        } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            x[0] = v.x; x[1] = v.y;
+        }
+    } else {
+        static_assert(C::ESZ == 1, "fp16 or FP8 rows");
+        if constexpr (C::DPL == 8) {
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            x[0] = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.x & 0xffffu));
+            x[1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.x >> 16));
+            x[2] = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.y & 0xffffu));
+            x[3] = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.y >> 16));
+        } else {
+            const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+            x[0] = e4m3x2_to_half2_bits(static_cast<uint16_t>(v & 0xffffu));
+            x[1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(v >> 16));
+        }
+    }
+}
+
 template <typename C>
 __device__ __forceinline__ void load_q(const char* qrow, int sub, float qs, float2 (&x)[C::DPL / 2]) {
     using QT = typename C::QT;
@@ -1014,6 +1055,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         else return t * C::ROW;
     };
     const int head_off = HP == 2 ? half * BR * C::ROW : half * C::ROW;
+    // fp16 and FP8 rows with fp16 queries: products of fp16 operands accumulated in fp32
+    // (fma.f32.f16), no widening of the K/V elements; the query stays unscaled fp16 and
+    // the score scale multiplies the reduced dot product.  fp32 pools: fp32 throughout.
+    constexpr bool MX = C::ESZ <= 2 && sizeof(typename C::QT) == 2;
+    uint32_t qh[G][DPL / 2];
     float2 q2[G][DPL / 2], acc[G][DPL / 2];
     float m[G], lsum[G];
     #pragma unroll
@@ -1021,7 +1067,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         m[g] = -CUDART_INF_F;
         lsum[g] = 0.f;
         #pragma unroll
-        for (int i = 0; i < DPL / 2; ++i) { q2[g][i] = make_float2(0.f, 0.f); acc[g][i] = make_float2(0.f, 0.f); }
+        for (int i = 0; i < DPL / 2; ++i) {
+            q2[g][i] = make_float2(0.f, 0.f);
+            qh[g][i] = 0u;
+            acc[g][i] = make_float2(0.f, 0.f);
+        }
     }
     Ticket tk{};
 
@@ -1051,8 +1101,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 lsum[g] = 0.f;
                 #pragma unroll
                 for (int i = 0; i < DPL / 2; ++i) acc[g][i] = make_float2(0.f, 0.f);
-                if (nt > 0) load_q<C>(stg + C::Q_OFF + (HP == 2 ? half : g) * D * sizeof(typename C::QT), sub,
-                                      a.qscale, q2[g]);
+                const char* qrow = stg + C::Q_OFF + (HP == 2 ? half : g) * D * sizeof(typename C::QT);
+                if constexpr (MX) {
+                    if (nt > 0) {
+                        const uint32_t* qp = reinterpret_cast<const uint32_t*>(qrow) + sub * (DPL / 2);
+                        #pragma unroll
+                        for (int i = 0; i < DPL / 2; ++i) qh[g][i] = qp[i];
+                    }
+                } else {
+                    if (nt > 0) load_q<C>(qrow, sub, a.qscale, q2[g]);
+                }
             }
         }
         if (meta.flags & F_PATCH) {
@@ -1094,16 +1152,30 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             float part[G][TPL];
             #pragma unroll
             for (int i = 0; i < TPL; ++i) {          // token 2i + half (pairs: i); one K load serves G queries
-                float2 kx[DPL / 2];
-                load_row<C>(K + tok_off(HP == 2 ? i : 2 * i), sub, kx);
-                #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float2 d2 = make_float2(0.f, 0.f);
+                if constexpr (MX) {
+                    uint32_t kx[DPL / 2];
+                    load_row_h<C>(K + tok_off(HP == 2 ? i : 2 * i), sub, kx);
                     #pragma unroll
-                    for (int u = 0; u < DPL / 2; ++u) d2 = ffma2(q2[g][u], kx[u], d2);
-                    part[g][i] = d2.x + d2.y;
+                    for (int g = 0; g < G; ++g) {
+                        float2 d2 = make_float2(0.f, 0.f);
+                        #pragma unroll
+                        for (int u = 0; u < DPL / 2; ++u) d2 = hfma2_f32(qh[g][u], kx[u], d2);
+                        part[g][i] = d2.x + d2.y;
+                    }
+                } else {
+                    float2 kx[DPL / 2];
+                    load_row<C>(K + tok_off(HP == 2 ? i : 2 * i), sub, kx);
+                    #pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float2 d2 = make_float2(0.f, 0.f);
+                        #pragma unroll
+                        for (int u = 0; u < DPL / 2; ++u) d2 = ffma2(q2[g][u], kx[u], d2);
+                        part[g][i] = d2.x + d2.y;
+                    }
                 }
             }
+            // log2-domain score scale of this lane's token (FP8: times its block's K scale)
+            const float xs = MX ? (C::FP8 ? ks * a.qscale : a.qscale) : (C::FP8 ? ks : 1.f);
             float pv[G];
             #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -1121,7 +1193,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 float x = part[g][0];
                 #pragma unroll
                 for (int off = TPL; off < 16; off <<= 1) x += __shfl_xor_sync(FULL, x, off);
-                if constexpr (C::FP8) x *= ks;
+                x *= xs;
                 x = (tok_l < nt && tok_l >= lo) ? x : -CUDART_INF_F;
                 if (__any_sync(FULL, x > m[g] + 8.f)) {   // raise the running max only when needed
                     const float m_new = fmaxf(m[g], HP == 2 ? half_max(x) : warp_max(x));
@@ -1135,20 +1207,40 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 if (primary) lsum[g] += pr;
                 pv[g] = pr * vs;
             }
+            // MX: p goes to the V products as fp16 (as the tensor-core consumer's P operand
+            // does), packed once per lane and broadcast packed
+            uint32_t pvh[G];
+            #pragma unroll
+            for (int g = 0; g < G; ++g) pvh[g] = MX ? pack_half2(pv[g], pv[g]) : 0u;
             #pragma unroll
             for (int i = 0; i < TPL; ++i) {          // token 2i + half (pairs: i), its p from lane i (+16)
-                float pt[G];
-                #pragma unroll
-                for (int g = 0; g < G; ++g) pt[g] = __shfl_sync(FULL, pv[g], i + (lane & 16));
                 const int ti = HP == 2 ? i : 2 * i + half;
-                if ((nt == CT && lo == 0) || (ti < nt && ti >= lo)) {
-                    float2 vx[DPL / 2];
-                    load_row<C>(V + tok_off(HP == 2 ? i : 2 * i), sub, vx);
+                if constexpr (MX) {
+                    uint32_t ph[G];
                     #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float2 p2 = make_float2(pt[g], pt[g]);
+                    for (int g = 0; g < G; ++g) ph[g] = __shfl_sync(FULL, pvh[g], i + (lane & 16));
+                    if ((nt == CT && lo == 0) || (ti < nt && ti >= lo)) {
+                        uint32_t vx[DPL / 2];
+                        load_row_h<C>(V + tok_off(HP == 2 ? i : 2 * i), sub, vx);
                         #pragma unroll
-                        for (int u = 0; u < DPL / 2; ++u) acc[g][u] = ffma2(p2, vx[u], acc[g][u]);
+                        for (int g = 0; g < G; ++g) {
+                            #pragma unroll
+                            for (int u = 0; u < DPL / 2; ++u) acc[g][u] = hfma2_f32(ph[g], vx[u], acc[g][u]);
+                        }
+                    }
+                } else {
+                    float pt[G];
+                    #pragma unroll
+                    for (int g = 0; g < G; ++g) pt[g] = __shfl_sync(FULL, pv[g], i + (lane & 16));
+                    if ((nt == CT && lo == 0) || (ti < nt && ti >= lo)) {
+                        float2 vx[DPL / 2];
+                        load_row<C>(V + tok_off(HP == 2 ? i : 2 * i), sub, vx);
+                        #pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float2 p2 = make_float2(pt[g], pt[g]);
+                            #pragma unroll
+                            for (int u = 0; u < DPL / 2; ++u) acc[g][u] = ffma2(p2, vx[u], acc[g][u]);
+                        }
                     }
                 }
             }
