@@ -215,14 +215,21 @@ KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int ma
  *   max_context   host upper bound of context_lens (sizes the split-context workspace).
  *   scale         score multiplier, usually 1/sqrt(head_dim); finite and > 0.
  *   partition_tokens  0 = library choice (about 8 work items per consumer warp, one
- *                 round for grouped-query launches, 256 to 1024 tokens); else tokens
- *                 per split-context partition, a multiple of 32.  Sequences longer
- *                 than one partition are split, attended per partition and merged
- *                 exactly (log-sum-exp) in the same launch by the warp that finishes
- *                 the last partition of that sequence and head.
+ *                 round for grouped-query launches, 256 to 1024 tokens; with 512 or
+ *                 more and several rounds of items, the last sequences of the batch
+ *                 take half of it); else tokens per split-context partition, a
+ *                 multiple of 32.  Sequences longer than one partition are split into
+ *                 equal parts of at most that many tokens, attended per partition and
+ *                 merged exactly (log-sum-exp) in the same launch by the warp that
+ *                 finishes the last partition of that sequence and head.
  *   workspace     device, >= paged_decode_workspace_size(...) bytes, 256-byte aligned,
  *                 contents need not be initialised; not shared between concurrent calls.
- * Arithmetic: fp32 scores, fp32 online softmax, fp32 accumulation of V.
+ * Arithmetic: fp32 scores, fp32 online softmax, fp32 accumulation of V.  For F16 and
+ * FP8 pools the products are of fp16 operands (q, K and V elements as fp16; E4M3 codes
+ * convert to fp16 exactly) accumulated in fp32, and the softmax weights enter the V
+ * products as fp16 (relative rounding 2^-11; below 2^8 by the running maximum).  With
+ * the FP8 V scale folded into those weights, v_scale values must stay below 255.
+ * F32 pools: fp32 operands throughout.
  * The cached decode step of [KV Cache篇] §3.1 / [KV缓存机制解析] §5.1 over the
  * block-table gather of [PagedAttention] §3.2, with [KV Cache篇] §6.3's tiling. */
 KV_API int paged_decode_attention(kv_pool* pool, int layer, const void* q, float* out,
