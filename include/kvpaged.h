@@ -114,14 +114,13 @@ KV_API int kv_pool_destroy(kv_pool* pool);
 KV_API int kv_pool_get_desc(const kv_pool* pool, kv_pool_desc* desc);
 
 /* Fast paths the pool was set up with, as bit flags in *flags.
- *   KV_FEATURE_TENSOR_MAPS  fp16 pool with head_dim 128: every layer has 128-byte-swizzled
- *                           tensor maps of its K and V pools, and grouped-query decode
- *                           (2, 4 or 8 query heads per KV head) runs its scores and P V on
- *                           the tensor cores.  Without it the same calls run on the CUDA
- *                           cores with identical semantics.  (FP8 pools with head_dim 128
- *                           need no tensor maps: their grouped-query decode dequantises
- *                           each tile to fp16 in shared memory and runs on the tensor
- *                           cores too.) */
+ *   KV_FEATURE_TENSOR_MAPS  fp16 or FP8 pool with head_dim 128: every layer has
+ *                           128-byte-swizzled tensor maps of its K and V pools, and
+ *                           grouped-query decode (2, 4 or 8 query heads per KV head) runs
+ *                           its scores and P V on the tensor cores (FP8: K fragments built
+ *                           from the E4M3 codes, V tiles dequantised to fp16 in shared
+ *                           memory).  Without it the same calls run on the CUDA cores with
+ *                           identical semantics. */
 #define KV_FEATURE_TENSOR_MAPS 1u
 KV_API int kv_pool_features(const kv_pool* pool, unsigned* flags);
 

@@ -32,13 +32,16 @@ void free_pool(kv_pool* p) {
     delete p;
 }
 
-// Tensor maps of an fp16, head_dim 128 pool for the grouped-query tensor-core path:
-// each layer's K and V viewed as [rows][2][64] fp16 (rows = num_blocks*H*B, a row being one
-// token of one head), box {64, 2, min(B, 16)}, 128-byte swizzle.  Leaves p->tmaps null if
-// the driver's encoder is unavailable or refuses (the CUDA-core path then serves).
+// Tensor maps of an fp16 or FP8, head_dim 128 pool for the grouped-query tensor-core path.
+// fp16: each layer's K and V viewed as [rows][2][64] fp16 (rows = num_blocks*H*B, a row
+// being one token of one head), box {64, 2, min(B, 16)}, 128-byte swizzle.  FP8: K and V
+// viewed as [rows][128] bytes, box {128, min(B, 32)}, 128-byte swizzle (one token row is
+// one swizzle line).  Leaves p->tmaps null if the driver's encoder is unavailable or
+// refuses (the CUDA-core path then serves).
 void make_tensor_maps(kv_pool* p) {
     const kv_pool_desc& d = p->desc;
-    if (d.dtype != KV_F16 || d.head_dim != 128) return;
+    const bool fp8 = d.dtype == KV_FP8_E4M3;
+    if (d.head_dim != 128 || (d.dtype != KV_F16 && !fp8)) return;
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -57,16 +60,25 @@ void make_tensor_maps(kv_pool* p) {
     // a token row of one head (128 halves) seen as two 64-half halves: the copied tile of
     // up to 16 rows lands half-major ([2][rows][64]), so 8 consecutive tokens of one half
     // are 8 consecutive 128-byte lines and their swizzled 16-byte pieces hit distinct banks
-    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(d.num_blocks) * d.num_heads * d.block_size, 2};
+    const cuuint64_t rows = static_cast<cuuint64_t>(d.num_blocks) * d.num_heads * d.block_size;
+    const cuuint64_t dims[3] = {64, rows, 2};
     const cuuint64_t strides[2] = {256, 128};
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(d.block_size < 16 ? d.block_size : 16), 2};
     const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t dims8[2] = {128, rows};
+    const cuuint64_t strides8[1] = {128};
+    const cuuint32_t box8[2] = {128, static_cast<cuuint32_t>(d.block_size < 32 ? d.block_size : 32)};
     for (int l = 0; l < L; ++l) {
         for (int kv = 0; kv < 2; ++kv) {
             void* base = kv == 0 ? p->k_layers[l] : p->v_layers[l];
-            if (encode(&maps[2 * l + kv], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            const CUresult rc =
+                fp8 ? encode(&maps[2 * l + kv], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims8, strides8, box8, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)
+                    : encode(&maps[2 * l + kv], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (rc != CUDA_SUCCESS) {
                 std::free(raw);
                 return;
             }

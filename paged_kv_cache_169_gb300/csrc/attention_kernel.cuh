@@ -164,11 +164,15 @@ struct Cfg {
     // path reads its query rows from global memory once per item and keeps a per-warp fp16
     // scratch (K, then V, of one chunk) instead.
     static constexpr bool SWZ_STAGE = MMA && !FP8;        // stages hold swizzled tensor-map tiles
+    // FP8 tensor-core path: K tiles arrive 128-byte swizzled through the layer's 2-D tensor
+    // map (the mma fragments are built straight from the E4M3 bytes), V tiles by plain
+    // bulk copies (dequantised to the fp16 scratch)
+    static constexpr bool SWZ_K = MMA && FP8;
     static constexpr int Q_STAGE = MMA ? 0 : Q_BYTES;
     static constexpr int QR_BYTES = SWZ_STAGE ? Q_BYTES : 0;
     static constexpr int SCR_BYTES = (MMA && FP8) ? 16 * D * 2 : 0;
     static constexpr int SC_OFF = Q_OFF + Q_STAGE;
-    static constexpr int STAGE = round_up(SC_OFF + SC_BYTES, SWZ_STAGE ? 1024 : 128);
+    static constexpr int STAGE = round_up(SC_OFF + SC_BYTES, (SWZ_STAGE || SWZ_K) ? 1024 : 128);
     static constexpr int NC_AUTO = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
     // more query heads per warp need more registers: fewer consumer warps
 #if defined(KVP_MMA_NC)
@@ -507,7 +511,7 @@ __device__ __forceinline__ void ticket_resolve(const AttnArgs& a, Ticket& tk, in
 // the bytes a separate kv_append would have stored.
 template <typename C>
 __device__ __forceinline__ void patch_row(const char* src, int in_bytes, char* srow, char* grow,
-                                          float scale, int lane) {
+                                          float scale, int lane, int swz = 0) {
     constexpr int DW = C::D / 32;
     const int e0 = lane * DW;
     if constexpr (C::ESZ == 4) {
@@ -542,8 +546,9 @@ __device__ __forceinline__ void patch_row(const char* src, int in_bytes, char* s
         for (int i = 0; i < DW / 2; ++i)
             q[i] = float2_to_e4m3x2(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
         if constexpr (DW == 4) {
+            // swz != 0: the stage row is 128-byte swizzled (16-byte piece c at c ^ swz)
             const uint32_t v = static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 16);
-            *reinterpret_cast<uint32_t*>(srow + e0) = v;
+            *reinterpret_cast<uint32_t*>(srow + ((((e0 >> 4) ^ swz) << 4) | (e0 & 15))) = v;
             *reinterpret_cast<uint32_t*>(grow + e0) = v;
         } else {
             *reinterpret_cast<uint16_t*>(srow + e0) = q[0];
@@ -646,6 +651,14 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                                                     (real ? g : 0) * D * 2);
             #pragma unroll
             for (int k = 0; k < 8; ++k) {
+                // FP8: k-index pairs (2t, 2t+1) and (2t+8, 2t+9) of k-step k stand for dims
+                // 16k+4t.. and 16k+4t+2.. (the order the K fragments are read in; a dot
+                // product is the same in any consistent order of its dims)
+                if constexpr (C::FP8) {
+                    qa[k][0] = real ? qrow[8 * k + 2 * t] : 0u;
+                    qa[k][1] = real ? qrow[8 * k + 2 * t + 1] : 0u;
+                    continue;
+                }
                 qa[k][0] = real ? qrow[8 * k + t] : 0u;
                 qa[k][1] = real ? qrow[8 * k + 4 + t] : 0u;
             }
@@ -655,8 +668,9 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             const int r = mp->patch_row;
             const int64_t sh = static_cast<int64_t>(ms) * a.H + mh;
             const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + mh) * a.B + mp->patch_off;
+            // K rows sit 128-byte swizzled in the stage (16-byte piece c of row r at c ^ (r % 8))
             patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, stg + C::K_OFF + r * C::ROW,
-                         a.kpool + grow * C::ROW, __ldg(a.kscale + mp->patch_id), lane);
+                         a.kpool + grow * C::ROW, __ldg(a.kscale + mp->patch_id), lane, r & 7);
             patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, stg + C::V_OFF + r * C::ROW,
                          a.vpool + grow * C::ROW, __ldg(a.vscale + mp->patch_id), lane);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -683,8 +697,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
         for (int t16 = 0; t16 < CT; t16 += 16) {
           if (t16 >= nt || t16 + 16 <= lo) continue;
           {
-            // FP8: per-block scales of this lane's token rows (t16 + g and t16 + g + 8) and
-            // this step's K rows dequantised into the scratch
+            // FP8: per-block scales of this lane's token rows (t16 + g and t16 + g + 8)
             float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
             if constexpr (C::FP8) {
                 const int rpc = a.B < CT ? a.B : CT;
@@ -693,9 +706,6 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 ks1 = __ldg(a.kscale + id1);
                 vs0 = __ldg(a.vscale + id0);
                 vs1 = __ldg(a.vscale + id1);
-                dequant(stg + C::K_OFF + t16 * C::ROW);
-                __syncwarp();
-                kbase = smem_u32(scr);
             }
             if (!C::FP8 && (nt < CT || lo > 0)) {
                 // rows outside [lo, nt) may hold anything (unused slots): zero their V so
@@ -710,12 +720,28 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             // S^T = K Q^T, the even and odd k-steps in two accumulators (shorter chains)
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
             const int mi = lane >> 3, mr = lane & 7;
+            // FP8: this lane's K rows t16 + g and t16 + g + 8 of the swizzled stage (both
+            // have row % 8 == g)
+            const char* kr0 = stg + C::K_OFF + (t16 + g) * C::ROW;
+            const char* kr1 = kr0 + 8 * C::ROW;
             #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                // A = K: (tok 0-7, dims 16k..) (tok 8-15, 16k..) (tok 0-7, +8..) (tok 8-15, +8..)
-                const int tok = (mi & 1) * 8 + mr, cp = 2 * k + (mi >> 1);
                 uint32_t kf[4];
-                ldsm_x4(kbase + tile_off(tok, cp * 16), kf);
+                if constexpr (C::FP8) {
+                    // A fragment straight from the E4M3 codes: the 4 codes of dims 16k+4t..
+                    // of each row (16-byte piece k sits at k ^ g; no bank conflicts: the 8
+                    // rows of a quarter-warp hit 8 distinct pieces), converted exactly
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kr0 + (((k ^ g) << 4) | (4 * t)));
+                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kr1 + (((k ^ g) << 4) | (4 * t)));
+                    kf[0] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w0 & 0xffffu));
+                    kf[1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w1 & 0xffffu));
+                    kf[2] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w0 >> 16));
+                    kf[3] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w1 >> 16));
+                } else {
+                    // A = K: (tok 0-7, dims 16k..) (tok 8-15, 16k..) (tok 0-7, +8..) (tok 8-15, +8..)
+                    const int tok = (mi & 1) * 8 + mr, cp = 2 * k + (mi >> 1);
+                    ldsm_x4(kbase + tile_off(tok, cp * 16), kf);
+                }
                 if (k & 1) mma_16816(sb, kf[0], kf[1], kf[2], kf[3], qa[k][0], qa[k][1]);
                 else mma_16816(sa, kf[0], kf[1], kf[2], kf[3], qa[k][0], qa[k][1]);
             }
@@ -975,6 +1001,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                                 const int row = static_cast<int>(toff / C::ROW);
                                 tma_load_3d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, 0, fb);
                                 tma_load_3d(dst + C::V_OFF + j * tile, &a.vmap, 0, row, 0, fb);
+                            } else if constexpr (C::SWZ_K) {
+                                // K: rpc rows of 128 codes, 128-byte swizzled; V: plain rows
+                                const int row = static_cast<int>(toff / C::ROW);
+                                tma_load_2d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, fb);
+                                bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
                             } else {
                                 bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
                                 bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);

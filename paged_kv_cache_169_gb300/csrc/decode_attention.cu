@@ -16,7 +16,8 @@ int consumers_for_g(const kv_pool* pool) {
     if constexpr (G > 1) {                         // grouped-query tensor-core configuration
         if (d.dtype == KV_F16 && d.head_dim == 128 && pool->tmaps)
             return consumers_of<Cfg<128, __half, __half, G, true>>();
-        if (d.dtype == KV_FP8_E4M3 && d.head_dim == 128) return consumers_of<Cfg<128, uint8_t, __half, G, true>>();
+        if (d.dtype == KV_FP8_E4M3 && d.head_dim == 128 && pool->tmaps)
+            return consumers_of<Cfg<128, uint8_t, __half, G, true>>();
     }
     if constexpr (G == 1) {                        // fp32 pools have no grouped path
         if (d.dtype == KV_F32) return d.head_dim == 128 ? consumers_of<Cfg<128, float, float>>()

@@ -20,8 +20,12 @@ int launch_g(const kv_pool* pool, const AttnArgs& a, const AttnPlan& plan, unsig
         return launch_typed<Cfg<64, __half, __half, G>>(pool, a, plan, counters, stream);
     }
     if (d.dtype == KV_FP8_E4M3) {
-        // head_dim 128: tensor cores on tiles dequantised to fp16 in shared memory
-        if (d.head_dim == 128) return launch_typed<Cfg<128, uint8_t, __half, G, true>>(pool, a, plan, counters, stream);
+        if (d.head_dim == 128) {
+            // tensor cores when the pool has its swizzled tensor maps (K fragments built
+            // from the E4M3 codes, V dequantised to fp16 in shared memory), else CUDA cores
+            if (pool->tmaps) return launch_typed<Cfg<128, uint8_t, __half, G, true>>(pool, a, plan, counters, stream);
+            return launch_typed<Cfg<128, uint8_t, __half, G>>(pool, a, plan, counters, stream);
+        }
         return launch_typed<Cfg<64, uint8_t, __half, G>>(pool, a, plan, counters, stream);
     }
     return KV_ERR_UNSUPPORTED;

@@ -50,7 +50,7 @@ def test_gqa_against_oracle(G, dtype, d, B):
     lens = [0, 1, 15, 16, 17, 100, 513, 1400, 2200]
     w, cache, alloc, seqs, ks, vs = _setup(G, 2, d, B, dtype, 80 + G, lens)
     # fp16 pools of head_dim 128 take the tensor-core path (tensor-map tiles)
-    want_tc = abi.KV_FEATURE_TENSOR_MAPS if (dtype == "f16" and d == 128) else 0
+    want_tc = abi.KV_FEATURE_TENSOR_MAPS if (dtype in ("f16", "fp8") and d == 128) else 0
     assert abi.kv_pool_features(cache.handle) == want_tc
     prefill(cache, alloc, seqs, ks, vs)
     bt, cl, _ = tables_for(alloc, seqs, max(-(-n // B) for n in lens))
