@@ -3,8 +3,11 @@ sampled (layer, sequence, head) outputs that the float64 oracle computes one by 
 
 Pools are filled with seeded N(0,1) values by torch's device generator (inputs, not
 kernel output); the oracle reads the sampled tiles back before the decode append and
-adds the new token itself.  Every layer's decode step is one kv_append of the new
-tokens followed by paged_decode_attention with the library-chosen partitioning.
+adds the new token itself.  The benchmark's call: one paged_decode_attention_ex per
+layer that appends each sequence's new token and attends, library-chosen partitioning,
+a workspace zero-filled once and kept over all calls (KV_DECODE_WORKSPACE_ZEROED) and
+programmatic dependent launch (KV_DECODE_PDL).  The 13B step also runs as kv_append
+followed by paged_decode_attention.
 """
 
 import numpy as np
@@ -15,9 +18,12 @@ import workloads as W
 from gpu_setup import max_abs, tol_for
 from oracle import attention as OA
 from oracle import fp8 as OF
+from paged_kv_cache_169_gb300 import abi
 from paged_kv_cache_169_gb300.cache import PagedKVCache
 
 pytestmark = pytest.mark.gpu
+
+BENCH_FLAGS = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL
 
 
 def _snapshot(pool: torch.Tensor, table_row, n_blocks: int, h: int) -> np.ndarray:
@@ -27,7 +33,8 @@ def _snapshot(pool: torch.Tensor, table_row, n_blocks: int, h: int) -> np.ndarra
     return t.reshape(-1, t.shape[-1]).cpu().numpy()
 
 
-def test_llama13b_full_step_sampled():
+@pytest.mark.parametrize("path", ["fused_flags", "unfused"])
+def test_llama13b_full_step_sampled(path):
     w = W.llama13b()
     B, H, d = w.block_size, w.num_heads, w.head_dim
     cache = PagedKVCache(w.num_layers, w.num_blocks, B, H, d, "f16")
@@ -47,13 +54,19 @@ def test_llama13b_full_step_sampled():
     for (l, s, h) in samples:
         snap[(l, s, h)] = (_snapshot(cache.k[l], tables[s], nbs[s], h), _snapshot(cache.v[l], tables[s], nbs[s], h))
     outs = {}
-    ws = cache.workspace(w.batch, max(w.lens))
+    fused = path == "fused_flags"
+    ws = cache.zeroed_workspace(w.batch, max(w.lens)) if fused else cache.workspace(w.batch, max(w.lens))
     for l in range(w.num_layers):
         k_new = W.host_step_tokens(w, 0, l, "k")
         v_new = W.host_step_tokens(w, 0, l, "v")
         q = W.host_queries(w, 0, l)
-        cache.append(l, torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda(), slots)
-        out = cache.attention(l, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale, workspace=ws)
+        if fused:
+            out = cache.attention_ex(l, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale,
+                                     k_new=torch.from_numpy(k_new).cuda(), v_new=torch.from_numpy(v_new).cuda(),
+                                     workspace=ws, flags=BENCH_FLAGS)
+        else:
+            cache.append(l, torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda(), slots)
+            out = cache.attention(l, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale, workspace=ws)
         if any(x[0] == l for x in samples):
             outs[l] = (out.cpu().numpy(), q, k_new, v_new)
     worst = 0.0
@@ -112,8 +125,11 @@ def test_ragged_full_size_sampled(B, dtype):
     k_new = W.host_step_tokens(w, 0, 0, "k")
     v_new = W.host_step_tokens(w, 0, 0, "v")
     q = W.host_queries(w)
-    cache.append(0, torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda(), slots)
-    out = cache.attention(0, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale).cpu().numpy()
+    assert slots.numel() == w.batch                     # the slots the fused call writes
+    ws = cache.zeroed_workspace(w.batch, max(w.lens))
+    out = cache.attention_ex(0, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale,
+                             k_new=torch.from_numpy(k_new).cuda(), v_new=torch.from_numpy(v_new).cuda(),
+                             workspace=ws, flags=BENCH_FLAGS).cpu().numpy()
     worst = 0.0
     for (s, h) in samples:
         n = w.lens[s]

@@ -145,8 +145,12 @@ def test_gqa70b_full_size_layer_sampled():
                              for p in (cache.k[l], cache.v[l]))
     q = W.host_queries(w, 0, l)
     k_new, v_new = W.host_step_tokens(w, 0, l, "k"), W.host_step_tokens(w, 0, l, "v")
-    out = cache.attention_gqa(l, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale,
-                              k_new=torch.from_numpy(k_new).cuda(), v_new=torch.from_numpy(v_new).cuda())
+    # the benchmark's call: every option in one argument block, a workspace zero-filled
+    # once, programmatic dependent launch
+    ws = cache.zeroed_workspace(w.batch, max(w.lens), num_q_heads=Hq)
+    out = cache.attention_ex(l, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale,
+                             k_new=torch.from_numpy(k_new).cuda(), v_new=torch.from_numpy(v_new).cuda(),
+                             workspace=ws, flags=abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL)
     out = out.cpu().numpy()
     worst = 0.0
     for (s, j) in samples:
