@@ -245,6 +245,14 @@ def job_throughput(world: int, bytes_per_step_per_rank: int, steps: int, elapsed
 
 
 # ----------------------------------------------------------------------------- reference arm
+def workload_config(w, args) -> dict:
+    """The workload keys of a bench line's config (shared by both arms)."""
+    return {"workload": args.workload, "layers": w.num_layers, "batch": w.batch, "heads": w.num_heads,
+            "q_heads": w.q_heads, "head_dim": w.head_dim, "block_size": w.block_size, "kv_dtype": w.kv,
+            "context_mean": sum(w.lens) / len(w.lens), "context_max": max(w.lens),
+            "window": args.window or None}
+
+
 def run_reference(args):
     world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
     if rank != 0:
@@ -262,7 +270,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload, "sample_units_per_step": per_step_units},
+        "data": "synthetic", "config": workload_config(apply_overrides(w, args), args) | {
+            "sample_units_per_step": per_step_units,
+            "sample": "each step times the oracle on this many (sequence, head) units of the workload"},
         "cpu_baseline": {k: vals[-1][k] for k in ("kind", "cores", "sample")} | {"value": value, "unit": "GB/s"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -450,14 +460,11 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32-accum/" + w.kv, "data": "synthetic",
-        "config": {"workload": args.workload, "layers": L, "batch": w.batch, "heads": H, "q_heads": Hq,
-                   "head_dim": d,
-                   "block_size": BS, "kv_dtype": w.kv, "context_mean": sum(w.lens) / len(w.lens),
-                   "context_max": max_ctx, "pool_gib": round(2 * L * w.num_blocks * H * BS * d *
-                                                             (1 if w.kv == "fp8" else 2) / 2 ** 30, 2),
+        "config": workload_config(w, args) | {
+                   "pool_gib": round(2 * L * w.num_blocks * H * BS * d * (1 if w.kv == "fp8" else 2) / 2 ** 30, 2),
                    "l2": "no flush: inputs (the KV pool) larger than L2",
                    "partition_tokens": args.partition or "auto", "parallelism": f"replica x{world}",
-                   "window": args.window or None, "launch_flags": args.launch_flags,
+                   "launch_flags": args.launch_flags,
                    "step": "kv_append + paged_decode_attention" if args.unfused
                            else "paged_decode_attention_append (fused)"},
         "pct_of_peak": 100.0 * value / world / peak,

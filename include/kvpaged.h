@@ -293,9 +293,13 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *     KV_DECODE_WORKSPACE_ZEROED  the workspace's counters are already zero, so the call
  *                does not clear them (one cudaMemsetAsync less per call).  True for a
  *                workspace zero-filled once after allocation and used since only by decode
- *                calls of this library that left no device error bit: every launch leaves
- *                its counters zero when it completes.  After a device error, zero-fill the
- *                workspace again before passing this flag.
+ *                calls of this library of one shape (the same layer pool geometry, batch,
+ *                num_q_heads, max_context, partition_tokens and window; context_lens,
+ *                tables, q and the layer may change) that left no device error bit: every
+ *                launch leaves its counters zero when it completes.  A call of another
+ *                shape places its counters elsewhere in the workspace, possibly where the
+ *                previous shape kept its partials: zero-fill the workspace again before
+ *                such a call, and after a device error, before passing this flag.
  *     KV_DECODE_PDL  launch with programmatic dependent launch: the kernel may be scheduled
  *                while the previous kernel on the stream is still finishing; it reads no
  *                global memory (inputs, pool or workspace) before that kernel has completed

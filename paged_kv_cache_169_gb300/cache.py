@@ -211,7 +211,8 @@ class PagedKVCache:
 
     def zeroed_workspace(self, batch: int, max_context: int, partition_tokens: int = 0,
                          num_q_heads: int = 0, window: int = 0) -> torch.Tensor:
-        """A new zero-filled workspace for attention_ex(..., flags=KV_DECODE_WORKSPACE_ZEROED)."""
+        """A new zero-filled workspace for attention_ex(..., flags=KV_DECODE_WORKSPACE_ZEROED),
+        valid for calls of this one shape (batch, query heads, max_context, partition, window)."""
         a = abi.kv_decode_args()
         a.num_q_heads, a.batch, a.max_context = num_q_heads, batch, max_context
         a.window, a.partition_tokens = window, partition_tokens
