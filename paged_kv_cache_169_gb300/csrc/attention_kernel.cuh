@@ -164,13 +164,12 @@ struct Cfg {
     // path reads its query rows from global memory once per item and keeps a per-warp fp16
     // scratch (K, then V, of one chunk) instead.
     static constexpr bool SWZ_STAGE = MMA && !FP8;        // stages hold swizzled tensor-map tiles
-    // FP8 tensor-core path: K tiles arrive 128-byte swizzled through the layer's 2-D tensor
-    // map (the mma fragments are built straight from the E4M3 bytes), V tiles by plain
-    // bulk copies (dequantised to the fp16 scratch)
+    // FP8 tensor-core path: K and V tiles arrive 128-byte swizzled through the layer's 2-D
+    // tensor maps, and the mma fragments are built straight from the E4M3 codes
     static constexpr bool SWZ_K = MMA && FP8;
     static constexpr int Q_STAGE = MMA ? 0 : Q_BYTES;
     static constexpr int QR_BYTES = SWZ_STAGE ? Q_BYTES : 0;
-    static constexpr int SCR_BYTES = (MMA && FP8) ? 16 * D * 2 : 0;
+    static constexpr int SCR_BYTES = 0;
     static constexpr int SC_OFF = Q_OFF + Q_STAGE;
     static constexpr int STAGE = round_up(SC_OFF + SC_BYTES, (SWZ_STAGE || SWZ_K) ? 1024 : 128);
     static constexpr int NC_AUTO = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
@@ -585,33 +584,14 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     // is padding.  Lane (g, t): token rows g and g+8, query columns 2t and 2t+1.
     const int g = lane >> 2, t = lane & 3;
     // byte x (0..255) of fp16 token row tok in a chunk: copies of rpc rows (8 or 16), each
-    // laid out half-major [2][rpc][64 halves], 128-byte swizzled.  fp16 stages are laid out
-    // by the tensor-map copies (rpc = min(B, 16)); the FP8 path's dequantised scratch is
-    // one 16-row copy.
-    const int rs = (C::FP8 || (a.B < CT ? a.B : CT) == 16) ? 4 : 3;
+    // laid out half-major [2][rpc][64 halves], 128-byte swizzled by the tensor-map copies
+    // (rpc = min(B, 16)).  FP8 stages hold plain [rows][128 codes], also 128-byte swizzled:
+    // 16-byte piece c of row r sits at piece c ^ (r % 8).
+    const int rs = (a.B < CT ? a.B : CT) == 16 ? 4 : 3;
     auto tile_off = [rs](int tok, int x) -> uint32_t {
         const int rpc = 1 << rs;
         return swz128(static_cast<uint32_t>(((tok >> rs) << (rs + 8)) + ((((x >> 7) << rs) + (tok & (rpc - 1))) << 7) +
                                             (x & 127)));
-    };
-    char* scr = smem + C::SCR_OFF + w * C::SCR_BYTES;      // FP8 only: fp16 K, then V, of a chunk
-    // FP8: the 16 rows x 128 codes at src become fp16 rows of the scratch (exact: every
-    // E4M3 value is an fp16 value); the block scales are applied to S and P instead
-    // Lane tasks: 16 rows x 16 pieces of 8 codes.  A half-warp reads one 128-byte row and
-    // each quarter-warp writes 8 distinct 16-byte chunks of one 128-byte scratch line, so
-    // neither the loads nor the stores conflict on banks.
-    auto dequant = [&](const char* src) {
-        #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int task = lane + 32 * i;
-            const int r = task >> 4, c = (task & 15) * 8;
-            const uint2 v = *reinterpret_cast<const uint2*>(src + r * 128 + c);
-            const uint32_t h0 = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.x & 0xffffu));
-            const uint32_t h1 = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.x >> 16));
-            const uint32_t h2 = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.y & 0xffffu));
-            const uint32_t h3 = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.y >> 16));
-            *reinterpret_cast<uint4*>(scr + tile_off(r, 2 * c)) = make_uint4(h0, h1, h2, h3);
-        }
     };
     uint32_t qa[8][2];                 // B fragments of Q^T: query g, dims 16k+2t.. and 16k+8+2t..
     float ot[8][4];                    // O^T tile i: dims 16i+g / 16i+g+8, queries 2t / 2t+1
@@ -668,11 +648,11 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             const int r = mp->patch_row;
             const int64_t sh = static_cast<int64_t>(ms) * a.H + mh;
             const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + mh) * a.B + mp->patch_off;
-            // K rows sit 128-byte swizzled in the stage (16-byte piece c of row r at c ^ (r % 8))
+            // K and V rows sit 128-byte swizzled in the stage (16-byte piece c of row r at c ^ (r % 8))
             patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, stg + C::K_OFF + r * C::ROW,
                          a.kpool + grow * C::ROW, __ldg(a.kscale + mp->patch_id), lane, r & 7);
             patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, stg + C::V_OFF + r * C::ROW,
-                         a.vpool + grow * C::ROW, __ldg(a.vscale + mp->patch_id), lane);
+                         a.vpool + grow * C::ROW, __ldg(a.vscale + mp->patch_id), lane, r & 7);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
         } else if (flags & F_PATCH) {
@@ -771,30 +751,49 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             // pair of, transposed in registers (V scales folded in; 1 for fp16 pools)
             const uint32_t pb0 = movmatrix_t(pack_half2(p0 * vs0, p1 * vs0));
             const uint32_t pb1 = movmatrix_t(pack_half2(p2 * vs1, p3 * vs1));
-            if constexpr (C::FP8) {
-                // V into the scratch once every lane is done reading K from it; rows outside
-                // [lo, nt) are zeroed so that their p = 0 contributes exactly nothing
-                __syncwarp();
-                dequant(stg + C::V_OFF + t16 * C::ROW);
-                if (t16 + 16 > nt || t16 < lo) {
-                    #pragma unroll 1
-                    for (int r = 0; r < 16; ++r)
-                        if ((t16 + r < lo || t16 + r >= nt) && lane < 16)
-                            *reinterpret_cast<uint4*>(scr + tile_off(r, lane * 16)) = make_uint4(0, 0, 0, 0);
-                }
-                __syncwarp();
-                vbase = smem_u32(scr);
-            }
             // O^T += V^T P^T, one 16-dim tile per mma
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                // A = V^T: (dims 16i.., tok 0-7) (dims 16i+8.., tok 0-7) (16i.., tok 8-15) (16i+8.., tok 8-15)
-                const int tok = (mi >> 1) * 8 + mr, cp = 2 * i + (mi & 1);
-                uint32_t vf[4];
-                ldsm_x4_t(vbase + tile_off(tok, cp * 16), vf);
-                mma_16816(ot[i], vf[0], vf[1], vf[2], vf[3], pb0, pb1);
+            if constexpr (C::FP8) {
+                // A = V^T straight from the E4M3 codes.  Output tile 2p+e: row g stands for
+                // dim 32p+4g+2e and row g+8 for dim 32p+4g+2e+1 (the rows are written back in
+                // that order); its k pairs are the tokens (2t, 2t+1) and (2t+8, 2t+9).  A lane
+                // reads codes 32p+4g..+3 of those 4 token rows (piece 2p + g/4 of each row,
+                // swizzled: no bank conflicts) and pairs equal dims of two tokens by byte
+                // permutes.  Rows outside [lo, nt) read as zero (their p is 0; their slots
+                // may hold anything).
+                const bool masked = t16 + 16 > nt || t16 < lo;
+                const char* vst = stg + C::V_OFF;
+                const int r0 = t16 + 2 * t;
+                #pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int piece = 2 * p + (g >> 2), sub = 4 * (g & 3);
+                    uint32_t wv[4];               // token rows r0, r0+1, r0+8, r0+9
+                    #pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int r = r0 + (u & 1) + 8 * (u >> 1);
+                        wv[u] = *reinterpret_cast<const uint32_t*>(vst + r * C::ROW + (((piece ^ (r & 7)) << 4) | sub));
+                        if (masked && (r < lo || r >= nt)) wv[u] = 0u;
+                    }
+                    const uint32_t d01 = __byte_perm(wv[0], wv[1], 0x5140), e01 = __byte_perm(wv[0], wv[1], 0x7362);
+                    const uint32_t d89 = __byte_perm(wv[2], wv[3], 0x5140), e89 = __byte_perm(wv[2], wv[3], 0x7362);
+                    mma_16816(ot[2 * p], e4m3x2_to_half2_bits(static_cast<uint16_t>(d01 & 0xffffu)),
+                              e4m3x2_to_half2_bits(static_cast<uint16_t>(d01 >> 16)),
+                              e4m3x2_to_half2_bits(static_cast<uint16_t>(d89 & 0xffffu)),
+                              e4m3x2_to_half2_bits(static_cast<uint16_t>(d89 >> 16)), pb0, pb1);
+                    mma_16816(ot[2 * p + 1], e4m3x2_to_half2_bits(static_cast<uint16_t>(e01 & 0xffffu)),
+                              e4m3x2_to_half2_bits(static_cast<uint16_t>(e01 >> 16)),
+                              e4m3x2_to_half2_bits(static_cast<uint16_t>(e89 & 0xffffu)),
+                              e4m3x2_to_half2_bits(static_cast<uint16_t>(e89 >> 16)), pb0, pb1);
+                }
+            } else {
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    // A = V^T: (dims 16i.., tok 0-7) (dims 16i+8.., tok 0-7) (16i.., tok 8-15) (16i+8.., tok 8-15)
+                    const int tok = (mi >> 1) * 8 + mr, cp = 2 * i + (mi & 1);
+                    uint32_t vf[4];
+                    ldsm_x4_t(vbase + tile_off(tok, cp * 16), vf);
+                    mma_16816(ot[i], vf[0], vf[1], vf[2], vf[3], pb0, pb1);
+                }
             }
-            if constexpr (C::FP8) __syncwarp();       // the next step rewrites the scratch
           }
         }
         __syncwarp();
@@ -813,25 +812,31 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 const int q = 2 * t + h2;
                 if (q >= G) continue;
                 const int64_t sq = shk * G + q;
+                float inv = 1.f;
+                float* dst;
                 if (flags & F_SINGLE) {
-                    const float inv = nt > 0 ? 1.f / (h2 ? lb : la) : 0.f;
-                    float* dst = a.out + sq * D + g;
-                    #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        dst[16 * i] = ot[i][h2] * inv;
-                        dst[16 * i + 8] = ot[i][2 + h2] * inv;
-                    }
+                    inv = nt > 0 ? 1.f / (h2 ? lb : la) : 0.f;
+                    dst = a.out + sq * D;
                 } else {
                     const int64_t idx = sq * a.max_parts + mpart;
                     if (g == 0) {
                         a.part_ml[2 * idx] = m2[h2];
                         a.part_ml[2 * idx + 1] = h2 ? lb : la;
                     }
-                    float* dst = a.part_o + idx * D + g;
+                    dst = a.part_o + idx * D;
+                }
+                if constexpr (C::FP8) {
+                    // tiles 2p, 2p+1 rows g, g+8: dims 32p+4g .. 32p+4g+3
+                    #pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        *reinterpret_cast<float4*>(dst + 32 * p + 4 * g) =
+                            make_float4(ot[2 * p][h2] * inv, ot[2 * p][2 + h2] * inv, ot[2 * p + 1][h2] * inv,
+                                        ot[2 * p + 1][2 + h2] * inv);
+                } else {
                     #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        dst[16 * i] = ot[i][h2];
-                        dst[16 * i + 8] = ot[i][2 + h2];
+                        dst[16 * i + g] = ot[i][h2] * inv;
+                        dst[16 * i + 8 + g] = ot[i][2 + h2] * inv;
                     }
                 }
             }
@@ -1002,10 +1007,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                                 tma_load_3d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, 0, fb);
                                 tma_load_3d(dst + C::V_OFF + j * tile, &a.vmap, 0, row, 0, fb);
                             } else if constexpr (C::SWZ_K) {
-                                // K: rpc rows of 128 codes, 128-byte swizzled; V: plain rows
+                                // rpc rows of 128 codes each, 128-byte swizzled
                                 const int row = static_cast<int>(toff / C::ROW);
                                 tma_load_2d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, fb);
-                                bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
+                                tma_load_2d(dst + C::V_OFF + j * tile, &a.vmap, 0, row, fb);
                             } else {
                                 bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
                                 bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
