@@ -671,67 +671,87 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
         }
-        // 16 tokens per step (a 32-token FP8 chunk takes two); a step with no token in
-        // [lo, nt) is skipped whole
-        #pragma unroll 1
-        for (int t16 = 0; t16 < CT; t16 += 16) {
-          if (t16 >= nt || t16 + 16 <= lo) continue;
-          {
-            // FP8: per-block scales of this lane's token rows (t16 + g and t16 + g + 8)
-            float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
-            if constexpr (C::FP8) {
-                const int rpc = a.B < CT ? a.B : CT;
-                const int id0 = mp->ids[t16 / rpc], id1 = mp->ids[(t16 + 8) / rpc];
-                ks0 = __ldg(a.kscale + id0);
-                ks1 = __ldg(a.kscale + id1);
-                vs0 = __ldg(a.vscale + id0);
-                vs1 = __ldg(a.vscale + id1);
-            }
-            if (!C::FP8 && (nt < CT || lo > 0)) {
-                // rows outside [lo, nt) may hold anything (unused slots): zero their V so
-                // that p = 0 rows contribute exactly nothing to P V
-                #pragma unroll 1
-                for (int r = 0; r < CT; ++r)
-                    if ((r < lo || r >= nt) && lane < 16)
-                        *reinterpret_cast<uint4*>(stg + C::V_OFF + tile_off(r, lane * 16)) = make_uint4(0, 0, 0, 0);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-            }
-            // S^T = K Q^T, the even and odd k-steps in two accumulators (shorter chains)
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        // 16-token steps (a 32-token FP8 chunk has two): every step's S mma first, one
+        // softmax update over the whole chunk, then every step's P V mma.  A step with no
+        // token in [lo, nt) is skipped.
+        constexpr int NS = CT / 16;
+        bool act[NS];
+        bool any = false;
+        #pragma unroll
+        for (int u = 0; u < NS; ++u) {
+            act[u] = 16 * u < nt && 16 * u + 16 > lo;
+            any = any || act[u];
+        }
+        if (!C::FP8 && any && (nt < CT || lo > 0)) {
+            // rows outside [lo, nt) may hold anything (unused slots): zero their V so
+            // that p = 0 rows contribute exactly nothing to P V
+            #pragma unroll 1
+            for (int r = 0; r < CT; ++r)
+                if ((r < lo || r >= nt) && lane < 16)
+                    *reinterpret_cast<uint4*>(stg + C::V_OFF + tile_off(r, lane * 16)) = make_uint4(0, 0, 0, 0);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+        }
+        if (any) {
             const int mi = lane >> 3, mr = lane & 7;
-            // FP8: this lane's K rows t16 + g and t16 + g + 8 of the swizzled stage (both
-            // have row % 8 == g)
-            const char* kr0 = stg + C::K_OFF + (t16 + g) * C::ROW;
-            const char* kr1 = kr0 + 8 * C::ROW;
+            float x[NS][4];
+            float vsc[NS][2];                  // V scales of this lane's rows (FP8; else 1)
             #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                uint32_t kf[4];
+            for (int u = 0; u < NS; ++u) {
+                const int t16 = 16 * u;
+                x[u][0] = x[u][1] = x[u][2] = x[u][3] = -CUDART_INF_F;
+                vsc[u][0] = vsc[u][1] = 1.f;
+                if (!act[u]) continue;
+                // FP8: per-block scales of this lane's token rows (t16 + g and t16 + g + 8)
+                float ks0 = 1.f, ks1 = 1.f;
                 if constexpr (C::FP8) {
-                    // A fragment straight from the E4M3 codes: the 4 codes of dims 16k+4t..
-                    // of each row (16-byte piece k sits at k ^ g; no bank conflicts: the 8
-                    // rows of a quarter-warp hit 8 distinct pieces), converted exactly
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kr0 + (((k ^ g) << 4) | (4 * t)));
-                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kr1 + (((k ^ g) << 4) | (4 * t)));
-                    kf[0] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w0 & 0xffffu));
-                    kf[1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w1 & 0xffffu));
-                    kf[2] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w0 >> 16));
-                    kf[3] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w1 >> 16));
-                } else {
-                    // A = K: (tok 0-7, dims 16k..) (tok 8-15, 16k..) (tok 0-7, +8..) (tok 8-15, +8..)
-                    const int tok = (mi & 1) * 8 + mr, cp = 2 * k + (mi >> 1);
-                    ldsm_x4(kbase + tile_off(tok, cp * 16), kf);
+                    const int rpc = a.B < CT ? a.B : CT;
+                    const int id0 = mp->ids[t16 / rpc], id1 = mp->ids[(t16 + 8) / rpc];
+                    ks0 = __ldg(a.kscale + id0);
+                    ks1 = __ldg(a.kscale + id1);
+                    vsc[u][0] = __ldg(a.vscale + id0);
+                    vsc[u][1] = __ldg(a.vscale + id1);
                 }
-                if (k & 1) mma_16816(sb, kf[0], kf[1], kf[2], kf[3], qa[k][0], qa[k][1]);
-                else mma_16816(sa, kf[0], kf[1], kf[2], kf[3], qa[k][0], qa[k][1]);
+                // S^T = K Q^T, the even and odd k-steps in two accumulators (shorter chains)
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                // FP8: this lane's K rows t16 + g and t16 + g + 8 of the swizzled stage
+                // (both have row % 8 == g)
+                const char* kr0 = stg + C::K_OFF + (t16 + g) * C::ROW;
+                const char* kr1 = kr0 + 8 * C::ROW;
+                #pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint32_t kf[4];
+                    if constexpr (C::FP8) {
+                        // A fragment straight from the E4M3 codes: the 4 codes of dims
+                        // 16k+4t.. of each row (16-byte piece k sits at k ^ g; no bank
+                        // conflicts: the 8 rows of a quarter-warp hit 8 distinct pieces)
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kr0 + (((k ^ g) << 4) | (4 * t)));
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kr1 + (((k ^ g) << 4) | (4 * t)));
+                        kf[0] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w0 & 0xffffu));
+                        kf[1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w1 & 0xffffu));
+                        kf[2] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w0 >> 16));
+                        kf[3] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w1 >> 16));
+                    } else {
+                        // A = K: (tok 0-7, dims 16k..) (tok 8-15, 16k..) (tok 0-7, +8..) (tok 8-15, +8..)
+                        const int tok = t16 + (mi & 1) * 8 + mr, cp = 2 * k + (mi >> 1);
+                        ldsm_x4(kbase + tile_off(tok, cp * 16), kf);
+                    }
+                    if (k & 1) mma_16816(sb, kf[0], kf[1], kf[2], kf[3], qa[k][0], qa[k][1]);
+                    else mma_16816(sa, kf[0], kf[1], kf[2], kf[3], qa[k][0], qa[k][1]);
+                }
+                // log2-domain scores of tokens g (x0: query 2t, x1: 2t+1) and g+8 (x2, x3)
+                const float qk0 = a.qscale * ks0, qk1 = a.qscale * ks1;   // K scales; 1 for fp16 pools
+                const bool v0 = t16 + g >= lo && t16 + g < nt, v1 = t16 + g + 8 >= lo && t16 + g + 8 < nt;
+                if (v0) { x[u][0] = (sa[0] + sb[0]) * qk0; x[u][1] = (sa[1] + sb[1]) * qk0; }
+                if (v1) { x[u][2] = (sa[2] + sb[2]) * qk1; x[u][3] = (sa[3] + sb[3]) * qk1; }
             }
-            // log2-domain scores of tokens g (x0: query 2t, x1: 2t+1) and g+8 (x2, x3)
-            const float qk0 = a.qscale * ks0, qk1 = a.qscale * ks1;   // K scales; 1 for fp16 pools
-            const bool v0 = t16 + g >= lo && t16 + g < nt, v1 = t16 + g + 8 >= lo && t16 + g + 8 < nt;
-            float x[4] = {v0 ? (sa[0] + sb[0]) * qk0 : -CUDART_INF_F, v0 ? (sa[1] + sb[1]) * qk0 : -CUDART_INF_F,
-                          v1 ? (sa[2] + sb[2]) * qk1 : -CUDART_INF_F, v1 ? (sa[3] + sb[3]) * qk1 : -CUDART_INF_F};
-            // column maxima over the 16 tokens: the 8 lanes of equal t hold them
-            float mxa = fmaxf(x[0], x[2]), mxb = fmaxf(x[1], x[3]);
+            // column maxima over the chunk's tokens: the 8 lanes of equal t hold them
+            float mxa = -CUDART_INF_F, mxb = -CUDART_INF_F;
+            #pragma unroll
+            for (int u = 0; u < NS; ++u) {
+                mxa = fmaxf(mxa, fmaxf(x[u][0], x[u][2]));
+                mxb = fmaxf(mxb, fmaxf(x[u][1], x[u][3]));
+            }
             #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 mxa = fmaxf(mxa, __shfl_xor_sync(FULL, mxa, off));
@@ -739,62 +759,69 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             }
             const float ma = fmaxf(m2[0], mxa), mb = fmaxf(m2[1], mxb);
             const float ca = ex2_approx(m2[0] - ma), cb = ex2_approx(m2[1] - mb);
-            const float p0 = ex2_approx(x[0] - ma), p1 = ex2_approx(x[1] - mb);
-            const float p2 = ex2_approx(x[2] - ma), p3 = ex2_approx(x[3] - mb);
-            l2[0] = fmaf(l2[0], ca, p0 + p2);        // this lane's tokens only; summed at the end
-            l2[1] = fmaf(l2[1], cb, p1 + p3);
+            l2[0] *= ca;
+            l2[1] *= cb;
             m2[0] = ma;
             m2[1] = mb;
             #pragma unroll
             for (int i = 0; i < 8; ++i) { ot[i][0] *= ca; ot[i][2] *= ca; ot[i][1] *= cb; ot[i][3] *= cb; }
-            // P^T as the B operand: the 8x8 blocks (tokens x queries) this lane holds a row
-            // pair of, transposed in registers (V scales folded in; 1 for fp16 pools)
-            const uint32_t pb0 = movmatrix_t(pack_half2(p0 * vs0, p1 * vs0));
-            const uint32_t pb1 = movmatrix_t(pack_half2(p2 * vs1, p3 * vs1));
-            // O^T += V^T P^T, one 16-dim tile per mma
-            if constexpr (C::FP8) {
-                // A = V^T straight from the E4M3 codes.  Output tile 2p+e: row g stands for
-                // dim 32p+4g+2e and row g+8 for dim 32p+4g+2e+1 (the rows are written back in
-                // that order); its k pairs are the tokens (2t, 2t+1) and (2t+8, 2t+9).  A lane
-                // reads codes 32p+4g..+3 of those 4 token rows (piece 2p + g/4 of each row,
-                // swizzled: no bank conflicts) and pairs equal dims of two tokens by byte
-                // permutes.  Rows outside [lo, nt) read as zero (their p is 0; their slots
-                // may hold anything).
-                const bool masked = t16 + 16 > nt || t16 < lo;
-                const char* vst = stg + C::V_OFF;
-                const int r0 = t16 + 2 * t;
-                #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const int piece = 2 * p + (g >> 2), sub = 4 * (g & 3);
-                    uint32_t wv[4];               // token rows r0, r0+1, r0+8, r0+9
+            #pragma unroll
+            for (int u = 0; u < NS; ++u) {
+                if (!act[u]) continue;
+                const int t16 = 16 * u;
+                const float p0 = ex2_approx(x[u][0] - ma), p1 = ex2_approx(x[u][1] - mb);
+                const float p2 = ex2_approx(x[u][2] - ma), p3 = ex2_approx(x[u][3] - mb);
+                l2[0] += p0 + p2;                    // this lane's tokens only; summed at the end
+                l2[1] += p1 + p3;
+                // P^T as the B operand: the 8x8 blocks (tokens x queries) this lane holds a
+                // row pair of, transposed in registers (V scales folded in; 1 for fp16 pools)
+                const uint32_t pb0 = movmatrix_t(pack_half2(p0 * vsc[u][0], p1 * vsc[u][0]));
+                const uint32_t pb1 = movmatrix_t(pack_half2(p2 * vsc[u][1], p3 * vsc[u][1]));
+                // O^T += V^T P^T, one 16-dim tile per mma
+                if constexpr (C::FP8) {
+                    // A = V^T straight from the E4M3 codes.  Output tile 2p+e: row g stands
+                    // for dim 32p+4g+2e and row g+8 for dim 32p+4g+2e+1 (the rows are written
+                    // back in that order); its k pairs are the tokens (2t, 2t+1) and (2t+8,
+                    // 2t+9).  A lane reads codes 32p+4g..+3 of those 4 token rows (piece
+                    // 2p + g/4 of each row, swizzled: no bank conflicts) and pairs equal
+                    // dims of two tokens by byte permutes.  Rows outside [lo, nt) read as
+                    // zero (their p is 0; their slots may hold anything).
+                    const bool masked = t16 + 16 > nt || t16 < lo;
+                    const char* vst = stg + C::V_OFF;
+                    const int r0 = t16 + 2 * t;
                     #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int r = r0 + (u & 1) + 8 * (u >> 1);
-                        wv[u] = *reinterpret_cast<const uint32_t*>(vst + r * C::ROW + (((piece ^ (r & 7)) << 4) | sub));
-                        if (masked && (r < lo || r >= nt)) wv[u] = 0u;
+                    for (int p = 0; p < 4; ++p) {
+                        const int piece = 2 * p + (g >> 2), sub = 4 * (g & 3);
+                        uint32_t wv[4];               // token rows r0, r0+1, r0+8, r0+9
+                        #pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int r = r0 + (v & 1) + 8 * (v >> 1);
+                            wv[v] = *reinterpret_cast<const uint32_t*>(vst + r * C::ROW +
+                                                                       (((piece ^ (r & 7)) << 4) | sub));
+                            if (masked && (r < lo || r >= nt)) wv[v] = 0u;
+                        }
+                        const uint32_t d01 = __byte_perm(wv[0], wv[1], 0x5140), e01 = __byte_perm(wv[0], wv[1], 0x7362);
+                        const uint32_t d89 = __byte_perm(wv[2], wv[3], 0x5140), e89 = __byte_perm(wv[2], wv[3], 0x7362);
+                        mma_16816(ot[2 * p], e4m3x2_to_half2_bits(static_cast<uint16_t>(d01 & 0xffffu)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(d01 >> 16)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(d89 & 0xffffu)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(d89 >> 16)), pb0, pb1);
+                        mma_16816(ot[2 * p + 1], e4m3x2_to_half2_bits(static_cast<uint16_t>(e01 & 0xffffu)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(e01 >> 16)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(e89 & 0xffffu)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(e89 >> 16)), pb0, pb1);
                     }
-                    const uint32_t d01 = __byte_perm(wv[0], wv[1], 0x5140), e01 = __byte_perm(wv[0], wv[1], 0x7362);
-                    const uint32_t d89 = __byte_perm(wv[2], wv[3], 0x5140), e89 = __byte_perm(wv[2], wv[3], 0x7362);
-                    mma_16816(ot[2 * p], e4m3x2_to_half2_bits(static_cast<uint16_t>(d01 & 0xffffu)),
-                              e4m3x2_to_half2_bits(static_cast<uint16_t>(d01 >> 16)),
-                              e4m3x2_to_half2_bits(static_cast<uint16_t>(d89 & 0xffffu)),
-                              e4m3x2_to_half2_bits(static_cast<uint16_t>(d89 >> 16)), pb0, pb1);
-                    mma_16816(ot[2 * p + 1], e4m3x2_to_half2_bits(static_cast<uint16_t>(e01 & 0xffffu)),
-                              e4m3x2_to_half2_bits(static_cast<uint16_t>(e01 >> 16)),
-                              e4m3x2_to_half2_bits(static_cast<uint16_t>(e89 & 0xffffu)),
-                              e4m3x2_to_half2_bits(static_cast<uint16_t>(e89 >> 16)), pb0, pb1);
-                }
-            } else {
-                #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    // A = V^T: (dims 16i.., tok 0-7) (dims 16i+8.., tok 0-7) (16i.., tok 8-15) (16i+8.., tok 8-15)
-                    const int tok = (mi >> 1) * 8 + mr, cp = 2 * i + (mi & 1);
-                    uint32_t vf[4];
-                    ldsm_x4_t(vbase + tile_off(tok, cp * 16), vf);
-                    mma_16816(ot[i], vf[0], vf[1], vf[2], vf[3], pb0, pb1);
+                } else {
+                    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        // A = V^T: (dims 16i.., tok 0-7) (dims 16i+8.., tok 0-7) (16i.., tok 8-15) (16i+8.., tok 8-15)
+                        const int tok = t16 + (mi >> 1) * 8 + mr, cp = 2 * i + (mi & 1);
+                        uint32_t vf[4];
+                        ldsm_x4_t(vbase + tile_off(tok, cp * 16), vf);
+                        mma_16816(ot[i], vf[0], vf[1], vf[2], vf[3], pb0, pb1);
+                    }
                 }
             }
-          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars[C::NC * NSW + w * NSW + st]));
