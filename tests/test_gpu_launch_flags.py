@@ -176,3 +176,48 @@ def test_unknown_flags_are_refused():
         cache.attention_ex(0, q, bt, cl, max(w.lens), w.scale, flags=4)
     cache.close()
     alloc.close()
+
+
+def test_flags_over_several_launches_with_head_pairs_and_fp8():
+    """2100 sequences (three launches of at most 1024), FP8 pool with B 16 and 2 heads
+    (head-pair items), fused append, 32-token partitions (a few long sequences merge in
+    two levels), KV_DECODE_WORKSPACE_ZEROED | KV_DECODE_PDL, two calls in a row on one
+    zeroed workspace: every launch's counters start and end at zero."""
+    B, H, d = 16, 2, 128
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 70, 2100).tolist()
+    lens[5], lens[1024 + 5], lens[2048 + 5] = 900, 1000, 700
+    nb = sum(-(-n // B) for n in lens) + 1
+    w = W.Workload("bigbatch_fp8", 92, 1, H, d, B, "f16", len(lens), lens, nb, 1 / math.sqrt(d))
+    cache = PagedKVCache(1, nb, B, H, d, "fp8")
+    poison(cache)
+    sc = np.float32(0.01)
+    for t in cache.k_scale + cache.v_scale:
+        t.fill_(float(sc))
+    alloc = BlockAllocator(nb, B, W.free_order(w))
+    seqs = [alloc.new_seq() for _ in lens]
+    ks = [W.host_tokens(w, s, n, "k") for s, n in enumerate(lens)]
+    vs = [W.host_tokens(w, s, n, "v") for s, n in enumerate(lens)]
+    # everything but each sequence's newest token is prefilled; the call appends it
+    prefill(cache, alloc, seqs, [k[:-1] if len(k) else k for k in ks], [v[:-1] if len(v) else v for v in vs])
+    for s, sid in enumerate(seqs):
+        if lens[s]:
+            alloc.append_slots(sid, 1)
+    bt, cl, got = tables_for(alloc, seqs, max(1, max(-(-n // B) for n in lens)))
+    assert got == lens
+    kn = torch.from_numpy(np.stack([k[-1] if len(k) else np.zeros((H, d), np.float16) for k in ks])).cuda()
+    vn = torch.from_numpy(np.stack([v[-1] if len(v) else np.zeros((H, d), np.float16) for v in vs])).cuda()
+    ksd = [OF.decode(OF.quantize(k, sc)) * float(sc) for k in ks]
+    vsd = [OF.decode(OF.quantize(v, sc)) * float(sc) for v in vs]
+    P = 32
+    ws = cache.zeroed_workspace(w.batch, max(lens), P)
+    for call in range(2):
+        q = W.host_queries(w, call)
+        # the second call appends the same token again into the same slot (same bytes)
+        out = cache.attention_ex(0, torch.from_numpy(q).cuda(), bt, cl, max(lens), w.scale, k_new=kn, v_new=vn,
+                                 partition_tokens=P, workspace=ws, flags=ZEROED | PDL)
+        err = max_abs(out.cpu().numpy(), OA.decode_attention(q, ksd, vsd, w.scale))
+        assert err <= tol_for("f16"), (call, err)
+    assert cache.device_error() == 0
+    cache.close()
+    alloc.close()
