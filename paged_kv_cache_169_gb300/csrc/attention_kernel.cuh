@@ -68,6 +68,7 @@ struct AttnArgs {
     int* err;
     int batch, H, B, max_blocks, ctx_limit, P, max_parts, num_blocks;
     int P_fine, s_fine;    // sequences s >= s_fine split into partitions of P_fine tokens (< P)
+    int early_tables;      // lens and tables may be read before griddepcontrol.wait (KV_DECODE_EARLY_TABLES)
     float qscale;          // scale * log2(e)
 };
 
@@ -898,9 +899,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
     // Programmatic dependent launch: nothing above read global memory.  Wait for the
     // kernels this launch depends on (a no-op when it was launched without that
     // attribute), then let the next launch on the stream begin scheduling: its CTAs start
-    // as this launch's CTAs exit and wait here in turn.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // as this launch's CTAs exit and wait here in turn.  With early_tables the caller has
+    // written context_lens and block_tables before the previous kernel began, so the
+    // prologue and the first block ids are read first and every warp waits just before
+    // its first other global access (producer: the first copies and claims; consumers:
+    // their first stage).
+    const bool early = a.early_tables != 0;
+    if (!early) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     // ---- prologue: clamp lengths, items per sequence, inclusive prefix
     for (int s = tid; s < a.batch; s += C::THREADS) {
         int c = a.lens[s];
@@ -969,9 +977,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         bool alive = mine;
         if (mine) {
             cur = decode(lane * gridDim.x + blockIdx.x);
-            if (cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
             load_ids(cur, 0);
         }
+        if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (mine && cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
         bool failed = false;
         uint64_t idle_since = 0;
         while (__any_sync(FULL, alive) && !failed) {
@@ -1099,6 +1108,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
     }
 
     // ==================================================================== consumer
+    if (early) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     if constexpr (C::MMA) {
         consumer_mma<C>(a, smem, s_ctx, warp, lane);
         return;

@@ -205,6 +205,7 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     const int64_t lim_tables = static_cast<int64_t>(max_blocks) * d.block_size;
     a.ctx_limit = static_cast<int>(lim_tables < max_context ? lim_tables : max_context);
     a.P = plan.partition;
+    a.early_tables = (plan.flags & KV_DECODE_PDL) && (plan.flags & KV_DECODE_EARLY_TABLES) ? 1 : 0;
     a.P_fine = plan.fine_partition;
     a.s_fine = plan.fine_from;
     a.max_parts = plan.max_parts;

@@ -5,8 +5,9 @@ Pools are filled with seeded N(0,1) values by torch's device generator (inputs, 
 kernel output); the oracle reads the sampled tiles back before the decode append and
 adds the new token itself.  The benchmark's call: one paged_decode_attention_ex per
 layer that appends each sequence's new token and attends, library-chosen partitioning,
-a workspace zero-filled once and kept over all calls (KV_DECODE_WORKSPACE_ZEROED) and
-programmatic dependent launch (KV_DECODE_PDL).  The 13B step also runs as kv_append
+a workspace zero-filled once and kept over all calls (KV_DECODE_WORKSPACE_ZEROED),
+programmatic dependent launch (KV_DECODE_PDL) and tables read before the previous launch
+ends (KV_DECODE_EARLY_TABLES: they are written before the layer loop).  The 13B step also runs as kv_append
 followed by paged_decode_attention.
 """
 
@@ -23,7 +24,7 @@ from paged_kv_cache_169_gb300.cache import PagedKVCache
 
 pytestmark = pytest.mark.gpu
 
-BENCH_FLAGS = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL
+BENCH_FLAGS = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL | abi.KV_DECODE_EARLY_TABLES
 
 
 def _snapshot(pool: torch.Tensor, table_row, n_blocks: int, h: int) -> np.ndarray:

@@ -150,7 +150,8 @@ def test_gqa70b_full_size_layer_sampled():
     ws = cache.zeroed_workspace(w.batch, max(w.lens), num_q_heads=Hq)
     out = cache.attention_ex(l, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale,
                              k_new=torch.from_numpy(k_new).cuda(), v_new=torch.from_numpy(v_new).cuda(),
-                             workspace=ws, flags=abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL)
+                             workspace=ws, flags=abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL |
+                             abi.KV_DECODE_EARLY_TABLES)
     out = out.cpu().numpy()
     worst = 0.0
     for (s, j) in samples:

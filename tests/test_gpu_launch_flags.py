@@ -25,7 +25,7 @@ from paged_kv_cache_169_gb300.cache import BlockAllocator, PagedKVCache
 
 pytestmark = pytest.mark.gpu
 
-ZEROED, PDL = abi.KV_DECODE_WORKSPACE_ZEROED, abi.KV_DECODE_PDL
+ZEROED, PDL, EARLY = abi.KV_DECODE_WORKSPACE_ZEROED, abi.KV_DECODE_PDL, abi.KV_DECODE_EARLY_TABLES
 COUNTER_BYTES = 512          # work and exit counters at the start of every workspace
 MERGE_FAN = 16               # partitions folded per group in a two-level merge
 
@@ -134,7 +134,10 @@ def _decode_loop_case(G):
 
 @pytest.mark.parametrize("G", [1, 8])
 @pytest.mark.parametrize("graph", [False, True])
-def test_pdl_back_to_back_fused_steps(G, graph):
+@pytest.mark.parametrize("early", [False, True])
+def test_pdl_back_to_back_fused_steps(G, graph, early):
+    """early: KV_DECODE_EARLY_TABLES as well (every step's tables and lengths are written
+    before the loop, so each launch may read them before the previous launch ends)."""
     w, cache, alloc, max_ctx, tabs, lens, qs, kn, vn, want = _decode_loop_case(G)
     steps = len(qs)
     P = 128     # several partitions per sequence: merges run in every launch
@@ -148,7 +151,7 @@ def test_pdl_back_to_back_fused_steps(G, graph):
         for i in range(steps):
             cache.attention_ex(0, qs[i], tabs[i], lens[i], max_ctx, w.scale, k_new=kn[i], v_new=vn[i],
                                out=outs[i], partition_tokens=P, workspace=ws, stream=stream,
-                               flags=ZEROED | PDL)
+                               flags=ZEROED | PDL | (EARLY if early else 0))
 
     if graph:
         g = torch.cuda.CUDAGraph()
@@ -173,7 +176,7 @@ def test_unknown_flags_are_refused():
     w, cache, alloc, ks, vs, bt, cl = _setup("f16", 1, 320)
     q = torch.from_numpy(W.host_queries(w)).cuda()
     with pytest.raises(abi.KvError):
-        cache.attention_ex(0, q, bt, cl, max(w.lens), w.scale, flags=4)
+        cache.attention_ex(0, q, bt, cl, max(w.lens), w.scale, flags=8)
     cache.close()
     alloc.close()
 
@@ -215,7 +218,7 @@ def test_flags_over_several_launches_with_head_pairs_and_fp8():
         q = W.host_queries(w, call)
         # the second call appends the same token again into the same slot (same bytes)
         out = cache.attention_ex(0, torch.from_numpy(q).cuda(), bt, cl, max(lens), w.scale, k_new=kn, v_new=vn,
-                                 partition_tokens=P, workspace=ws, flags=ZEROED | PDL)
+                                 partition_tokens=P, workspace=ws, flags=ZEROED | PDL | (EARLY if call else 0))
         err = max_abs(out.cpu().numpy(), OA.decode_attention(q, ksd, vsd, w.scale))
         assert err <= tol_for("f16"), (call, err)
     assert cache.device_error() == 0
