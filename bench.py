@@ -1,12 +1,14 @@
 """Benchmark: paged decode attention on GB300.
 
-Default workload: the LLaMA-13B-shaped full decode step — 40 layers x (kv_append of the
-new token of each of 48 sequences + paged_decode_attention over 48 sequences x 40 heads x
-2048 tokens, d 128, fp16 K/V, block size 16).  The pool is ~75 GiB, far larger than L2,
-so no flush is needed between steps.
+Default workload: the LLaMA-13B-shaped full decode step — 40 layers x one fused call
+(paged_decode_attention_ex: append the new token of each of 48 sequences, then attend
+over 48 sequences x 40 heads x 2048 tokens, d 128, fp16 K/V, block size 16), with a
+workspace zero-filled once, programmatic dependent launch and early tables (the three
+launch flags; ``--launch-flags`` and ``--unfused`` select the other forms).  The pool is
+~75 GiB, far larger than L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 oracle on the
-host cores instead (the reference arm of this build).
+host cores instead (the benchmark's reference arm).
 """
 
 from __future__ import annotations

@@ -47,7 +47,7 @@ typedef enum {
     KV_ERR_STATE = -3,        /* allocator: unknown/freed sequence, refcount misuse     */
     KV_ERR_CUDA = -4,         /* a CUDA runtime call failed (launch, query, memcpy)     */
     KV_ERR_DEVICE = -5,       /* kv_get_device_error found a device-side error bit      */
-    KV_ERR_UNSUPPORTED = -6   /* valid request this build does not implement            */
+    KV_ERR_UNSUPPORTED = -6   /* valid request this library version does not implement  */
 } kv_status;
 
 typedef enum { KV_F32 = 0, KV_F16 = 1, KV_FP8_E4M3 = 2 } kv_dtype;
