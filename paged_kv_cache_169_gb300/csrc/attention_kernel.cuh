@@ -196,8 +196,9 @@ struct Cfg {
     static constexpr int SCR_OFF = round_up(QR_OFF + NC * NSW * QR_BYTES, 1024);   // FP8 MMA scratch
     static constexpr int BAR_OFF = SCR_OFF + NC * SCR_BYTES;
     static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
+    static constexpr int ZERO_OFF = PREFIX_OFF + 2 * kMaxBatch * 4;  // 128 zero bytes (FP8 mma: masked rows)
     static constexpr int ALIGN_SLACK = MMA ? 1024 : 0;           // to 1024-align the base
-    static constexpr int SMEM = PREFIX_OFF + 2 * kMaxBatch * 4 + ALIGN_SLACK;
+    static constexpr int SMEM = ZERO_OFF + 128 + ALIGN_SLACK;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(NC <= 32 && (CT == 8 || CT == 16 || CT == 32), "launch shape");
     static_assert(Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && META_R % 16 == 0 && QR_OFF % 16 == 0, "alignment");
@@ -776,41 +777,44 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 l2[1] += p1 + p3;
                 // P^T as the B operand: the 8x8 blocks (tokens x queries) this lane holds a
                 // row pair of, transposed in registers (V scales folded in; 1 for fp16 pools)
-                const uint32_t pb0 = movmatrix_t(pack_half2(p0 * vsc[u][0], p1 * vsc[u][0]));
-                const uint32_t pb1 = movmatrix_t(pack_half2(p2 * vsc[u][1], p3 * vsc[u][1]));
+                uint32_t pb0 = movmatrix_t(pack_half2(p0 * vsc[u][0], p1 * vsc[u][0]));
+                uint32_t pb1 = movmatrix_t(pack_half2(p2 * vsc[u][1], p3 * vsc[u][1]));
+                if constexpr (C::FP8) {
+                    // the FP8 V fragments below pair tokens (4t, 4t+1) and (4t+2, 4t+3)
+                    // as k pairs (2t, 2t+1) and (2t+8, 2t+9): fetch P^T in that order
+                    // (tokens 4t.. sit with lane t' = 2t mod 4 of the first or second
+                    // 8-token block)
+                    const int s0 = 4 * g + ((2 * t) & 3), s1 = s0 + 1;
+                    const uint32_t a0 = __shfl_sync(FULL, pb0, s0), b0 = __shfl_sync(FULL, pb1, s0);
+                    const uint32_t a1 = __shfl_sync(FULL, pb0, s1), b1 = __shfl_sync(FULL, pb1, s1);
+                    pb0 = t < 2 ? a0 : b0;
+                    pb1 = t < 2 ? a1 : b1;
+                }
                 // O^T += V^T P^T, one 16-dim tile per mma
                 if constexpr (C::FP8) {
-                    // A = V^T straight from the E4M3 codes.  Output tile 2p+e: row g stands
-                    // for dim 32p+4g+2e and row g+8 for dim 32p+4g+2e+1 (the rows are written
-                    // back in that order); its k pairs are the tokens (2t, 2t+1) and (2t+8,
-                    // 2t+9).  A lane reads codes 32p+4g..+3 of those 4 token rows (piece
-                    // 2p + g/4 of each row, swizzled: no bank conflicts) and pairs equal
-                    // dims of two tokens by byte permutes.  Rows outside [lo, nt) read as
-                    // zero (their p is 0; their slots may hold anything).
-                    const bool masked = t16 + 16 > nt || t16 < lo;
-                    const char* vst = stg + C::V_OFF;
-                    const int r0 = t16 + 2 * t;
+                    // A = V^T from the E4M3 codes by a transposing byte ldmatrix: lanes 0-15
+                    // address the 16 token rows of dim tile 2pp, lanes 16-31 those of tile
+                    // 2pp+1 (16-byte piece of the swizzled row); lane (g, t) receives dims g
+                    // and g+8 of tokens 4t..4t+3, converted exactly to the fp16 pairs of
+                    // k pairs (2t, 2t+1) and (2t+8, 2t+9).  Rows outside [lo, nt) point at
+                    // a zero line (their p is 0; their slots may hold anything).
+                    const int vr = t16 + (lane & 15);
+                    const bool vzero = (t16 + 16 > nt || t16 < lo) && (vr < lo || vr >= nt);
+                    const uint32_t zaddr = smem_u32(smem + C::ZERO_OFF);
                     #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const int piece = 2 * p + (g >> 2), sub = 4 * (g & 3);
-                        uint32_t wv[4];               // token rows r0, r0+1, r0+8, r0+9
-                        #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int r = r0 + (v & 1) + 8 * (v >> 1);
-                            wv[v] = *reinterpret_cast<const uint32_t*>(vst + r * C::ROW +
-                                                                       (((piece ^ (r & 7)) << 4) | sub));
-                            if (masked && (r < lo || r >= nt)) wv[v] = 0u;
-                        }
-                        const uint32_t d01 = __byte_perm(wv[0], wv[1], 0x5140), e01 = __byte_perm(wv[0], wv[1], 0x7362);
-                        const uint32_t d89 = __byte_perm(wv[2], wv[3], 0x5140), e89 = __byte_perm(wv[2], wv[3], 0x7362);
-                        mma_16816(ot[2 * p], e4m3x2_to_half2_bits(static_cast<uint16_t>(d01 & 0xffffu)),
-                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(d01 >> 16)),
-                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(d89 & 0xffffu)),
-                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(d89 >> 16)), pb0, pb1);
-                        mma_16816(ot[2 * p + 1], e4m3x2_to_half2_bits(static_cast<uint16_t>(e01 & 0xffffu)),
-                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(e01 >> 16)),
-                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(e89 & 0xffffu)),
-                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(e89 >> 16)), pb0, pb1);
+                    for (int pp = 0; pp < 4; ++pp) {
+                        const int tile = 2 * pp + (lane >> 4);
+                        const uint32_t addr = vzero ? zaddr : vbase + vr * C::ROW + ((tile ^ (vr & 7)) << 4);
+                        uint32_t r[4];
+                        ldsm_b8_x2_t(addr, r);
+                        mma_16816(ot[2 * pp], e4m3x2_to_half2_bits(static_cast<uint16_t>(r[0] & 0xffffu)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(r[1] & 0xffffu)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(r[0] >> 16)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(r[1] >> 16)), pb0, pb1);
+                        mma_16816(ot[2 * pp + 1], e4m3x2_to_half2_bits(static_cast<uint16_t>(r[2] & 0xffffu)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(r[3] & 0xffffu)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(r[2] >> 16)),
+                                  e4m3x2_to_half2_bits(static_cast<uint16_t>(r[3] >> 16)), pb0, pb1);
                     }
                 } else {
                     #pragma unroll
@@ -853,19 +857,10 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                     }
                     dst = a.part_o + idx * D;
                 }
-                if constexpr (C::FP8) {
-                    // tiles 2p, 2p+1 rows g, g+8: dims 32p+4g .. 32p+4g+3
-                    #pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        *reinterpret_cast<float4*>(dst + 32 * p + 4 * g) =
-                            make_float4(ot[2 * p][h2] * inv, ot[2 * p][2 + h2] * inv, ot[2 * p + 1][h2] * inv,
-                                        ot[2 * p + 1][2 + h2] * inv);
-                } else {
-                    #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        dst[16 * i + g] = ot[i][h2] * inv;
-                        dst[16 * i + 8 + g] = ot[i][2 + h2] * inv;
-                    }
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    dst[16 * i + g] = ot[i][h2] * inv;
+                    dst[16 * i + 8 + g] = ot[i][2 + h2] * inv;
                 }
             }
             if (!(flags & F_SINGLE)) {
@@ -896,6 +891,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         for (int i = 0; i < 2 * NC * NSW; ++i) mbar_init(smem_u32(&bars[i]), 1);
         fence_mbar_init();
     }
+    if (tid < 32) reinterpret_cast<uint32_t*>(smem + C::ZERO_OFF)[tid] = 0u;   // read after the prologue's sync
     // Programmatic dependent launch: nothing above read global memory.  Wait for the
     // kernels this launch depends on (a no-op when it was launched without that
     // attribute), then let the next launch on the stream begin scheduling: its CTAs start

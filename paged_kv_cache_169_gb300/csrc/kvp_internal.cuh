@@ -181,6 +181,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
 }
 
+// Two 16x16 byte matrices from shared memory, transposed (lanes 0-15 give the 16 row
+// addresses of the first, lanes 16-31 of the second).  Lane 4g+t receives, of each
+// matrix, the bytes of column g in rows 4t..4t+3 (r[0], r[2]) and of column g+8 in rows
+// 4t..4t+3 (r[1], r[3]), in row order.
+__device__ __forceinline__ void ldsm_b8_x2_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
 // D += A(16x16, fp16, row) * B(16x8, fp16, col) with fp32 accumulation.
 // Transpose of an 8x8 b16 matrix held one row pair per lane (lane 4r + c: row r, cols 2c, 2c+1).
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
