@@ -68,6 +68,7 @@ struct AttnArgs {
     int* err;
     int batch, H, B, max_blocks, ctx_limit, P, max_parts, num_blocks;
     int P_fine, s_fine;    // sequences s >= s_fine split into partitions of P_fine tokens (< P)
+    int P_alt;             // < P: use P_alt instead when it still gives at most one item per consumer warp
     int early_tables;      // lens and tables may be read before griddepcontrol.wait (KV_DECODE_EARLY_TABLES)
     float qscale;          // scale * log2(e)
 };
@@ -197,8 +198,9 @@ struct Cfg {
     static constexpr int BAR_OFF = SCR_OFF + NC * SCR_BYTES;
     static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
     static constexpr int ZERO_OFF = PREFIX_OFF + 2 * kMaxBatch * 4;  // 128 zero bytes (FP8 mma: masked rows)
+    static constexpr int MISC_OFF = ZERO_OFF + 128;             // launch-wide values (the partition size)
     static constexpr int ALIGN_SLACK = MMA ? 1024 : 0;           // to 1024-align the base
-    static constexpr int SMEM = ZERO_OFF + 128 + ALIGN_SLACK;
+    static constexpr int SMEM = MISC_OFF + 16 + ALIGN_SLACK;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(NC <= 32 && (CT == 8 || CT == 16 || CT == 32), "launch shape");
     static_assert(Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && META_R % 16 == 0 && QR_OFF % 16 == 0, "alignment");
@@ -208,9 +210,10 @@ struct Cfg {
 
 __device__ __forceinline__ int nparts_of(int ctx, int P) { return ctx <= P ? 1 : (ctx + P - 1) / P; }
 
-// Partition size of sequence s: the sequences handed out last (s >= s_fine) take finer
-// partitions, so the last round of work items is short and the launch ends evenly.
-__device__ __forceinline__ int part_of(const AttnArgs& a, int s) { return s >= a.s_fine ? a.P_fine : a.P; }
+// Partition size of sequence s under the launch's partition size P: the sequences handed
+// out last (s >= s_fine) take finer partitions, so the last round of work items is short
+// and the launch ends evenly.
+__device__ __forceinline__ int part_of(int P, const AttnArgs& a, int s) { return s >= a.s_fine ? a.P_fine : P; }
 
 // Sliding window: the first attended token, and the first token actually read — rounded
 // down to a whole copy unit (rpc rows) so every copy stays inside blocks the window still
@@ -577,7 +580,8 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 //                     by ldmatrix.trans; 16 dim tiles of 8
 // fp32 accumulation and softmax, exact running max.
 template <typename C>
-__device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, const int* s_ctx, int w, int lane) {
+__device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, const int* s_ctx, int w, int lane,
+                                             int P_eff) {
     constexpr int NSW = C::NSW, D = C::D, G = C::G, CT = C::CT;
     static_assert((CT == 16 || (C::FP8 && CT == 32)) && D == 128, "tensor-core consumer shape");
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -865,7 +869,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             }
             if (!(flags & F_SINGLE)) {
                 const int ctx_s = s_ctx[ms];
-                const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), part_of(a, ms));
+                const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT), part_of(P_eff, a, ms));
                 ticket_issue(a, tk, shk, mpart, np, lane);
             }
         }
@@ -913,10 +917,31 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             c = c < 0 ? 0 : a.ctx_limit;
         }
         s_ctx[s] = c;
-        s_end[s] = HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), part_of(a, s));
+        s_end[s] = HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), part_of(a.P, a, s));
     }
     __syncthreads();
+    int* s_misc = reinterpret_cast<int*>(smem + C::MISC_OFF);
     if (warp == 0) {
+        // A launch whose items all fit in one round balances best with the smallest
+        // partition that still gives every item a consumer warp: take P_alt when it does.
+        int P_eff = a.P;
+        if (a.P_alt < a.P) {
+            int alt = 0;
+            for (int s = lane; s < a.batch; s += 32) {
+                const int c = s_ctx[s];
+                alt += HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), a.P_alt);
+            }
+            alt = __reduce_add_sync(FULL, alt);
+            if (alt <= static_cast<int>(gridDim.x) * NC) {
+                P_eff = a.P_alt;
+                for (int s = lane; s < a.batch; s += 32) {
+                    const int c = s_ctx[s];
+                    s_end[s] = HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), a.P_alt);
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) s_misc[0] = P_eff;
         int carry = 0;
         for (int base = 0; base < a.batch; base += 32) {
             int v = base + lane < a.batch ? s_end[base + lane] : 0;
@@ -932,6 +957,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
     }
     __syncthreads();
     const int n_items = s_end[a.batch - 1];
+    const int P_eff = s_misc[0];                // the launch's partition size
 
     auto full_bar = [&](int w, int st) { return smem_u32(&bars[w * NSW + st]); };
     auto empty_bar = [&](int w, int st) { return smem_u32(&bars[NC * NSW + w * NSW + st]); };
@@ -956,7 +982,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         const unsigned first_claim = gridDim.x * NC;
         auto claim = [&]() { pending = atomicAdd(a.counter, 1u) + first_claim; claimed = true; };
         auto decode = [&](unsigned idx) {
-            return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, HU, a.P, a.s_fine,
+            return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, HU, P_eff, a.s_fine,
                                    a.P_fine, a.window, rpc);
         };
         int ids[CBMAX];
@@ -1109,7 +1135,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     if constexpr (C::MMA) {
-        consumer_mma<C>(a, smem, s_ctx, warp, lane);
+        consumer_mma<C>(a, smem, s_ctx, warp, lane, P_eff);
         return;
     }
     constexpr int G = C::G, HP = C::HP, GE = C::GE, BR = C::BR;
@@ -1361,7 +1387,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 // publish the partials, then take a ticket; the last partition merges
                 const int ctx_s = s_ctx[meta.s];
                 const int np = nparts_of(ctx_s - attend_first(ctx_s, a.window, a.B < CT ? a.B : CT),
-                                         part_of(a, meta.s));
+                                         part_of(P_eff, a, meta.s));
                 ticket_issue(a, tk, shk, meta.p, np, lane);
             }
         }

@@ -52,6 +52,7 @@ struct AttnPlan {
     int partition;       // tokens per split-context partition
     int fine_partition;  // tokens per partition of the sequences from fine_from on
     int fine_from;       // first sequence with the finer partitions (batch: none)
+    int alt_partition;   // < partition: the kernel takes it when that still fits one round of items
     int max_parts;       // ceil(max_context / smallest partition)
     int consumers;       // consumer warps per CTA
     int group;           // query heads per KV head
