@@ -216,7 +216,10 @@ KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int ma
  *   partition_tokens  0 = library choice (about 8 work items per consumer warp, one
  *                 round for grouped-query launches, 256 to 1024 tokens; with 512 or
  *                 more and several rounds of items, the last sequences of the batch
- *                 take half of it); else tokens per split-context partition, a
+ *                 take half of it; at 256, the kernel splits into 192-token partitions
+ *                 when the actual lengths still give every item its own consumer warp,
+ *                 and the workspace is sized for that); else tokens per split-context
+ *                 partition, a
  *                 multiple of 32.  Sequences longer than one partition are split into
  *                 equal parts of at most that many tokens, attended per partition and
  *                 merged exactly (log-sum-exp) in the same launch by the warp that
