@@ -219,8 +219,8 @@ KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int ma
  *                 take half of it; at 256, the kernel splits into 192-token partitions
  *                 when the actual lengths still give every item its own consumer warp,
  *                 and the workspace is sized for that); else tokens per split-context
- *                 partition, a
- *                 multiple of 32.  Sequences longer than one partition are split into
+ *                 partition, a multiple of 32.  Sequences longer than one partition are
+ *                 split into
  *                 equal parts of at most that many tokens, attended per partition and
  *                 merged exactly (log-sum-exp) in the same launch by the warp that
  *                 finishes the last partition of that sequence and head.
