@@ -220,10 +220,9 @@ KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int ma
  *                 when the actual lengths still give every item its own consumer warp,
  *                 and the workspace is sized for that); else tokens per split-context
  *                 partition, a multiple of 32.  Sequences longer than one partition are
- *                 split into
- *                 equal parts of at most that many tokens, attended per partition and
- *                 merged exactly (log-sum-exp) in the same launch by the warp that
- *                 finishes the last partition of that sequence and head.
+ *                 split into equal parts of at most that many tokens, attended per
+ *                 partition and merged exactly (log-sum-exp) in the same launch by the
+ *                 warp that finishes the last partition of that sequence and head.
  *   workspace     device, >= paged_decode_workspace_size(...) bytes, 256-byte aligned,
  *                 contents need not be initialised; not shared between concurrent calls.
  * Arithmetic: fp32 scores, fp32 online softmax, fp32 accumulation of V.  For F16 and
