@@ -90,6 +90,21 @@ def test_window_with_fused_append(dtype, B, G):
     assert cache.device_error() == 0
 
 
+@pytest.mark.parametrize("dtype,B,G", [("f16", 16, 1), ("fp8", 16, 1), ("fp8", 16, 8), ("f16", 8, 4)])
+def test_window_with_fused_append_and_all_launch_flags(dtype, B, G):
+    """The window, the fused append and the three launch flags together, twice in a row
+    on one zero-filled workspace (the second call rewrites the same slots)."""
+    from paged_kv_cache_169_gb300 import abi
+    cache, q, bt, cl, kn, vn, want, _, w = _case(dtype, B, G, 100, 151 + G, fused=True)
+    flags = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL | abi.KV_DECODE_EARLY_TABLES
+    ws = cache.zeroed_workspace(w.batch, max(w.lens), 0, num_q_heads=w.q_heads, window=100)
+    for _ in range(2):
+        out = cache.attention_ex(0, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale, window=100,
+                                 k_new=kn, v_new=vn, workspace=ws, flags=flags).cpu().numpy()
+        assert max_abs(out, want) <= tol_for("f16")
+    assert cache.device_error() == 0
+
+
 def test_no_window_equals_plain_entry():
     cache, q, bt, cl, _, _, _, _, w = _case("f16", 16, 1, 10 ** 6, 140, fused=False)
     qt = torch.from_numpy(q).cuda()
