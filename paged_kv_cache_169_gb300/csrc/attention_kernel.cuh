@@ -139,7 +139,8 @@ struct Cfg {
     static constexpr int BR = BR_;
     static constexpr int GE = G_ * HP_;                   // output rows per work item
     static_assert(!MMA || (sizeof(KV_) <= 2 && D_ == 128 && G_ >= 2), "tensor-core path: fp16 or FP8, d 128, G >= 2");
-    static_assert(HP == 1 || (HP == 2 && G == 1 && !MMA && (BR == 8 || BR == 16)), "head pairs: one query per head");
+    static_assert(HP == 1 || ((HP == 2 || HP == 4) && G == 1 && !MMA && (BR == 8 || BR == 16)),
+                  "head groups: one query per head");
     using KV = KV_;
     using QT = QT_;
     static constexpr int ESZ = sizeof(KV);
@@ -149,10 +150,11 @@ struct Cfg {
     // as an fp16 one).  Head pairs: a chunk of CT tokens of two heads (fp16: 8, FP8: 16),
     // as many bytes as the single-head chunk.
     static constexpr int CT = MMA ? (ESZ == 1 ? 32 : 16)
-                                  : HP == 2 ? 16 / ESZ : (G >= 4 ? 16 : Tune<ESZ>::CT);
+                                  : HP == 4 ? 8 : HP == 2 ? 16 / ESZ : (G >= 4 ? 16 : Tune<ESZ>::CT);
     static_assert(HP == 1 || BR <= CT, "head pairs: whole blocks per copy");
-    static constexpr int TPL = CT * HP / 2;               // tokens per lane per chunk
-    static constexpr int DPL = D / 16;                    // dims per lane
+    static constexpr int TPL = HP >= 2 ? CT : CT / 2;     // tokens per lane per chunk
+    static constexpr int LPR = HP == 4 ? 8 : 16;          // lanes per token row
+    static constexpr int DPL = D / LPR;                   // dims per lane
     static constexpr int CBMAX = CT >= 8 ? CT / 8 : 1;    // blocks per chunk at B = 8
     static constexpr int ROW = D * ESZ;                   // bytes of one token row of one head
     static constexpr int KV_BYTES = CT * ROW * HP;        // bytes of K (or V) per chunk
@@ -235,15 +237,17 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
     return v;
 }
-// over the 16 lanes of each half-warp
-__device__ __forceinline__ float half_max(float v) {
+// over each group of W consecutive lanes (W = 16: half-warps, 8: quarter-warps)
+template <int W>
+__device__ __forceinline__ float group_max(float v) {
     #pragma unroll
-    for (int o = 8; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+    for (int o = W / 2; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
     return v;
 }
-__device__ __forceinline__ float half_sum(float v) {
+template <int W>
+__device__ __forceinline__ float group_sum(float v) {
     #pragma unroll
-    for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+    for (int o = W / 2; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
     return v;
 }
 
@@ -335,7 +339,15 @@ __device__ __forceinline__ void load_row_h(const char* row, int sub, uint32_t (&
         }
     } else {
         static_assert(C::ESZ == 1, "fp16 or FP8 rows");
-        if constexpr (C::DPL == 8) {
+        if constexpr (C::DPL == 16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                x[2 * k] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w4[k] & 0xffffu));
+                x[2 * k + 1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w4[k] >> 16));
+            }
+        } else if constexpr (C::DPL == 8) {
             const uint2 v = *reinterpret_cast<const uint2*>(p);
             x[0] = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.x & 0xffffu));
             x[1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(v.x >> 16));
@@ -1138,21 +1150,22 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         consumer_mma<C>(a, smem, s_ctx, warp, lane, P_eff);
         return;
     }
-    constexpr int G = C::G, HP = C::HP, GE = C::GE, BR = C::BR;
+    constexpr int G = C::G, HP = C::HP, GE = C::GE, BR = C::BR, LPR = C::LPR;
     const int w = warp;
     // single heads: the half-warps take alternate tokens (half = which token of each row
-    // pair); head pairs: half-warp e takes head e of the pair, every token of the chunk
-    const int half = lane >> 4;
-    const int sub = lane & 15;                  // which DPL-element slice of the row
-    const int tok_l = HP == 2 ? (lane & (TPL - 1)) : 2 * (lane & (TPL - 1)) + half;   // token whose score this lane holds
-    const bool primary = (lane & 15) < TPL;              // one holder per token when TPL < 16
+    // pair); head groups: lane group e (16 lanes for pairs, 8 for quads) takes head e of
+    // the item, every token of the chunk
+    const int half = lane / LPR;
+    const int sub = lane & (LPR - 1);           // which DPL-element slice of the row
+    const int tok_l = HP >= 2 ? (lane & (TPL - 1)) : 2 * (lane & (TPL - 1)) + half;   // token whose score this lane holds
+    const bool primary = (lane & (LPR - 1)) < TPL;       // one holder per token when TPL < LPR
     // stage byte offset of token row t (of the lane's head, from its K/V base): with head
     // pairs each copy holds BR rows of head 0, then BR rows of head 1
     auto tok_off = [](int t) -> int {
-        if constexpr (HP == 2) return (t / BR) * 2 * BR * C::ROW + (t % BR) * C::ROW;
+        if constexpr (HP >= 2) return (t / BR) * HP * BR * C::ROW + (t % BR) * C::ROW;
         else return t * C::ROW;
     };
-    const int head_off = HP == 2 ? half * BR * C::ROW : half * C::ROW;
+    const int head_off = HP >= 2 ? half * BR * C::ROW : half * C::ROW;
     // fp16 and FP8 rows with fp16 queries: products of fp16 operands accumulated in fp32
     // (fma.f32.f16), no widening of the K/V elements; the query stays unscaled fp16 and
     // the score scale multiplies the reduced dot product.  fp32 pools: fp32 throughout.
@@ -1199,7 +1212,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 lsum[g] = 0.f;
                 #pragma unroll
                 for (int i = 0; i < DPL / 2; ++i) acc[g][i] = make_float2(0.f, 0.f);
-                const char* qrow = stg + C::Q_OFF + (HP == 2 ? half : g) * D * sizeof(typename C::QT);
+                const char* qrow = stg + C::Q_OFF + (HP >= 2 ? half : g) * D * sizeof(typename C::QT);
                 if constexpr (MX) {
                     if (nt > 0) {
                         const uint32_t* qp = reinterpret_cast<const uint32_t*>(qrow) + sub * (DPL / 2);
@@ -1226,7 +1239,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 const int head = meta.h * HP + e;
                 const int64_t sh = static_cast<int64_t>(meta.s) * a.H + head;
                 const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + head) * a.B + mp->patch_off;
-                const int so = tok_off(r) + (HP == 2 ? e * BR * C::ROW : 0);
+                const int so = tok_off(r) + (HP >= 2 ? e * BR * C::ROW : 0);
                 patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, srow + C::K_OFF + so,
                              a.kpool + grow * C::ROW, ksc, lane);
                 patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, srow + C::V_OFF + so,
@@ -1252,7 +1265,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             for (int i = 0; i < TPL; ++i) {          // token 2i + half (pairs: i); one K load serves G queries
                 if constexpr (MX) {
                     uint32_t kx[DPL / 2];
-                    load_row_h<C>(K + tok_off(HP == 2 ? i : 2 * i), sub, kx);
+                    load_row_h<C>(K + tok_off(HP >= 2 ? i : 2 * i), sub, kx);
                     #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         float2 d2 = make_float2(0.f, 0.f);
@@ -1262,7 +1275,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                     }
                 } else {
                     float2 kx[DPL / 2];
-                    load_row<C>(K + tok_off(HP == 2 ? i : 2 * i), sub, kx);
+                    load_row<C>(K + tok_off(HP >= 2 ? i : 2 * i), sub, kx);
                     #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         float2 d2 = make_float2(0.f, 0.f);
@@ -1290,11 +1303,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 }
                 float x = part[g][0];
                 #pragma unroll
-                for (int off = TPL; off < 16; off <<= 1) x += __shfl_xor_sync(FULL, x, off);
+                for (int off = TPL; off < LPR; off <<= 1) x += __shfl_xor_sync(FULL, x, off);
                 x *= xs;
                 x = (tok_l < nt && tok_l >= lo) ? x : -CUDART_INF_F;
                 if (__any_sync(FULL, x > m[g] + 8.f)) {   // raise the running max only when needed
-                    const float m_new = fmaxf(m[g], HP == 2 ? half_max(x) : warp_max(x));
+                    const float m_new = fmaxf(m[g], HP >= 2 ? group_max<LPR>(x) : warp_max(x));
                     const float corr = ex2_approx(m[g] - m_new);
                     lsum[g] *= corr;
                     #pragma unroll
@@ -1312,14 +1325,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             for (int g = 0; g < G; ++g) pvh[g] = MX ? pack_half2(pv[g], pv[g]) : 0u;
             #pragma unroll
             for (int i = 0; i < TPL; ++i) {          // token 2i + half (pairs: i), its p from lane i (+16)
-                const int ti = HP == 2 ? i : 2 * i + half;
+                const int ti = HP >= 2 ? i : 2 * i + half;
                 if constexpr (MX) {
                     uint32_t ph[G];
                     #pragma unroll
-                    for (int g = 0; g < G; ++g) ph[g] = __shfl_sync(FULL, pvh[g], i + (lane & 16));
+                    for (int g = 0; g < G; ++g) ph[g] = __shfl_sync(FULL, pvh[g], i + (lane & ~(LPR - 1)));
                     if ((nt == CT && lo == 0) || (ti < nt && ti >= lo)) {
                         uint32_t vx[DPL / 2];
-                        load_row_h<C>(V + tok_off(HP == 2 ? i : 2 * i), sub, vx);
+                        load_row_h<C>(V + tok_off(HP >= 2 ? i : 2 * i), sub, vx);
                         #pragma unroll
                         for (int g = 0; g < G; ++g) {
                             #pragma unroll
@@ -1329,10 +1342,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 } else {
                     float pt[G];
                     #pragma unroll
-                    for (int g = 0; g < G; ++g) pt[g] = __shfl_sync(FULL, pv[g], i + (lane & 16));
+                    for (int g = 0; g < G; ++g) pt[g] = __shfl_sync(FULL, pv[g], i + (lane & ~(LPR - 1)));
                     if ((nt == CT && lo == 0) || (ti < nt && ti >= lo)) {
                         float2 vx[DPL / 2];
-                        load_row<C>(V + tok_off(HP == 2 ? i : 2 * i), sub, vx);
+                        load_row<C>(V + tok_off(HP >= 2 ? i : 2 * i), sub, vx);
                         #pragma unroll
                         for (int g = 0; g < G; ++g) {
                             const float2 p2 = make_float2(pt[g], pt[g]);
@@ -1350,20 +1363,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             const int64_t shk = static_cast<int64_t>(meta.s) * HU + meta.h;   // (sequence, work unit)
             #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float l = HP == 2 ? half_sum(lsum[g]) : warp_sum(lsum[g]);
+                const float l = HP >= 2 ? group_sum<LPR>(lsum[g]) : warp_sum(lsum[g]);
                 float2 o[DPL / 2];
                 #pragma unroll
                 for (int i = 0; i < DPL / 2; ++i) {
-                    if constexpr (HP == 2) {
-                        o[i] = acc[g][i];              // each half holds its own head
+                    if constexpr (HP >= 2) {
+                        o[i] = acc[g][i];              // each lane group holds its own head
                     } else {                           // the two halves saw different tokens
                         o[i].x = acc[g][i].x + __shfl_xor_sync(FULL, acc[g][i].x, 16);
                         o[i].y = acc[g][i].y + __shfl_xor_sync(FULL, acc[g][i].y, 16);
                     }
                 }
-                const int64_t sq = shk * GE + (HP == 2 ? half : g);   // (sequence, query head)
+                const int64_t sq = shk * GE + (HP >= 2 ? half : g);   // (sequence, query head)
                 if (meta.flags & F_SINGLE) {
-                    if (HP == 2 || half == 0) {
+                    if (HP >= 2 || half == 0) {
                         float2* dst = reinterpret_cast<float2*>(a.out + sq * D + sub * DPL);
                         const float inv = nt > 0 ? 1.f / l : 0.f;   // empty sequence -> zeros
                         #pragma unroll
@@ -1372,11 +1385,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                     }
                 } else {
                     const int64_t idx = sq * a.max_parts + meta.p;
-                    if (HP == 2 ? sub == 0 : lane == 0) {
+                    if (HP >= 2 ? sub == 0 : lane == 0) {
                         a.part_ml[2 * idx] = m[g];
                         a.part_ml[2 * idx + 1] = l;
                     }
-                    if (HP == 2 || half == 0) {
+                    if (HP >= 2 || half == 0) {
                         float2* dst = reinterpret_cast<float2*>(a.part_o + idx * D + sub * DPL);
                         #pragma unroll
                         for (int i = 0; i < DPL / 2; ++i) dst[i] = o[i];

@@ -31,29 +31,34 @@ int consumers_for_g(const kv_pool* pool) {
 
 }  // namespace
 
-// Block rows of the head-pair configuration (Cfg HP = 2) this pool runs single-query
-// decode with, or 0 for one head per work item.  Pools whose (block, head) tiles are
-// small pay for every copy: FP8 pools with B = 8 or 16, fp16 pools with B = 8 (head_dim
-// 128, an even number of heads).  KVP_NO_HEAD_PAIRS (tuning builds only) turns it off.
-int head_pair_rows(const kv_pool_desc& d, int group) {
+// Heads per work item of this pool's single-query decode (Cfg HP: 1, 2 or 4).  Pools whose
+// (block, head) tiles are small pay for every copy, so one copy brings a block's tiles of
+// several adjacent heads: FP8 pools with B = 8 take four (4 KiB copies), FP8 pools with
+// B = 16 and fp16 pools with B = 8 two (head_dim 128; the head count a multiple of the
+// group).  KVP_NO_HEAD_PAIRS (tuning builds only) turns it off.
+int head_group(const kv_pool_desc& d, int group) {
 #if defined(KVP_NO_HEAD_PAIRS)
     (void)d; (void)group;
-    return 0;
+    return 1;
 #else
-    if (group != 1 || d.head_dim != 128 || d.num_heads % 2 != 0) return 0;
-    if (d.dtype == KV_FP8_E4M3 && (d.block_size == 8 || d.block_size == 16)) return d.block_size;
-    if (d.dtype == KV_F16 && d.block_size == 8) return 8;
-    return 0;
+    if (group != 1 || d.head_dim != 128) return 1;
+    if (d.dtype == KV_FP8_E4M3 && d.block_size == 8 && d.num_heads % 4 == 0) return 4;
+    if (d.num_heads % 2 != 0) return 1;
+    if (d.dtype == KV_FP8_E4M3 && (d.block_size == 8 || d.block_size == 16)) return 2;
+    if (d.dtype == KV_F16 && d.block_size == 8) return 2;
+    return 1;
 #endif
 }
 
 namespace {
 
 int consumers_for(const kv_pool* pool, int group) {
-    if (const int br = head_pair_rows(pool->desc, group)) {
+    const int hp = head_group(pool->desc, group);
+    if (hp == 4) return consumers_of<Cfg<128, uint8_t, __half, 1, false, 4, 8>>();
+    if (hp == 2) {
         if (pool->desc.dtype == KV_F16) return consumers_of<Cfg<128, __half, __half, 1, false, 2, 8>>();
-        return br == 8 ? consumers_of<Cfg<128, uint8_t, __half, 1, false, 2, 8>>()
-                       : consumers_of<Cfg<128, uint8_t, __half, 1, false, 2, 16>>();
+        return pool->desc.block_size == 8 ? consumers_of<Cfg<128, uint8_t, __half, 1, false, 2, 8>>()
+                                          : consumers_of<Cfg<128, uint8_t, __half, 1, false, 2, 16>>();
     }
     switch (group) {
         case 2: return consumers_for_g<2>(pool);
@@ -91,7 +96,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     } else if (partition_tokens == 0) {
         // work items are (sequence, KV head or head pair, partition), handed out dynamically
         const int64_t units = static_cast<int64_t>(batch > 0 ? batch : 1) * d.num_heads /
-                              (head_pair_rows(d, group) ? 2 : 1);
+                              head_group(d, group);
         const int64_t warps = static_cast<int64_t>(pool->num_sms) * nc;
         int64_t parts;
         if (group == 1) {
@@ -132,7 +137,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
         // half-size partitions (measured: ragged 256 sequences +1 % fp16, +4 % FP8; with
         // 256-token items it gained nothing and the doubled split count of long contexts
         // cost 3 %).
-        const int hu = d.num_heads / (head_pair_rows(d, group) ? 2 : 1);
+        const int hu = d.num_heads / head_group(d, group);
         const int64_t warps = static_cast<int64_t>(pool->num_sms) * nc;
         const int64_t items = static_cast<int64_t>(batch) * hu * ((span + P - 1) / P);
         if (items >= 2 * warps) {
@@ -231,10 +236,14 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
         if (d.head_dim == 128) return launch_typed<Cfg<128, float, float>>(pool, a, plan, counters, stream);
         return launch_typed<Cfg<64, float, float>>(pool, a, plan, counters, stream);
     }
-    if (const int br = head_pair_rows(d, 1)) {      // two heads per work item
+    const int hp = head_group(d, 1);
+    if (hp == 4)                                     // four heads per work item
+        return launch_typed<Cfg<128, uint8_t, __half, 1, false, 4, 8>>(pool, a, plan, counters, stream);
+    if (hp == 2) {                                   // two heads per work item
         if (d.dtype == KV_F16)
             return launch_typed<Cfg<128, __half, __half, 1, false, 2, 8>>(pool, a, plan, counters, stream);
-        if (br == 8) return launch_typed<Cfg<128, uint8_t, __half, 1, false, 2, 8>>(pool, a, plan, counters, stream);
+        if (d.block_size == 8)
+            return launch_typed<Cfg<128, uint8_t, __half, 1, false, 2, 8>>(pool, a, plan, counters, stream);
         return launch_typed<Cfg<128, uint8_t, __half, 1, false, 2, 16>>(pool, a, plan, counters, stream);
     }
     if (d.dtype == KV_F16) {

@@ -68,8 +68,8 @@ struct AttnPlan {
 };
 // group: query heads per KV head (1, or 2/4/8 for fp16 and FP8 pools)
 bool valid_group(const kv_pool_desc& d, int group);
-// block rows of the head-pair launch shape used for this pool (0: one head per work item)
-int head_pair_rows(const kv_pool_desc& d, int group);
+// heads per work item of this pool's single-query decode (1, 2 or 4)
+int head_group(const kv_pool_desc& d, int group);
 int plan_attention(const kv_pool* pool, int batch, int max_context, int partition_tokens,
                    AttnPlan* plan, int group = 1, int window = 0);
 int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,

@@ -27,12 +27,14 @@ def _bits(t):
     return a.view({4: np.uint32, 2: np.uint16, 1: np.uint8}[a.itemsize])
 
 
-@pytest.mark.parametrize("dtype,B,d,P", [("f16", 16, 128, 0), ("f16", 8, 128, 64), ("f16", 32, 64, 0),
-                                         ("f32", 16, 64, 32), ("fp8", 16, 128, 0), ("fp8", 8, 64, 64)])
-def test_fused_equals_append_then_attention(dtype, B, d, P):
+@pytest.mark.parametrize("dtype,B,d,P,H", [("f16", 16, 128, 0, 6), ("f16", 8, 128, 64, 6), ("f16", 32, 64, 0, 6),
+                                           ("f32", 16, 64, 32, 6), ("fp8", 16, 128, 0, 6), ("fp8", 8, 64, 64, 6),
+                                           ("fp8", 8, 128, 0, 8), ("fp8", 8, 128, 32, 6)])
+def test_fused_equals_append_then_attention(dtype, B, d, P, H):
+    """Head groups: FP8 with B 8 and 8 heads takes four heads per work item, with 6 heads
+    two; FP8 with B 16 and fp16 with B 8 two."""
     rng = np.random.default_rng(61)
     lens = [0, 1, B, B + 1, 31, 32, 33, 300, 777, 1500]
-    H = 6
     nb = sum(-(-n // B) for n in lens) + 5
     w = W.Workload("fused", 61, 1, H, d, B, "f32" if dtype == "f32" else "f16", len(lens), lens, nb,
                    1 / math.sqrt(d))
