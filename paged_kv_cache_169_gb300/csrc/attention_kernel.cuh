@@ -155,6 +155,7 @@ struct Cfg {
     static constexpr int TPL = HP >= 2 ? CT : CT / 2;     // tokens per lane per chunk
     static constexpr int LPR = HP == 4 ? 8 : 16;          // lanes per token row
     static constexpr int DPL = D / LPR;                   // dims per lane
+    static_assert(TPL <= LPR, "the transpose-reduce leaves one token per lane");
     static constexpr int CBMAX = CT >= 8 ? CT / 8 : 1;    // blocks per chunk at B = 8
     static constexpr int ROW = D * ESZ;                   // bytes of one token row of one head
     static constexpr int KV_BYTES = CT * ROW * HP;        // bytes of K (or V) per chunk
