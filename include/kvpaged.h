@@ -313,10 +313,18 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *                started (for instance host copies issued before a step's layer loop), so
  *                the kernel may read them, and the first block ids they point to, while
  *                that kernel is still finishing.  q, k_new, v_new, the pool, out and the
- *                workspace are still read and written only after it has completed. */
+ *                workspace are still read and written only after it has completed.
+ *     KV_DECODE_OUT_F16  out is float16 [batch][num_q_heads][head_dim] instead of float32:
+ *                each element is the float32 result rounded to nearest even (beyond the
+ *                float16 range: +-inf), as the attention output of [KV Cache篇] §3.1 is cast
+ *                back to the query's type.  Partials and their merge stay float32; only the
+ *                final store is rounded, so the value equals the float32 call's, rounded.
+ *   out          device float32 [batch][num_q_heads][head_dim], or float16 with
+ *                KV_DECODE_OUT_F16; 16-byte aligned. */
 #define KV_DECODE_WORKSPACE_ZEROED 1u
 #define KV_DECODE_PDL 2u
 #define KV_DECODE_EARLY_TABLES 4u
+#define KV_DECODE_OUT_F16 8u
 typedef struct {
     int layer;
     const void* q;
@@ -324,7 +332,7 @@ typedef struct {
     const void* k_new;
     const void* v_new;
     kv_dtype in_dtype;
-    float* out;
+    void* out;
     const int32_t* block_tables;
     int max_blocks_per_seq;
     const int32_t* context_lens;

@@ -179,16 +179,23 @@ class PagedKVCache:
                      context_lens: torch.Tensor, max_context: int, scale: float, window: int = 0,
                      k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
                      out: torch.Tensor | None = None, partition_tokens: int = 0,
-                     workspace: torch.Tensor | None = None, stream=None, flags: int = 0) -> torch.Tensor:
+                     workspace: torch.Tensor | None = None, stream=None, flags: int = 0,
+                     out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
         """Every decode option in one call (paged_decode_attention_ex): grouped-query heads
         (q [batch, Hq, d]), optional fused append, and a sliding window of ``window`` tokens.
         ``flags``: abi.KV_DECODE_WORKSPACE_ZEROED (the workspace's counters are zero: a
-        zero-filled workspace used only by decode calls since) and/or abi.KV_DECODE_PDL."""
+        zero-filled workspace used only by decode calls since), abi.KV_DECODE_PDL,
+        abi.KV_DECODE_EARLY_TABLES.  A float16 ``out`` (or ``out_dtype``) adds
+        abi.KV_DECODE_OUT_F16: the result is stored rounded to float16."""
         batch, hq = q.shape[0], q.shape[1]
         if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
             raise ValueError("block_tables and context_lens must be int32")
         if out is None:
-            out = torch.empty((batch, hq, self.head_dim), dtype=torch.float32, device=q.device)
+            out = torch.empty((batch, hq, self.head_dim), dtype=out_dtype, device=q.device)
+        if out.dtype == torch.float16:
+            flags |= abi.KV_DECODE_OUT_F16
+        elif out.dtype != torch.float32 or flags & abi.KV_DECODE_OUT_F16:
+            raise ValueError("out must be float32, or float16 (KV_DECODE_OUT_F16)")
         a = abi.kv_decode_args()
         a.layer, a.q, a.num_q_heads = layer, _dev_ptr(q, "q"), hq
         a.k_new = _dev_ptr(k_new, "k_new") if k_new is not None else None

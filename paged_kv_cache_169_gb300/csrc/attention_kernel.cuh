@@ -51,7 +51,7 @@ struct AttnArgs {
     const float* kscale;
     const float* vscale;
     const void* q;
-    float* out;
+    void* out;             // [batch][H*G][D]: float, or __half when out_f16
     const int32_t* tables;
     const int32_t* lens;
     float* part_ml;        // [batch*H*max_parts][2]  (m in log2 units, l)
@@ -70,6 +70,7 @@ struct AttnArgs {
     int P_fine, s_fine;    // sequences s >= s_fine split into partitions of P_fine tokens (< P)
     int P_alt;             // < P: use P_alt instead when it still gives at most one item per consumer warp
     int early_tables;      // lens and tables may be read before griddepcontrol.wait (KV_DECODE_EARLY_TABLES)
+    int out_f16;           // the result is stored as float16, rounded to nearest (KV_DECODE_OUT_F16)
     float qscale;          // scale * log2(e)
 };
 
@@ -456,7 +457,24 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
         }
     }
     const float inv = FINAL ? 1.f / L : 1.f;
-    float* out = FINAL ? a.out + (sh0 + g) * D : a.part_o + base * D;
+    if (FINAL && a.out_f16) {                          // rounded once, from the float32 result
+        __half* oh = static_cast<__half*>(a.out) + (sh0 + g) * D;
+        #pragma unroll
+        for (int i = 0; i < DL / VEC; ++i) {
+            if constexpr (VEC == 4) {
+                const __half2 lo = __floats2half2_rn(acc[4 * i] * inv, acc[4 * i + 1] * inv);
+                const __half2 hi = __floats2half2_rn(acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+                uint2 w;
+                w.x = *reinterpret_cast<const unsigned*>(&lo);
+                w.y = *reinterpret_cast<const unsigned*>(&hi);
+                reinterpret_cast<uint2*>(oh)[i * LPH + q] = w;
+            } else {
+                reinterpret_cast<__half2*>(oh)[i * LPH + q] = __floats2half2_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+            }
+        }
+        return;
+    }
+    float* out = FINAL ? static_cast<float*>(a.out) + (sh0 + g) * D : a.part_o + base * D;
     if (!FINAL) {
         __syncwarp();                                  // every lane has read partial `first`
         if (q == 0) reinterpret_cast<float2*>(a.part_ml)[base] = make_float2(mx, L);
@@ -865,7 +883,16 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 float* dst;
                 if (flags & F_SINGLE) {
                     inv = nt > 0 ? 1.f / (h2 ? lb : la) : 0.f;
-                    dst = a.out + sq * D;
+                    if (a.out_f16) {
+                        __half* dh = static_cast<__half*>(a.out) + sq * D;
+                        #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            dh[16 * i + g] = __float2half_rn(ot[i][h2] * inv);
+                            dh[16 * i + 8 + g] = __float2half_rn(ot[i][2 + h2] * inv);
+                        }
+                        continue;
+                    }
+                    dst = static_cast<float*>(a.out) + sq * D;
                 } else {
                     const int64_t idx = sq * a.max_parts + mpart;
                     if (g == 0) {
@@ -1378,11 +1405,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 const int64_t sq = shk * GE + (HP >= 2 ? half : g);   // (sequence, query head)
                 if (meta.flags & F_SINGLE) {
                     if (HP >= 2 || half == 0) {
-                        float2* dst = reinterpret_cast<float2*>(a.out + sq * D + sub * DPL);
                         const float inv = nt > 0 ? 1.f / l : 0.f;   // empty sequence -> zeros
-                        #pragma unroll
-                        for (int i = 0; i < DPL / 2; ++i)
-                            dst[i] = nt > 0 ? make_float2(o[i].x * inv, o[i].y * inv) : make_float2(0.f, 0.f);
+                        if (a.out_f16) {
+                            __half2* dst = reinterpret_cast<__half2*>(static_cast<__half*>(a.out) + sq * D + sub * DPL);
+                            #pragma unroll
+                            for (int i = 0; i < DPL / 2; ++i)
+                                dst[i] = __floats2half2_rn(nt > 0 ? o[i].x * inv : 0.f, nt > 0 ? o[i].y * inv : 0.f);
+                        } else {
+                            float2* dst = reinterpret_cast<float2*>(static_cast<float*>(a.out) + sq * D + sub * DPL);
+                            #pragma unroll
+                            for (int i = 0; i < DPL / 2; ++i)
+                                dst[i] = nt > 0 ? make_float2(o[i].x * inv, o[i].y * inv) : make_float2(0.f, 0.f);
+                        }
                     }
                 } else {
                     const int64_t idx = sq * a.max_parts + meta.p;
@@ -1427,7 +1461,8 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
         AttnArgs sa = args;
         sa.batch = total - s0 < kMaxBatch ? total - s0 : kMaxBatch;
         sa.q = static_cast<const char*>(args.q) + s0 * qrow;
-        sa.out = args.out + static_cast<int64_t>(s0) * args.H * C::G * C::D;
+        sa.out = static_cast<char*>(args.out) +
+                 static_cast<int64_t>(s0) * args.H * C::G * C::D * (args.out_f16 ? 2 : 4);
         sa.tables = args.tables + static_cast<int64_t>(s0) * args.max_blocks;
         sa.lens = args.lens + s0;
         if (args.k_new) {

@@ -173,7 +173,7 @@ int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,
 }
 
 int launch_attention_append(const kv_pool* pool, int layer, const void* q, const void* k_new,
-                            const void* v_new, int in_bytes, float* out, const int32_t* block_tables,
+                            const void* v_new, int in_bytes, void* out, const int32_t* block_tables,
                             int max_blocks, const int32_t* context_lens, int batch, int max_context,
                             float scale, const AttnPlan& plan, void* workspace, cudaStream_t stream) {
     const kv_pool_desc& d = pool->desc;
@@ -219,6 +219,7 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     a.ctx_limit = static_cast<int>(lim_tables < max_context ? lim_tables : max_context);
     a.P = plan.partition;
     a.early_tables = (plan.flags & KV_DECODE_PDL) && (plan.flags & KV_DECODE_EARLY_TABLES) ? 1 : 0;
+    a.out_f16 = (plan.flags & KV_DECODE_OUT_F16) ? 1 : 0;
     a.P_fine = plan.fine_partition;
     a.P_alt = plan.alt_partition;
     a.s_fine = plan.fine_from;

@@ -78,7 +78,7 @@ int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,
                      void* workspace, cudaStream_t stream);
 // Same, with the fused append of each sequence's newest token (k_new/v_new [batch][H][D]).
 int launch_attention_append(const kv_pool* pool, int layer, const void* q, const void* k_new,
-                            const void* v_new, int in_bytes, float* out, const int32_t* block_tables,
+                            const void* v_new, int in_bytes, void* out, const int32_t* block_tables,
                             int max_blocks, const int32_t* context_lens, int batch, int max_context,
                             float scale, const AttnPlan& plan, void* workspace, cudaStream_t stream);
 

@@ -37,6 +37,20 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(abi._SIGS), "binding and header must list the same entry points"
 
 
+def test_header_constants_match_the_binding():
+    """Every #define KV_* with an integer value in the header equals the binding's constant
+    of the same name (the flags and status codes cross the ABI as plain integers)."""
+    text = open(HEADER, encoding="utf-8").read()
+    defs = dict(re.findall(r"^#define\s+(KV_[A-Z0-9_]+)\s+\(?(-?\d+)u?\)?\s*$", text, flags=re.M))
+    assert {"KV_DECODE_WORKSPACE_ZEROED", "KV_DECODE_PDL", "KV_DECODE_EARLY_TABLES",
+            "KV_DECODE_OUT_F16"} <= set(defs)
+    for name, value in defs.items():
+        if hasattr(abi, name):
+            assert getattr(abi, name) == int(value), name
+    flags = [int(defs[n]) for n in defs if n.startswith("KV_DECODE_")]
+    assert sum(flags) == 15 and all(f & (f - 1) == 0 for f in flags)   # distinct bits
+
+
 def test_status_strings(lib):
     assert abi.kv_status_str(0) == "ok"
     assert abi.kv_status_str(abi.KV_ERR_NO_BLOCKS) == "no free blocks"

@@ -176,7 +176,7 @@ def test_unknown_flags_are_refused():
     w, cache, alloc, ks, vs, bt, cl = _setup("f16", 1, 320)
     q = torch.from_numpy(W.host_queries(w)).cuda()
     with pytest.raises(abi.KvError):
-        cache.attention_ex(0, q, bt, cl, max(w.lens), w.scale, flags=8)
+        cache.attention_ex(0, q, bt, cl, max(w.lens), w.scale, flags=16)
     cache.close()
     alloc.close()
 
