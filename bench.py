@@ -355,30 +355,33 @@ def run_ours(args):
     # my kernels per layer: the attention kernel (one per 1024 sequences) [+ kv_append]
     launches_per_layer = (1 if args.unfused else 0) + 1 + (w.batch - 1) // 1024
 
+    def layer_call(l, ev=None):
+        if args.unfused:
+            cache.append(l, k_new[l], v_new[l], slots)
+        if ev is not None:
+            ev[l][0].record(stream)
+        if args.window or flags:
+            cache.attention_ex(l, q[l], bt, cl, max_ctx, w.scale, window=args.window,
+                               k_new=None if args.unfused else k_new[l],
+                               v_new=None if args.unfused else v_new[l], out=out[l],
+                               partition_tokens=args.partition, workspace=ws, flags=flags)
+        elif grouped:
+            cache.attention_gqa(l, q[l], bt, cl, max_ctx, w.scale,
+                                k_new=None if args.unfused else k_new[l],
+                                v_new=None if args.unfused else v_new[l], out=out[l],
+                                partition_tokens=args.partition, workspace=ws)
+        elif args.unfused:
+            cache.attention(l, q[l], bt, cl, max_ctx, w.scale, out=out[l],
+                            partition_tokens=args.partition, workspace=ws)
+        else:   # one launch: append each sequence's newest token, then attend
+            cache.attention_append(l, q[l], k_new[l], v_new[l], bt, cl, max_ctx, w.scale, out=out[l],
+                                   partition_tokens=args.partition, workspace=ws)
+        if ev is not None:
+            ev[l][1].record(stream)
+
     def step(ev=None):
         for l in range(L):
-            if args.unfused:
-                cache.append(l, k_new[l], v_new[l], slots)
-            if ev is not None:
-                ev[l][0].record(stream)
-            if args.window or flags:
-                cache.attention_ex(l, q[l], bt, cl, max_ctx, w.scale, window=args.window,
-                                   k_new=None if args.unfused else k_new[l],
-                                   v_new=None if args.unfused else v_new[l], out=out[l],
-                                   partition_tokens=args.partition, workspace=ws, flags=flags)
-            elif grouped:
-                cache.attention_gqa(l, q[l], bt, cl, max_ctx, w.scale,
-                                    k_new=None if args.unfused else k_new[l],
-                                    v_new=None if args.unfused else v_new[l], out=out[l],
-                                    partition_tokens=args.partition, workspace=ws)
-            elif args.unfused:
-                cache.attention(l, q[l], bt, cl, max_ctx, w.scale, out=out[l],
-                                partition_tokens=args.partition, workspace=ws)
-            else:   # one launch: append each sequence's newest token, then attend
-                cache.attention_append(l, q[l], k_new[l], v_new[l], bt, cl, max_ctx, w.scale, out=out[l],
-                                       partition_tokens=args.partition, workspace=ws)
-            if ev is not None:
-                ev[l][1].record(stream)
+            layer_call(l, ev)
 
     for _ in range(args.warmup):
         step()
@@ -424,18 +427,48 @@ def run_ours(args):
     h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "slots", "bt", "cl"))
     d2h = pin["out"].numel() * pin["out"].element_size()
 
+    # The step's copies overlap its layers: tables, lengths and the first `pre` layers'
+    # inputs go first on the compute stream; the other layers' inputs follow on a copy
+    # stream (layer `pre` waits for them), and the outputs return in chunks on the copy
+    # stream while later layers run (only the last layer's output is copied after it).
+    # Every event between two launches costs that pair its programmatic-dependent-launch
+    # overlap, so there are few: one wait for the inputs, two output chunks, one join.
+    copy_stream = torch.cuda.Stream(dev)
+    pre = min(L, 2)
+    marks = sorted({m for m in (L // 2 - 1, L - 2) if pre <= m < L - 1}) if L >= 4 else []
+    ev_start, ev_in, ev_join = (torch.cuda.Event() for _ in range(3))
+    ev_out = {m: torch.cuda.Event() for m in marks}
+
     def e2e_step():
-        q.copy_(pin["q"], non_blocking=True)
-        k_new.copy_(pin["k"], non_blocking=True)
-        v_new.copy_(pin["v"], non_blocking=True)
         slots.copy_(pin["slots"], non_blocking=True)
         bt.copy_(pin["bt"], non_blocking=True)
         cl.copy_(pin["cl"], non_blocking=True)
-        step()
-        pin["out"].copy_(out, non_blocking=True)
+        for dst, key in ((q, "q"), (k_new, "k"), (v_new, "v")):
+            dst[:pre].copy_(pin[key][:pre], non_blocking=True)
+        ev_start.record(stream)                     # the previous step is done with every buffer
+        copy_stream.wait_event(ev_start)
+        with torch.cuda.stream(copy_stream):
+            for dst, key in ((q, "q"), (k_new, "k"), (v_new, "v")):
+                dst[pre:].copy_(pin[key][pre:], non_blocking=True)
+            ev_in.record(copy_stream)
+        first = 0
+        for l in range(L):
+            if l == pre:
+                stream.wait_event(ev_in)
+            layer_call(l)
+            if l in ev_out:
+                ev_out[l].record(stream)
+                copy_stream.wait_event(ev_out[l])
+                with torch.cuda.stream(copy_stream):
+                    pin["out"][first:l + 1].copy_(out[first:l + 1], non_blocking=True)
+                first = l + 1
+        pin["out"][first:].copy_(out[first:], non_blocking=True)
+        ev_join.record(copy_stream)
+        stream.wait_event(ev_join)
 
     e2e_step()
     torch.cuda.synchronize()
+    pin["out"].fill_(float("nan"))                 # every output chunk must come back
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -444,6 +477,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    if not torch.equal(pin["out"], out.cpu()):
+        raise SystemExit("end-to-end step: the host copy of the outputs differs from the device's")
     err = cache.device_error()
     if err != 0:
         raise SystemExit(f"device error bits {err}")
