@@ -200,9 +200,14 @@ KV_API int kv_swap_in(kv_pool* pool, const void* host_src, const int32_t* blocks
 KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int max_context,
                                    int partition_tokens);
 
+/* Largest batch of one decode-attention call (every entry point); a larger batch is
+ * refused with KV_ERR_INVALID_ARG before anything is launched. */
+#define KV_MAX_DECODE_BATCH 65536
+
 /* out[s,h,:] = softmax(scale * q[s,h,:] . K_s^T) . V_s  over the first
  * context_lens[s] tokens of sequence s, for every sequence s and head h, read
- * through block_tables.  One query token per sequence (decode).
+ * through block_tables.  One query token per sequence (decode); batch 0 ..
+ * KV_MAX_DECODE_BATCH.
  *   q             device [batch][num_heads][head_dim]: float32 for F32 pools, float16
  *                 for F16 and FP8 pools; 16-byte aligned.
  *   out           device float32 [batch][num_heads][head_dim] (written, not accumulated).

@@ -123,9 +123,9 @@ template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_
 #endif
 
 // G_: query heads per KV head (grouped-query attention; 1 = one query per KV head).
-// MMA_: grouped-query tensor-core consumer (head_dim 128, G >= 2).  fp16 pools are fed by
-// swizzled tensor-map copies; FP8 pools by plain bulk copies, each tile dequantised to a
-// swizzled fp16 scratch in shared memory before the mma.
+// MMA_: grouped-query tensor-core consumer (head_dim 128, G >= 2).  Both pool types are fed
+// by 128-byte-swizzled tensor-map copies: fp16 tiles as [2][rows][64] halves, FP8 tiles as
+// [rows][128 codes], whose mma fragments are converted from the E4M3 codes in registers.
 // HP_ = 2 (one query per KV head only): a work item covers two adjacent heads.  Their
 // (block, head) tiles are adjacent in the pool, so one bulk copy brings both: half as many
 // copies per byte, which is what limits pools with small tiles (FP8, and fp16 with B = 8).
@@ -161,23 +161,19 @@ struct Cfg {
     static constexpr int ROW = D * ESZ;                   // bytes of one token row of one head
     static constexpr int KV_BYTES = CT * ROW * HP;        // bytes of K (or V) per chunk
     static constexpr int Q_BYTES = GE * D * sizeof(QT);   // the query rows of one item
-    static constexpr int SC_BYTES = 0;
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = KV_BYTES;
     static constexpr int Q_OFF = 2 * KV_BYTES;
     // the fp16 tensor-core path keeps its 1024-aligned stages to exactly K and V (8 KiB):
     // its query rows go to a region of their own, one slot per stage.  The FP8 tensor-core
-    // path reads its query rows from global memory once per item and keeps a per-warp fp16
-    // scratch (K, then V, of one chunk) instead.
+    // path reads its query rows from global memory once per item.
     static constexpr bool SWZ_STAGE = MMA && !FP8;        // stages hold swizzled tensor-map tiles
     // FP8 tensor-core path: K and V tiles arrive 128-byte swizzled through the layer's 2-D
     // tensor maps, and the mma fragments are built straight from the E4M3 codes
     static constexpr bool SWZ_K = MMA && FP8;
     static constexpr int Q_STAGE = MMA ? 0 : Q_BYTES;
     static constexpr int QR_BYTES = SWZ_STAGE ? Q_BYTES : 0;
-    static constexpr int SCR_BYTES = 0;
-    static constexpr int SC_OFF = Q_OFF + Q_STAGE;
-    static constexpr int STAGE = round_up(SC_OFF + SC_BYTES, (SWZ_STAGE || SWZ_K) ? 1024 : 128);
+    static constexpr int STAGE = round_up(Q_OFF + Q_STAGE, (SWZ_STAGE || SWZ_K) ? 1024 : 128);
     static constexpr int NC_AUTO = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
     // more query heads per warp need more registers: fewer consumer warps
 #if defined(KVP_MMA_NC)
@@ -190,7 +186,7 @@ struct Cfg {
                                            : (G == 2 ? 12 : (G == 4 ? 8 : 6));
     // stages that fit beside the prefix table and the barriers
     static constexpr int NSW_FIT =
-        (227 * 1024 - 2 * kMaxBatch * 4 - 1024 - (MMA ? 2048 : 0) - NC * SCR_BYTES) /
+        (227 * 1024 - 2 * kMaxBatch * 4 - 1024 - (MMA ? 2048 : 0)) /
         (NC * (STAGE + (int)sizeof(Meta) + QR_BYTES));
     static constexpr int NSW_CAP = (MMA && FP8) ? 6 : 4;   // FP8 stages are half as large
     static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > NSW_CAP ? NSW_CAP : NSW_FIT);
@@ -198,8 +194,7 @@ struct Cfg {
     static constexpr int THREADS = (NC + 1) * 32;
     static constexpr int META_R = NC * NSW * STAGE;                   // one Meta per stage
     static constexpr int QR_OFF = META_R + NC * NSW * (int)sizeof(Meta);   // MMA: one q slot per stage
-    static constexpr int SCR_OFF = round_up(QR_OFF + NC * NSW * QR_BYTES, 1024);   // FP8 MMA scratch
-    static constexpr int BAR_OFF = SCR_OFF + NC * SCR_BYTES;
+    static constexpr int BAR_OFF = round_up(QR_OFF + NC * NSW * QR_BYTES, 128);
     static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
     static constexpr int ZERO_OFF = PREFIX_OFF + 2 * kMaxBatch * 4;  // 128 zero bytes (FP8 mma: masked rows)
     static constexpr int MISC_OFF = ZERO_OFF + 128;             // launch-wide values (the partition size)
@@ -207,7 +202,7 @@ struct Cfg {
     static constexpr int SMEM = MISC_OFF + 16 + ALIGN_SLACK;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(NC <= 32 && (CT == 8 || CT == 16 || CT == 32), "launch shape");
-    static_assert(Q_OFF % 16 == 0 && SC_OFF % 16 == 0 && META_R % 16 == 0 && QR_OFF % 16 == 0, "alignment");
+    static_assert(Q_OFF % 16 == 0 && META_R % 16 == 0 && QR_OFF % 16 == 0, "alignment");
 };
 
 

@@ -81,6 +81,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
                    AttnPlan* plan, int group, int window) {
     const kv_pool_desc& d = pool->desc;
     if (batch < 0 || max_context < 0 || window < 0 || batch > kMaxBatch * kMaxSub) return KV_ERR_INVALID_ARG;
+    static_assert(kMaxBatch * kMaxSub == KV_MAX_DECODE_BATCH, "the documented batch limit");
     // a sliding window bounds the tokens read per sequence (window + up to 31 masked rows)
     const int span = (window > 0 && window + 32 < max_context) ? window + 32 : max_context;
     if (!valid_group(d, group)) return KV_ERR_INVALID_ARG;
