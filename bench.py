@@ -14,6 +14,7 @@ host cores instead (the benchmark's reference arm).
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -113,7 +114,10 @@ def traffic_record(kernel_srcs):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms; stop() keeps those taken between start() (after the
+    first sample has arrived) and stop(), by their timestamps, and falls back to all of
+    them when none falls inside."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -121,44 +125,56 @@ class ClockSampler:
         self.proc = None
         self.gpu = gpu_index
         self.path = os.path.join("/tmp", f"kvpaged_clocks_{os.getpid()}.csv")
+        self.t0 = 0.0
 
     def start(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            deadline = time.time() + 3.0         # the sampler is running before the region starts
+            while time.time() < deadline and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+        self.t0 = time.time()
 
     def stop(self):
         if self.proc is None:
             return None
+        t1 = time.time()
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = max(mx, float(parts[2]))
+                sm_mhz, max_mhz = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            active = {n for n, v in zip(names, parts[6:10]) if v.lower().startswith("active")}
+            rows.append((ts, sm_mhz, max_mhz, active))
         os.unlink(self.path)
-        if not sm:
+        inside = [r for r in rows if r[0] is not None and self.t0 - 0.06 <= r[0] <= t1 + 0.06]
+        rows = inside or rows
+        if not rows:
             return None
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        sm = sorted(r[1] for r in rows)
+        reasons = set().union(*(r[3] for r in rows))
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in rows), "reasons": sorted(reasons),
+                "samples": len(sm), "interval_ms": 50, "within_region": bool(inside)}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU)
