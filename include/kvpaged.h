@@ -196,7 +196,10 @@ KV_API int kv_swap_in(kv_pool* pool, const void* host_src, const int32_t* blocks
 /* ---------------------------------------------------------------- decode attention */
 
 /* Bytes of device workspace paged_decode_attention needs for these arguments
- * (0 on invalid arguments).  partition_tokens as in paged_decode_attention. */
+ * (0 on invalid arguments).  partition_tokens as in paged_decode_attention.  Arguments
+ * whose split-context work would exceed 2^30 items per launch of 1024 sequences
+ * (min(batch, 1024) x num_heads x ceil(max_context / partition)) are invalid here and in
+ * every decode entry point. */
 KV_API size_t paged_decode_workspace_size(const kv_pool* pool, int batch, int max_context,
                                    int partition_tokens);
 

@@ -150,6 +150,12 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     }
     const int pmin = plan->fine_from < batch ? plan->fine_partition : plan->alt_partition;
     plan->max_parts = span <= pmin ? 1 : (span + pmin - 1) / pmin;
+    // the kernel numbers a launch's work items with an int, and the workspace is sized in
+    // size_t: refuse sizes that would overflow either (about 10^9 items per launch, far
+    // beyond any pool a GPU holds)
+    const int64_t launch_items = static_cast<int64_t>(batch < kMaxBatch ? batch : kMaxBatch) *
+                                 d.num_heads * plan->max_parts;
+    if (launch_items > (int64_t{1} << 30)) return KV_ERR_INVALID_ARG;
     plan->consumers = nc;
     plan->group = group;
     plan->window = window;

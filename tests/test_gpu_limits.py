@@ -71,6 +71,14 @@ def test_largest_batch_and_the_first_refused():
     assert e.value.status == abi.KV_ERR_INVALID_ARG
     with pytest.raises(abi.KvError):                    # the size query answers 0
         abi.paged_decode_workspace_size(cache.handle, n + 1, 1, 0)
+    # split counts whose item numbers or workspace bytes would overflow are refused too
+    with pytest.raises(abi.KvError):
+        abi.paged_decode_workspace_size(cache.handle, n, 2 ** 31 - 1, 32)
+    with pytest.raises(abi.KvError) as e:
+        cache.attention(0, q1[:n], bt1[:n], cl1[:n], 2 ** 31 - 1, w.scale, out=out1[:n], partition_tokens=32,
+                        workspace=ws)
+    assert e.value.status == abi.KV_ERR_INVALID_ARG
+    assert abi.paged_decode_workspace_size(cache.handle, n, 2 ** 20, 32) > 0   # 2^25 items: fine
     torch.cuda.synchronize()
     assert bool(torch.all(out1 == 7.0))
     cache.close()
