@@ -222,10 +222,12 @@ def oracle_rate(w, units_total: int):
     busy = max(times)
     bytes_per_unit = n * w.head_dim * 2 * 2 + w.head_dim * 2 + w.head_dim * 4
     gbs = units_total * bytes_per_unit / busy / 1e9
+    # one process's own rate (single-threaded, while the other cores run theirs)
+    one_core = sum(p * bytes_per_unit / t for p, t in zip(per, times)) / len(per) / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": len(per), "kind": "oracle",
             "sample": f"{units_total} (sequence, head) units of context {n}, d {w.head_dim}, "
                       f"fp16 inputs widened to float64; numpy, one single-threaded process per core",
-            "seconds": busy, "wall_seconds": wall}
+            "one_core_value": one_core, "seconds": busy, "wall_seconds": wall}
 
 
 # ----------------------------------------------------------------------------- distributed
