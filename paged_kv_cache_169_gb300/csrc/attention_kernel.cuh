@@ -663,12 +663,13 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                                                     (real ? g : 0) * D * 2);
             #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                // FP8: k-index pairs (2t, 2t+1) and (2t+8, 2t+9) of k-step k stand for dims
-                // 16k+4t.. and 16k+4t+2.. (the order the K fragments are read in; a dot
-                // product is the same in any consistent order of its dims)
+                // FP8: k-index pairs (2t, 2t+1) and (2t+8, 2t+9) of k-step k = 4j + i stand
+                // for dims 32t+16j+4i.. and 32t+16j+4i+2.. (the order the K fragments are
+                // read in; a dot product is the same in any consistent order of its dims)
                 if constexpr (C::FP8) {
-                    qa[k][0] = real ? qrow[8 * k + 2 * t] : 0u;
-                    qa[k][1] = real ? qrow[8 * k + 2 * t + 1] : 0u;
+                    const int h2 = 16 * t + 8 * (k >> 2) + 2 * (k & 3);   // uint32 = 2 dims
+                    qa[k][0] = real ? qrow[h2] : 0u;
+                    qa[k][1] = real ? qrow[h2 + 1] : 0u;
                     continue;
                 }
                 qa[k][0] = real ? qrow[8 * k + t] : 0u;
@@ -747,18 +748,27 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 // S^T = K Q^T, the even and odd k-steps in two accumulators (shorter chains)
                 float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
                 // FP8: this lane's K rows t16 + g and t16 + g + 8 of the swizzled stage
-                // (both have row % 8 == g)
-                const char* kr0 = stg + C::K_OFF + (t16 + g) * C::ROW;
-                const char* kr1 = kr0 + 8 * C::ROW;
+                // (both have row % 8 == g): 16-byte pieces 2t and 2t+1 of each (dims
+                // 32t..32t+31), piece c sitting at c ^ g.  A quarter-warp reads rows g and
+                // g+1 (g even), whose pieces (2t+j)^g and (2t+j)^g^1 are 8 distinct ones:
+                // no bank conflicts.
+                uint4 kw[2][2];
+                if constexpr (C::FP8) {
+                    const char* kr0 = stg + C::K_OFF + (t16 + g) * C::ROW;
+                    #pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        kw[0][j] = *reinterpret_cast<const uint4*>(kr0 + (((2 * t + j) ^ g) << 4));
+                        kw[1][j] = *reinterpret_cast<const uint4*>(kr0 + 8 * C::ROW + (((2 * t + j) ^ g) << 4));
+                    }
+                }
                 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     uint32_t kf[4];
                     if constexpr (C::FP8) {
                         // A fragment straight from the E4M3 codes: the 4 codes of dims
-                        // 16k+4t.. of each row (16-byte piece k sits at k ^ g; no bank
-                        // conflicts: the 8 rows of a quarter-warp hit 8 distinct pieces)
-                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kr0 + (((k ^ g) << 4) | (4 * t)));
-                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kr1 + (((k ^ g) << 4) | (4 * t)));
+                        // 32t+16j+4i.. of each row (k = 4j + i)
+                        const uint32_t w0 = reinterpret_cast<const uint32_t*>(&kw[0][k >> 2])[k & 3];
+                        const uint32_t w1 = reinterpret_cast<const uint32_t*>(&kw[1][k >> 2])[k & 3];
                         kf[0] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w0 & 0xffffu));
                         kf[1] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w1 & 0xffffu));
                         kf[2] = e4m3x2_to_half2_bits(static_cast<uint16_t>(w0 >> 16));
