@@ -117,10 +117,10 @@ KV_API int kv_pool_get_desc(const kv_pool* pool, kv_pool_desc* desc);
  *   KV_FEATURE_TENSOR_MAPS  fp16 or FP8 pool with head_dim 128: every layer has
  *                           128-byte-swizzled tensor maps of its K and V pools, and
  *                           grouped-query decode (2, 4 or 8 query heads per KV head) runs
- *                           its scores and P V on the tensor cores (FP8: K fragments built
- *                           from the E4M3 codes, V tiles dequantised to fp16 in shared
- *                           memory).  Without it the same calls run on the CUDA cores with
- *                           identical semantics. */
+ *                           its scores and P V on the tensor cores (FP8: the K and V
+ *                           fragments are converted exactly from the E4M3 codes in
+ *                           registers).  Without it the same calls run on the CUDA cores
+ *                           with identical semantics. */
 #define KV_FEATURE_TENSOR_MAPS 1u
 KV_API int kv_pool_features(const kv_pool* pool, unsigned* flags);
 
