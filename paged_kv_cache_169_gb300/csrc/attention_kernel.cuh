@@ -597,14 +597,16 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Grouped-query consumer on the tensor cores (fp16, head_dim 128, G query heads per K/V
-// head).  Per 16-token chunk, with queries as the M dimension (G real rows of 16) and
-// tokens as N:
-//   S  = Q K^T        8 k-steps x 2 token tiles of mma.m16n8k16; K fragments by ldmatrix
-//   softmax           rows owned by the 4 lanes of a quad (lane/4 = query, lane%4 = tokens)
-//   O += P V          P re-used from the S accumulators as fp16 A fragments; V fragments
-//                     by ldmatrix.trans; 16 dim tiles of 8
-// fp32 accumulation and softmax, exact running max.
+// Grouped-query consumer on the tensor cores (fp16 or FP8 pools, head_dim 128, G query
+// heads per K/V head).  Per 16-token step, with the tokens (and output dims) as the M side
+// of mma.m16n8k16 and the query heads, padded to 8, as its N side:
+//   S^T  = K Q^T      8 k-steps over the 128 dims; K fragments by ldmatrix (fp16) or
+//                     converted from 16-byte reads of E4M3 codes (FP8)
+//   softmax           per query column (the 8 lanes of equal lane%4), in the log2 domain
+//   O^T += V^T P^T    P^T from the S accumulators by movmatrix.trans; V^T fragments by
+//                     ldmatrix.trans (fp16) or the 8-bit transposing ldmatrix (FP8);
+//                     8 output tiles of 16 dims
+// fp32 accumulation and softmax, exact running max (FP8: one update per 32-token chunk).
 template <typename C>
 __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, const int* s_ctx, int w, int lane,
                                              int P_eff) {
