@@ -11,14 +11,16 @@
 // block into shared memory and attends block by block; here the same idea is laid
 // out for sm_103a:
 //
-// * Work items are (sequence, head, partition) triples; a partition is P tokens
-//   (split-context, flash-decoding style).  Items are handed out dynamically with one
-//   atomic counter, so ragged batches balance.
+// * Work items are (sequence, head, partition) triples (a head pair or quad for pools
+//   with small tiles); a partition is at most P tokens (split-context, flash-decoding
+//   style).  Items are handed out dynamically with one atomic counter, so ragged
+//   batches balance.
 // * Each CTA is persistent (one per SM): warps 0..NC-1 are consumers, warp NC is the
 //   producer.  Producer lane w serves consumer w: it polls that consumer's ring without
 //   blocking, and for every physical block of the next CT-token chunk issues one 1-D
 //   bulk copy (cp.async.bulk, the TMA engine) of the contiguous (block, head) K tile
-//   and one of the V tile into the ring stage, completing on the stage's mbarrier.
+//   and one of the V tile into the ring stage, completing on the stage's mbarrier (the
+//   tensor-core consumer's tiles come through swizzling tensor-map copies instead).
 //   Block-table entries are fetched one chunk ahead, work items one item ahead.
 // * A consumer warp owns NSW ring stages.  Its two half-warps read two token rows per
 //   16-byte shared-memory load (lane: head_dim/16 dims of one row).  Each lane forms
@@ -33,7 +35,10 @@
 //   partitions with an atomic ticket; the warp that finishes the last one merges them
 //   (exact log-sum-exp merge) — no second kernel, and no warp ever waits for another.
 //
-// No tensor cores: one query row per head is a matrix-vector product bound by HBM.
+// One query row per head is a matrix-vector product bound by HBM: it runs on the CUDA
+// cores.  Grouped queries (G query heads per K/V head) make each K and V tile a small
+// dense contraction: for fp16 and FP8 pools with head_dim 128 it runs on the tensor
+// cores (consumer_mma below).
 
 #pragma once
 
