@@ -322,6 +322,16 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *                the kernel may read them, and the first block ids they point to, while
  *                that kernel is still finishing.  q, k_new, v_new, the pool, out and the
  *                workspace are still read and written only after it has completed.
+ *     KV_DECODE_EARLY_POOL  (with KV_DECODE_PDL and KV_DECODE_EARLY_TABLES; ignored
+ *                otherwise) the previous kernel on the stream writes no K/V pool row this
+ *                call reads, except each sequence's last two rows, context_len - 2 and
+ *                context_len - 1 (the token a fused decode step of the same layer appended
+ *                just before, and this call's own slot).  Then the first K/V tiles (whole
+ *                chunks below those rows) are fetched while that kernel is still
+ *                finishing.  True in a model's layer loop (the kernel before a layer's
+ *                attention does not write its pool) and in a loop of fused decode steps
+ *                over one layer; false right after kv_copy_blocks, kv_swap_in or kv_append
+ *                into rows this call reads.
  *     KV_DECODE_OUT_F16  out is float16 [batch][num_q_heads][head_dim] instead of float32:
  *                each element is the float32 result rounded to nearest even (beyond the
  *                float16 range: +-inf), as the attention output of [KV Cache篇] §3.1 is cast
@@ -333,6 +343,7 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
 #define KV_DECODE_PDL 2u
 #define KV_DECODE_EARLY_TABLES 4u
 #define KV_DECODE_OUT_F16 8u
+#define KV_DECODE_EARLY_POOL 16u
 typedef struct {
     int layer;
     const void* q;

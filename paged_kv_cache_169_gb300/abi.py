@@ -18,6 +18,7 @@ KV_F32, KV_F16, KV_FP8_E4M3 = 0, 1, 2
 KV_DEVERR_SLOT, KV_DEVERR_BLOCK_ID, KV_DEVERR_CONTEXT, KV_DEVERR_TIMEOUT = 1, 2, 4, 8
 KV_FEATURE_TENSOR_MAPS = 1
 KV_DECODE_WORKSPACE_ZEROED, KV_DECODE_PDL, KV_DECODE_EARLY_TABLES, KV_DECODE_OUT_F16 = 1, 2, 4, 8
+KV_DECODE_EARLY_POOL = 16
 KV_MAX_DECODE_BATCH = 65536
 
 

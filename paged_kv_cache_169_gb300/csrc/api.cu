@@ -360,7 +360,8 @@ int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* x) {
         }
     }
     if (!(x->scale > 0.f) || !(x->scale < 3.0e38f)) return KV_ERR_INVALID_ARG;
-    if (x->flags & ~(KV_DECODE_WORKSPACE_ZEROED | KV_DECODE_PDL | KV_DECODE_EARLY_TABLES | KV_DECODE_OUT_F16))
+    if (x->flags & ~(KV_DECODE_WORKSPACE_ZEROED | KV_DECODE_PDL | KV_DECODE_EARLY_TABLES | KV_DECODE_OUT_F16 |
+                     KV_DECODE_EARLY_POOL))
         return KV_ERR_INVALID_ARG;
     kvp::AttnPlan plan;
     int rc = kvp::plan_attention(pool, x->batch, x->max_context, x->partition_tokens, &plan, group, x->window);

@@ -75,6 +75,7 @@ struct AttnArgs {
     int P_fine, s_fine;    // sequences s >= s_fine split into partitions of P_fine tokens (< P)
     int P_alt;             // < P: use P_alt instead when it still gives at most one item per consumer warp
     int early_tables;      // lens and tables may be read before griddepcontrol.wait (KV_DECODE_EARLY_TABLES)
+    int early_pool;        // with early_tables: the first stages may be filled before it (KV_DECODE_EARLY_POOL)
     int out_f16;           // the result is stored as float16, rounded to nearest (KV_DECODE_OUT_F16)
     float qscale;          // scale * log2(e)
 };
@@ -1053,8 +1054,123 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             cur = decode(lane * gridDim.x + blockIdx.x);
             load_ids(cur, 0);
         }
+        // the query rows of cur, into stage st (they complete on that stage's barrier)
+        auto copy_q = [&](int st) {
+            const char* qsrc = static_cast<const char*>(a.q) + (static_cast<int64_t>(cur.s) * HU + cur.h) * C::Q_BYTES;
+            const uint32_t qdst = C::QR_BYTES ? smem_u32(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES)
+                                              : smem_u32(stage_ptr(w, st)) + C::Q_OFF;
+            bulk_g2s(qdst, qsrc, C::Q_BYTES, full_bar(w, st));
+        };
+        // Fill stage st with chunk c of cur (or the end marker) and advance.  pre: before
+        // griddepcontrol.wait (KV_DECODE_EARLY_POOL): K and V tiles only, the query copy
+        // is left to q_stage and no item is claimed.
+        int q_stage = -1;
+        auto fill = [&](int st, bool pre) {
+            char* stg = stage_ptr(w, st);
+            Meta* meta = reinterpret_cast<Meta*>(smem + C::META_R + (w * NSW + st) * sizeof(Meta));
+            const uint32_t fb = full_bar(w, st);
+            if (!cur.valid) {
+                meta->flags = F_TERM;
+                mbar_arrive(fb);
+                alive = false;
+            } else {
+                const int nt = min(CT, cur.ntok - c * CT);     // 0 only for an empty sequence
+                const int nblk = nt > 0 ? (nt + rpc - 1) / rpc : 0;   // copies of this chunk
+                const int row0 = (cur.tok0 + c * CT) % a.B;   // first row inside the block
+                #pragma unroll
+                for (int j = 0; j < CBMAX; ++j) {
+                    if (j < nblk && (ids[j] < 0 || ids[j] >= a.num_blocks)) {
+                        atomicOr(a.err, KV_DEVERR_BLOCK_ID);
+                        ids[j] = 0;
+                    }
+                }
+                const bool with_q = (c == 0) && nt > 0 && (C::Q_STAGE > 0 || C::QR_BYTES > 0);
+                const uint32_t bytes = nblk * 2 * tile + (with_q ? C::Q_BYTES : 0);
+                meta->s = cur.s;
+                meta->h = cur.h;
+                meta->p = cur.p;
+                meta->ntok = nt;
+                meta->lo = c == 0 ? cur.lo : 0;
+                // fused append: the sequence's newest token is the last row of the
+                // last chunk of its last partition
+                const bool patch = a.k_new != nullptr && cur.last && c == cur.nchunks - 1 && nt > 0;
+                meta->flags = (c == 0 ? F_FIRST : 0) | (c == cur.nchunks - 1 ? F_LAST : 0) |
+                              (cur.single ? F_SINGLE : 0) | (patch ? F_PATCH : 0);
+                if (patch) {
+                    const int r = nt - 1, jr = r / rpc;
+                    int pid = ids[0];
+                    #pragma unroll
+                    for (int j = 1; j < CBMAX; ++j) if (j == jr) pid = ids[j];
+                    meta->patch_row = r;
+                    meta->patch_id = pid;
+                    meta->patch_off = row0 + r % rpc;
+                }
+                #pragma unroll
+                for (int j = 0; j < CBMAX; ++j) meta->ids[j] = ids[j];
+                if (bytes) mbar_arrive_expect_tx(fb, bytes);
+                else mbar_arrive(fb);
+                const uint32_t dst = smem_u32(stg);
+                #pragma unroll
+                for (int j = 0; j < CBMAX; ++j) {
+                    if (j < nblk) {
+                        const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h * C::HP) * a.B +
+                                              row0) * C::ROW;
+                        if constexpr (C::SWZ_STAGE) {
+                            // rpc token rows of one head as [2][rows][64], 128-byte swizzled
+                            const int row = static_cast<int>(toff / C::ROW);
+                            tma_load_3d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, 0, fb);
+                            tma_load_3d(dst + C::V_OFF + j * tile, &a.vmap, 0, row, 0, fb);
+                        } else if constexpr (C::SWZ_K) {
+                            // rpc rows of 128 codes each, 128-byte swizzled
+                            const int row = static_cast<int>(toff / C::ROW);
+                            tma_load_2d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, fb);
+                            tma_load_2d(dst + C::V_OFF + j * tile, &a.vmap, 0, row, fb);
+                        } else {
+                            bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
+                            bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
+                        }
+                    }
+                }
+                if (with_q) {
+                    if (pre) q_stage = st;                // copied once the wait has returned
+                    else copy_q(st);
+                }
+                if (pre) {                                // never the item's last chunk: no claim
+                    ++c;
+                    load_ids(cur, c);
+                    return;
+                }
+                const int rem = cur.nchunks - 1 - c;      // chunks of cur still to fill
+                if (rem <= kClaimLead && !claimed) claim();
+                if (rem == 0) {
+                    if (!claimed) claim();
+                    cur = decode(pending);
+                    claimed = false;
+                    c = 0;
+                    if (cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
+                } else {
+                    ++c;
+                }
+                load_ids(cur, c);                  // used at this lane's next fill
+            }
+        };
+        // KV_DECODE_EARLY_POOL: the previous kernel on the stream writes no pool row this
+        // launch reads except each sequence's last two (context_len - 2: the token the
+        // previous decode step appended; context_len - 1: this call's slot), so the first
+        // stages of every lane's first item may be filled before the wait: up to NSW full
+        // chunks lying wholly below those rows, never the item's last chunk (which would
+        // need a claim).
+        if (a.early_pool) {
+            for (int k = 0; k < NSW; ++k) {
+                if (mine && cur.valid && c < cur.nchunks - 1 && cur.tok0 + (c + 1) * CT <= s_ctx[cur.s] - 2) {
+                    fill(fills % NSW, true);
+                    ++fills;
+                }
+            }
+        }
         if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (mine && cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
+        if (q_stage >= 0) copy_q(q_stage);
+        if (mine && cur.valid && cur.nchunks - 1 - c <= kClaimLead) claim();
         bool failed = false;
         uint64_t idle_since = 0;
         while (__any_sync(FULL, alive) && !failed) {
@@ -1062,91 +1178,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             bool ready = false;
             if (alive) ready = mbar_test_wait(empty_bar(w, st), ((fills / NSW) & 1) ^ 1);
             if (ready) {
-                char* stg = stage_ptr(w, st);
-                Meta* meta = reinterpret_cast<Meta*>(smem + C::META_R + (w * NSW + st) * sizeof(Meta));
-                const uint32_t fb = full_bar(w, st);
-                if (!cur.valid) {
-                    meta->flags = F_TERM;
-                    mbar_arrive(fb);
-                    alive = false;
-                } else {
-                    const int nt = min(CT, cur.ntok - c * CT);     // 0 only for an empty sequence
-                    const int nblk = nt > 0 ? (nt + rpc - 1) / rpc : 0;   // copies of this chunk
-                    const int row0 = (cur.tok0 + c * CT) % a.B;   // first row inside the block
-                    #pragma unroll
-                    for (int j = 0; j < CBMAX; ++j) {
-                        if (j < nblk && (ids[j] < 0 || ids[j] >= a.num_blocks)) {
-                            atomicOr(a.err, KV_DEVERR_BLOCK_ID);
-                            ids[j] = 0;
-                        }
-                    }
-                    const bool with_q = (c == 0) && nt > 0 && (C::Q_STAGE > 0 || C::QR_BYTES > 0);
-                    const uint32_t bytes = nblk * 2 * tile + (with_q ? C::Q_BYTES : 0);
-                    meta->s = cur.s;
-                    meta->h = cur.h;
-                    meta->p = cur.p;
-                    meta->ntok = nt;
-                    meta->lo = c == 0 ? cur.lo : 0;
-                    // fused append: the sequence's newest token is the last row of the
-                    // last chunk of its last partition
-                    const bool patch = a.k_new != nullptr && cur.last && c == cur.nchunks - 1 && nt > 0;
-                    meta->flags = (c == 0 ? F_FIRST : 0) | (c == cur.nchunks - 1 ? F_LAST : 0) |
-                                  (cur.single ? F_SINGLE : 0) | (patch ? F_PATCH : 0);
-                    if (patch) {
-                        const int r = nt - 1, jr = r / rpc;
-                        int pid = ids[0];
-                        #pragma unroll
-                        for (int j = 1; j < CBMAX; ++j) if (j == jr) pid = ids[j];
-                        meta->patch_row = r;
-                        meta->patch_id = pid;
-                        meta->patch_off = row0 + r % rpc;
-                    }
-                    #pragma unroll
-                    for (int j = 0; j < CBMAX; ++j) meta->ids[j] = ids[j];
-                    if (bytes) mbar_arrive_expect_tx(fb, bytes);
-                    else mbar_arrive(fb);
-                    const uint32_t dst = smem_u32(stg);
-                    #pragma unroll
-                    for (int j = 0; j < CBMAX; ++j) {
-                        if (j < nblk) {
-                            const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h * C::HP) * a.B +
-                                                  row0) * C::ROW;
-                            if constexpr (C::SWZ_STAGE) {
-                                // rpc token rows of one head as [2][rows][64], 128-byte swizzled
-                                const int row = static_cast<int>(toff / C::ROW);
-                                tma_load_3d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, 0, fb);
-                                tma_load_3d(dst + C::V_OFF + j * tile, &a.vmap, 0, row, 0, fb);
-                            } else if constexpr (C::SWZ_K) {
-                                // rpc rows of 128 codes each, 128-byte swizzled
-                                const int row = static_cast<int>(toff / C::ROW);
-                                tma_load_2d(dst + C::K_OFF + j * tile, &a.kmap, 0, row, fb);
-                                tma_load_2d(dst + C::V_OFF + j * tile, &a.vmap, 0, row, fb);
-                            } else {
-                                bulk_g2s(dst + C::K_OFF + j * tile, a.kpool + toff, tile, fb);
-                                bulk_g2s(dst + C::V_OFF + j * tile, a.vpool + toff, tile, fb);
-                            }
-                        }
-                    }
-                    if (with_q) {
-                        const char* qsrc = static_cast<const char*>(a.q) +
-                                           (static_cast<int64_t>(cur.s) * HU + cur.h) * C::Q_BYTES;
-                        const uint32_t qdst = C::QR_BYTES ? smem_u32(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES)
-                                                          : dst + C::Q_OFF;
-                        bulk_g2s(qdst, qsrc, C::Q_BYTES, fb);
-                    }
-                    const int rem = cur.nchunks - 1 - c;      // chunks of cur still to fill
-                    if (rem <= kClaimLead && !claimed) claim();
-                    if (rem == 0) {
-                        if (!claimed) claim();
-                        cur = decode(pending);
-                        claimed = false;
-                        c = 0;
-                        if (cur.valid && cur.nchunks - 1 <= kClaimLead) claim();
-                    } else {
-                        ++c;
-                    }
-                    load_ids(cur, c);                  // used at this lane's next fill
-                }
+                fill(st, false);
                 ++fills;
             }
             // watchdog: no stage became free anywhere for about a second -> give up

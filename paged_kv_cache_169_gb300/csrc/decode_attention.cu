@@ -227,6 +227,7 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     a.P = plan.partition;
     a.early_tables = (plan.flags & KV_DECODE_PDL) && (plan.flags & KV_DECODE_EARLY_TABLES) ? 1 : 0;
     a.out_f16 = (plan.flags & KV_DECODE_OUT_F16) ? 1 : 0;
+    a.early_pool = a.early_tables && (plan.flags & KV_DECODE_EARLY_POOL) ? 1 : 0;
     a.P_fine = plan.fine_partition;
     a.P_alt = plan.alt_partition;
     a.s_fine = plan.fine_from;

@@ -43,12 +43,12 @@ def test_header_constants_match_the_binding():
     text = open(HEADER, encoding="utf-8").read()
     defs = dict(re.findall(r"^#define\s+(KV_[A-Z0-9_]+)\s+\(?(-?\d+)u?\)?\s*$", text, flags=re.M))
     assert {"KV_DECODE_WORKSPACE_ZEROED", "KV_DECODE_PDL", "KV_DECODE_EARLY_TABLES",
-            "KV_DECODE_OUT_F16"} <= set(defs)
+            "KV_DECODE_OUT_F16", "KV_DECODE_EARLY_POOL"} <= set(defs)
     for name, value in defs.items():
         if hasattr(abi, name):
             assert getattr(abi, name) == int(value), name
     flags = [int(defs[n]) for n in defs if n.startswith("KV_DECODE_")]
-    assert sum(flags) == 15 and all(f & (f - 1) == 0 for f in flags)   # distinct bits
+    assert sum(flags) == 31 and all(f & (f - 1) == 0 for f in flags)   # distinct bits
 
 
 def test_status_strings(lib):

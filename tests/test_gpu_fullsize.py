@@ -6,9 +6,10 @@ kernel output); the oracle reads the sampled tiles back before the decode append
 adds the new token itself.  The benchmark's call: one paged_decode_attention_ex per
 layer that appends each sequence's new token and attends, library-chosen partitioning,
 a workspace zero-filled once and kept over all calls (KV_DECODE_WORKSPACE_ZEROED),
-programmatic dependent launch (KV_DECODE_PDL) and tables read before the previous launch
-ends (KV_DECODE_EARLY_TABLES: they are written before the layer loop).  The 13B step also runs as kv_append
-followed by paged_decode_attention.
+programmatic dependent launch (KV_DECODE_PDL), tables read before the previous launch
+ends (KV_DECODE_EARLY_TABLES: they are written before the layer loop) and the first K/V
+tiles fetched before it ends (KV_DECODE_EARLY_POOL: the previous launch wrote another
+layer's pool).  The 13B step also runs as kv_append followed by paged_decode_attention.
 """
 
 import numpy as np
@@ -24,7 +25,8 @@ from paged_kv_cache_169_gb300.cache import PagedKVCache
 
 pytestmark = pytest.mark.gpu
 
-BENCH_FLAGS = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL | abi.KV_DECODE_EARLY_TABLES
+BENCH_FLAGS = (abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL | abi.KV_DECODE_EARLY_TABLES |
+               abi.KV_DECODE_EARLY_POOL)
 
 
 def _snapshot(pool: torch.Tensor, table_row, n_blocks: int, h: int) -> np.ndarray:

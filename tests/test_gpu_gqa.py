@@ -146,12 +146,12 @@ def test_gqa70b_full_size_layer_sampled():
     q = W.host_queries(w, 0, l)
     k_new, v_new = W.host_step_tokens(w, 0, l, "k"), W.host_step_tokens(w, 0, l, "v")
     # the benchmark's call: every option in one argument block, a workspace zero-filled
-    # once, programmatic dependent launch
+    # once, programmatic dependent launch, early tables and early K/V tiles
     ws = cache.zeroed_workspace(w.batch, max(w.lens), num_q_heads=Hq)
     out = cache.attention_ex(l, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale,
                              k_new=torch.from_numpy(k_new).cuda(), v_new=torch.from_numpy(v_new).cuda(),
                              workspace=ws, flags=abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL |
-                             abi.KV_DECODE_EARLY_TABLES)
+                             abi.KV_DECODE_EARLY_TABLES | abi.KV_DECODE_EARLY_POOL)
     out = out.cpu().numpy()
     worst = 0.0
     for (s, j) in samples:

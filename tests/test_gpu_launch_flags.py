@@ -26,6 +26,7 @@ from paged_kv_cache_169_gb300.cache import BlockAllocator, PagedKVCache
 pytestmark = pytest.mark.gpu
 
 ZEROED, PDL, EARLY = abi.KV_DECODE_WORKSPACE_ZEROED, abi.KV_DECODE_PDL, abi.KV_DECODE_EARLY_TABLES
+EARLY_POOL = abi.KV_DECODE_EARLY_POOL
 COUNTER_BYTES = 512          # work and exit counters at the start of every workspace
 MERGE_FAN = 16               # partitions folded per group in a two-level merge
 
@@ -134,10 +135,12 @@ def _decode_loop_case(G):
 
 @pytest.mark.parametrize("G", [1, 8])
 @pytest.mark.parametrize("graph", [False, True])
-@pytest.mark.parametrize("early", [False, True])
+@pytest.mark.parametrize("early", [0, EARLY, EARLY | EARLY_POOL])
 def test_pdl_back_to_back_fused_steps(G, graph, early):
     """early: KV_DECODE_EARLY_TABLES as well (every step's tables and lengths are written
-    before the loop, so each launch may read them before the previous launch ends)."""
+    before the loop, so each launch may read them before the previous launch ends), and
+    KV_DECODE_EARLY_POOL (each launch fetches its first K/V tiles while the previous step,
+    which appended row context_len - 2 of every sequence of this same layer, finishes)."""
     w, cache, alloc, max_ctx, tabs, lens, qs, kn, vn, want = _decode_loop_case(G)
     steps = len(qs)
     P = 128     # several partitions per sequence: merges run in every launch
@@ -151,7 +154,7 @@ def test_pdl_back_to_back_fused_steps(G, graph, early):
         for i in range(steps):
             cache.attention_ex(0, qs[i], tabs[i], lens[i], max_ctx, w.scale, k_new=kn[i], v_new=vn[i],
                                out=outs[i], partition_tokens=P, workspace=ws, stream=stream,
-                               flags=ZEROED | PDL | (EARLY if early else 0))
+                               flags=ZEROED | PDL | early)
 
     if graph:
         g = torch.cuda.CUDAGraph()
@@ -176,7 +179,7 @@ def test_unknown_flags_are_refused():
     w, cache, alloc, ks, vs, bt, cl = _setup("f16", 1, 320)
     q = torch.from_numpy(W.host_queries(w)).cuda()
     with pytest.raises(abi.KvError):
-        cache.attention_ex(0, q, bt, cl, max(w.lens), w.scale, flags=16)
+        cache.attention_ex(0, q, bt, cl, max(w.lens), w.scale, flags=32)
     cache.close()
     alloc.close()
 

@@ -97,9 +97,9 @@ def test_f16_output_is_the_f32_result_rounded(dtype, d, B, H, G):
 
 @pytest.mark.parametrize("dtype,B,H,G", [("fp8", 8, 4, 1), ("f16", 16, 2, 8), ("f16", 16, 4, 1)])
 def test_f16_output_with_fused_append_window_and_launch_flags(dtype, B, H, G):
-    """The benchmark's call (fused append, zeroed workspace, PDL, early tables) with a
-    sliding window, float16 result: equal to the float32 call's, rounded, and to the
-    oracle over the window."""
+    """The benchmark's call (fused append, zeroed workspace, PDL, early tables and K/V
+    tiles) with a sliding window, float16 result: equal to the float32 call's, rounded,
+    and to the oracle over the window."""
     d, window = 128, 256
     lens = [1, 9, 255, 257, 700, 2049]
     nb = sum(-(-n // B) for n in lens) + 4
@@ -118,7 +118,8 @@ def test_f16_output_with_fused_append_window_and_launch_flags(dtype, B, H, G):
     q = torch.from_numpy(qh).cuda()
     k_new = torch.from_numpy(np.stack([k[-1] for k in ks])).cuda()
     v_new = torch.from_numpy(np.stack([v[-1] for v in vs])).cuda()
-    flags = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL | abi.KV_DECODE_EARLY_TABLES
+    flags = (abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL | abi.KV_DECODE_EARLY_TABLES |
+             abi.KV_DECODE_EARLY_POOL)
     ws = cache.zeroed_workspace(len(lens), max(lens), num_q_heads=G * H, window=window)
     kw = dict(window=window, k_new=k_new, v_new=v_new, workspace=ws, flags=flags)
     o32 = cache.attention_ex(0, q, bt, cl, max(lens), w.scale, **kw)

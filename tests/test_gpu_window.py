@@ -92,11 +92,12 @@ def test_window_with_fused_append(dtype, B, G):
 
 @pytest.mark.parametrize("dtype,B,G", [("f16", 16, 1), ("fp8", 16, 1), ("fp8", 16, 8), ("f16", 8, 4)])
 def test_window_with_fused_append_and_all_launch_flags(dtype, B, G):
-    """The window, the fused append and the three launch flags together, twice in a row
+    """The window, the fused append and the four launch flags together, twice in a row
     on one zero-filled workspace (the second call rewrites the same slots)."""
     from paged_kv_cache_169_gb300 import abi
     cache, q, bt, cl, kn, vn, want, _, w = _case(dtype, B, G, 100, 151 + G, fused=True)
-    flags = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL | abi.KV_DECODE_EARLY_TABLES
+    flags = (abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL | abi.KV_DECODE_EARLY_TABLES |
+             abi.KV_DECODE_EARLY_POOL)
     ws = cache.zeroed_workspace(w.batch, max(w.lens), 0, num_q_heads=w.q_heads, window=100)
     for _ in range(2):
         out = cache.attention_ex(0, torch.from_numpy(q).cuda(), bt, cl, max(w.lens), w.scale, window=100,
