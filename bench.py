@@ -3,8 +3,9 @@
 Default workload: the LLaMA-13B-shaped full decode step — 40 layers x one fused call
 (paged_decode_attention_ex: append the new token of each of 48 sequences, then attend
 over 48 sequences x 40 heads x 2048 tokens, d 128, fp16 K/V, block size 16), with a
-workspace zero-filled once, programmatic dependent launch and early tables (the three
-launch flags; ``--launch-flags`` and ``--unfused`` select the other forms).  The pool is
+workspace zero-filled once, programmatic dependent launch, early tables and early K/V
+tiles (the four launch flags; ``--launch-flags`` and ``--unfused`` select the other
+forms).  The pool is
 ~75 GiB, far larger than L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 oracle on the
@@ -27,7 +28,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak); seq-steps/s"
-# kv_decode_args.flags: KV_DECODE_WORKSPACE_ZEROED = 1, KV_DECODE_PDL = 2, KV_DECODE_EARLY_TABLES = 4
+# kv_decode_args.flags: KV_DECODE_WORKSPACE_ZEROED = 1, KV_DECODE_PDL = 2, KV_DECODE_EARLY_TABLES = 4,
+# KV_DECODE_EARLY_POOL = 16
 LAUNCH_FLAGS = {"none": 0, "zeroed": 1, "pdl": 3, "early": 7, "earlypool": 23}
 FALLBACK_HBM_GBS = 6800.0
 
