@@ -187,8 +187,9 @@ def test_unknown_flags_are_refused():
 def test_flags_over_several_launches_with_head_pairs_and_fp8():
     """2100 sequences (three launches of at most 1024), FP8 pool with B 16 and 2 heads
     (head-pair items), fused append, 32-token partitions (a few long sequences merge in
-    two levels), KV_DECODE_WORKSPACE_ZEROED | KV_DECODE_PDL, two calls in a row on one
-    zeroed workspace: every launch's counters start and end at zero."""
+    two levels), KV_DECODE_WORKSPACE_ZEROED | KV_DECODE_PDL, three calls in a row on one
+    zeroed workspace (the later ones with early tables, then early K/V tiles too): every
+    launch's counters start and end at zero."""
     B, H, d = 16, 2, 128
     rng = np.random.default_rng(21)
     lens = rng.integers(0, 70, 2100).tolist()
@@ -217,11 +218,11 @@ def test_flags_over_several_launches_with_head_pairs_and_fp8():
     vsd = [OF.decode(OF.quantize(v, sc)) * float(sc) for v in vs]
     P = 32
     ws = cache.zeroed_workspace(w.batch, max(lens), P)
-    for call in range(2):
+    for call, extra in enumerate((0, EARLY, EARLY | EARLY_POOL)):
         q = W.host_queries(w, call)
-        # the second call appends the same token again into the same slot (same bytes)
+        # later calls append the same token again into the same slot (same bytes)
         out = cache.attention_ex(0, torch.from_numpy(q).cuda(), bt, cl, max(lens), w.scale, k_new=kn, v_new=vn,
-                                 partition_tokens=P, workspace=ws, flags=ZEROED | PDL | (EARLY if call else 0))
+                                 partition_tokens=P, workspace=ws, flags=ZEROED | PDL | extra)
         err = max_abs(out.cpu().numpy(), OA.decode_attention(q, ksd, vsd, w.scale))
         assert err <= tol_for("f16"), (call, err)
     assert cache.device_error() == 0
