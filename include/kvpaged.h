@@ -299,7 +299,7 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *                rolling-window cache of [KV缓存机制解析] §8 keeps the most recent tokens.
  *                Blocks lying wholly before position context_len - W are never read, so the
  *                host may release them (kv_alloc_seq_trim) and leave their table entries -1.
- *   flags        0, or a sum of:
+ *   flags        0, or a sum of the bits below (any other bit: KV_ERR_INVALID_ARG):
  *     KV_DECODE_WORKSPACE_ZEROED  the workspace's counters are already zero, so the call
  *                does not clear them (one cudaMemsetAsync less per call).  True for a
  *                workspace zero-filled once after allocation and used since only by decode
@@ -313,15 +313,16 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *     KV_DECODE_PDL  launch with programmatic dependent launch: the kernel may be scheduled
  *                while the previous kernel on the stream is still finishing; it reads no
  *                global memory (inputs, pool or workspace) before that kernel has completed
- *                and its writes are visible.  Saves the launch gap between back-to-back
+ *                and its writes are visible, except as the two EARLY flags below allow.  Saves the launch gap between back-to-back
  *                kernels (with KV_DECODE_WORKSPACE_ZEROED no clearing copy sits between
  *                two consecutive decode calls).  Also valid inside stream capture.
  *     KV_DECODE_EARLY_TABLES  (with KV_DECODE_PDL; ignored without it) context_lens and
  *                block_tables were written before the previous kernel on the stream
  *                started (for instance host copies issued before a step's layer loop), so
  *                the kernel may read them, and the first block ids they point to, while
- *                that kernel is still finishing.  q, k_new, v_new, the pool, out and the
- *                workspace are still read and written only after it has completed.
+ *                that kernel is still finishing.  q, k_new, v_new, out and the workspace
+ *                are still read and written only after it has completed (the pool too,
+ *                unless KV_DECODE_EARLY_POOL).
  *     KV_DECODE_EARLY_POOL  (with KV_DECODE_PDL and KV_DECODE_EARLY_TABLES; ignored
  *                otherwise) the previous kernel on the stream writes no K/V pool row this
  *                call reads, except each sequence's last two rows, context_len - 2 and
