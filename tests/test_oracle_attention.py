@@ -245,22 +245,39 @@ def test_matches_torch_sdpa_float64():
 
 
 def test_fp8_paged_dequantises_with_block_scale():
-    """FP8 pool: element value = decode(code) * scale[physical block]."""
+    """FP8 pool: element value = decode(code) * scale[physical block].  Pinned through an
+    independent route: torch's own float8_e4m3fn type widens the codes, torch indexing
+    picks each token's block and block scale, and torch's float64 SDPA attends.  The
+    scales differ per block (K and V too) and the table is permuted, so a scale taken by
+    logical block, or K's scale used for V, fails; unused slots hold the NaN code."""
     from oracle import fp8
     rng = np.random.default_rng(400)
     B, H, d, nb = 4, 2, 8, 6
-    codes_k = rng.integers(0, 0x7E, (nb, H, B, d), dtype=np.uint8)
-    codes_v = rng.integers(0, 0x7E, (nb, H, B, d), dtype=np.uint8)
-    ks = rng.uniform(0.01, 2.0, nb)
-    vs = rng.uniform(0.01, 2.0, nb)
+    # codes of magnitudes below 2 (exponent field <= 7) and both signs: with block scales
+    # in [0.25, 2] the softmax weights stay spread, so every scale matters
+    sign = lambda: (rng.integers(0, 2, (nb, H, B, d)) << 7).astype(np.uint8)
+    codes_k = rng.integers(0, 0x40, (nb, H, B, d), dtype=np.uint8) | sign()
+    codes_v = rng.integers(0, 0x40, (nb, H, B, d), dtype=np.uint8) | sign()
+    ks = rng.uniform(0.25, 2.0, nb)
+    vs = rng.uniform(0.25, 2.0, nb)
     table = np.array([[4, 0, 2]])
-    n = 10
+    n = 10                                                  # block 2 holds 2 of its 4 slots
+    codes_k[2, :, 2:] = 0x7F
+    codes_v[2, :, 2:] = 0x7F
     q = rng.standard_normal((1, H, d))
     got = A.paged_decode_attention(q, codes_k, codes_v, table, [n], 0.3, B, ks, vs, fp8.decode)
-    K = np.stack([fp8.decode(codes_k[table[0, t // B], :, t % B]) * ks[table[0, t // B]] for t in range(n)])
-    V = np.stack([fp8.decode(codes_v[table[0, t // B], :, t % B]) * vs[table[0, t // B]] for t in range(n)])
-    want = A.decode_attention(q, [K], [V], 0.3)
-    np.testing.assert_allclose(got, want, rtol=0, atol=0)
+    assert np.all(np.isfinite(got))
+
+    def widened(codes, scale):                              # [n, H, d] float64, torch only
+        t = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64)
+        tok = torch.arange(n)
+        phys = torch.from_numpy(table[0])[tok // B]
+        return t[phys, :, tok % B, :] * torch.from_numpy(scale)[phys].view(n, 1, 1)
+
+    K, V = widened(codes_k, ks), widened(codes_v, vs)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q[0]).view(H, 1, d), K.permute(1, 0, 2), V.permute(1, 0, 2), scale=0.3).view(H, d)
+    np.testing.assert_allclose(got[0], ref.numpy(), rtol=0, atol=1e-13)
 
 
 # ---------------------------------------------------------------- grouped-query attention
