@@ -386,7 +386,13 @@ KV_API int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* args);
  * file-scope device array of KV_STATIC_SCRATCH_BYTES that every GPU loading the library
  * holds until the process exits.
  *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current); make that first call before any stream capture.  The
+ *     address belongs to the device's context: the first call after cudaDeviceReset
+ *     replaced that context looks it up again (so does every call if the context's id
+ *     cannot be read).
+ *   - It runs the plain call only: no launch flags (no programmatic dependent launch, no
+ *     early tables or tiles, float32 output), and there is no fused-append, grouped-query
+ *     or sliding-window form of it.
  *   - The pool's device must be the current device (else KV_ERR_INVALID_ARG).
  *   - If the scratch these arguments need (paged_decode_workspace_size) exceeds
  *     KV_STATIC_SCRATCH_BYTES the call is refused with KV_ERR_INVALID_ARG and nothing

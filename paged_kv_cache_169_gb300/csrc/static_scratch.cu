@@ -25,17 +25,57 @@ static __device__ __align__(256) unsigned char kv_static_scratch[KV_STATIC_SCRAT
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};   // context the address belongs to
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Process-unique id of the current context, 0 if it cannot be read.  A context created
+// after cudaDeviceReset gets a new id, so an address looked up in the old one is never
+// reused.  The two driver entry points are fetched on the first call (with g_scratch_mu held).
+unsigned long long current_context_id() {
+    static bool tried = false;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (!tried) {
+        tried = true;
+        void* f0 = nullptr;
+        void* f1 = nullptr;
+        cudaDriverEntryPointQueryResult q0, q1;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 12000, cudaEnableDefault, &q0) == cudaSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+            q0 == cudaDriverEntryPointSuccess && q1 == cudaDriverEntryPointSuccess && f0 && f1) {
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f0);
+            get_id = reinterpret_cast<CtxGetIdFn>(f1);
+        } else {
+            cudaGetLastError();
+        }
+    }
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 // Device address of the scratch array on the current device `dev`.  In host code the
 // name kv_static_scratch is only a host-side stand-in, so the address must come from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, with that device current.  It is looked up once per device and
+// context: on the first call on a device, and again on the first call after the device's
+// context was replaced (cudaDeviceReset), or on every call if the context id cannot be read.
 int scratch_address(int dev, void** out) {
     if (dev < 0 || dev >= kMaxDevices) return KV_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, kv_static_scratch) != cudaSuccess || !p) return KV_ERR_CUDA;
+        if (cudaGetSymbolAddress(&p, kv_static_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            g_scratch_ptr[dev] = nullptr;
+            return KV_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return KV_OK;
