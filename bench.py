@@ -623,6 +623,14 @@ def run_swap(args):
 
 
 
+def abi_workspace_bytes(cache, batch, max_ctx, partition, prefix_groups):
+    from paged_kv_cache_169_gb300 import abi
+    a = abi.kv_decode_args()
+    a.batch, a.max_context, a.partition_tokens = batch, max_ctx, partition
+    a.num_prefix_groups = 1 if prefix_groups else 0
+    return abi.paged_decode_workspace_size_ex(cache.handle, a)
+
+
 def _flush_l2(buf):
     buf.add_(1)                                         # 256 MB write: evicts the 129 MB L2
 
@@ -801,19 +809,26 @@ def run_parallel(args):
     out = torch.empty(shape, dtype=torch.float32, device=dev)
     max_ctx = prompt + S
     flags = LAUNCH_FLAGS[args.launch_flags]
-    ws = (cache.zeroed_workspace(C, max_ctx, args.partition) if flags & 1
-          else cache.workspace(C, max_ctx, args.partition))
+    # the candidates share the prompt's whole blocks (64 of them) for all 128 steps: one
+    # prefix group, so each shared (block, head) tile is read once for all 8 query rows
+    use_groups = not args.no_prefix_groups
+    groups = torch.tensor([[0, C, (prompt // BS) * BS]], dtype=torch.int32, device=dev) if use_groups else None
+    if flags & 1:
+        ws = cache.zeroed_workspace(C, max_ctx, args.partition, prefix_groups=use_groups)
+    else:
+        ws = torch.zeros(abi_workspace_bytes(cache, C, max_ctx, args.partition, use_groups), dtype=torch.uint8,
+                         device=dev)
     stream = torch.cuda.Stream(dev)
 
     def loop():
         for i in range(S):
             if cows[i] is not None:
                 cache.copy_blocks(cows[i], stream=stream)
-            if flags:
+            if flags or use_groups:
                 # a step after block copies reads rows the copy kernel just wrote: no early pool
                 cache.attention_ex(0, q[i], bt[i], cl[i], max_ctx, w.scale, k_new=kn[i], v_new=vn[i],
                                    out=out[i], partition_tokens=args.partition, workspace=ws, stream=stream,
-                                   flags=flags if cows[i] is None else flags & ~16)
+                                   flags=flags if cows[i] is None else flags & ~16, prefix_groups=groups)
             else:
                 cache.attention_append(0, q[i], kn[i], vn[i], bt[i], cl[i], max_ctx, w.scale, out=out[i],
                                        partition_tokens=args.partition, workspace=ws, stream=stream)
@@ -822,23 +837,36 @@ def run_parallel(args):
         for _ in range(args.warmup):
             loop()
     stream.synchronize()
+    # the 128 steps are captured once in a CUDA graph and replayed (as a serving loop
+    # would); replaying repeats the same copies and appends, so the pool ends identical
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        loop()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    total = 0.0
+
+    def timed(fn):
+        total = 0.0
+        for _ in range(args.steps):
+            with torch.cuda.stream(stream):
+                _flush_l2(flush)
+                ev[0].record(stream)
+                fn()
+                ev[1].record(stream)
+            stream.synchronize()
+            total += ev[0].elapsed_time(ev[1])
+        return total / args.steps
+
+    for _ in range(args.warmup):
+        graph.replay()
+    stream.synchronize()
     clocks = ClockSampler(0)
     clocks.start()
-    for _ in range(args.steps):
-        with torch.cuda.stream(stream):
-            _flush_l2(flush)
-            ev[0].record(stream)
-            loop()
-            ev[1].record(stream)
-        stream.synchronize()
-        total += ev[0].elapsed_time(ev[1])
+    ms = timed(graph.replay)
     clk = clocks.stop()
+    eager_ms = timed(loop)
     if cache.device_error():
         raise SystemExit("device error during parallel sampling")
-    ms = total / args.steps
     peak, peak_src = measured_peak()
     uniq_gbs = unique / (ms / 1e3) / 1e9
     line = {
@@ -847,10 +875,12 @@ def run_parallel(args):
         "vs_baseline": None, "dtype": "f32-accum/f16", "data": "synthetic",
         "config": {"workload": "parallel", "layers": 1, "candidates": C, "prompt": prompt, "decode_steps": S,
                    "heads": H, "head_dim": d, "block_size": BS, "cow_copies": n_cow, "launch_flags": args.launch_flags,
+                   "prefix_groups": [[0, C, (prompt // BS) * BS]] if use_groups else None,
                    "blocks_in_use": w.num_blocks - len(alloc.free_list()),
                    "l2": "flushed (256 MB write) before each timed 128-step run",
-                   "step": "128 x (block copies + fused append + attention), one run per timed step"},
+                   "step": "128 x (block copies + fused append + attention), one CUDA graph per timed step"},
         "seq_steps_per_s": C * S / (ms / 1e3),
+        "eager": {"ms_per_128_steps": eager_ms, "unique_GB/s": unique / (eager_ms / 1e3) / 1e9},
         "logical_GB/s": logical / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": uniq_gbs, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": uniq_gbs / peak, "traffic": None, "unique_bytes_per_run": unique,
@@ -877,6 +907,8 @@ def main():
     ap.add_argument("--ref-units", type=int, default=768, help="oracle units per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="time kv_append + paged_decode_attention as two calls")
+    ap.add_argument("--no-prefix-groups", action="store_true",
+                    help="parallel sampling: attend without prefix groups (each candidate reads the shared prompt)")
     ap.add_argument("--window", type=int, default=0, help="sliding-window decode over the last N tokens")
     ap.add_argument("--launch-flags", choices=sorted(LAUNCH_FLAGS), default=None,
                     help="zeroed: a zero-filled workspace kept across calls (no clearing copy per call); "

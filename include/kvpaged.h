@@ -58,7 +58,8 @@ enum {
     KV_DEVERR_SLOT = 1,        /* slot_mapping entry >= num_blocks*block_size           */
     KV_DEVERR_BLOCK_ID = 2,    /* block table / copy pair id outside [0, num_blocks)    */
     KV_DEVERR_CONTEXT = 4,     /* context_len < 0, > max_blocks*block_size or > max_context */
-    KV_DEVERR_TIMEOUT = 8      /* a bounded mbarrier wait ran out (about one second)    */
+    KV_DEVERR_TIMEOUT = 8,     /* a bounded mbarrier wait ran out (about one second)    */
+    KV_DEVERR_PREFIX = 16      /* a prefix group broke its rules (attended without sharing) */
 };
 
 typedef struct {
@@ -339,7 +340,31 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *                back to the query's type.  Partials and their merge stay float32; only the
  *                final store is rounded, so the value equals the float32 call's, rounded.
  *   out          device float32 [batch][num_q_heads][head_dim], or float16 with
- *                KV_DECODE_OUT_F16; 16-byte aligned. */
+ *                KV_DECODE_OUT_F16; 16-byte aligned.
+ *   prefix_groups, num_prefix_groups  NULL and 0, or shared prompt prefixes: device int32
+ *                [num_prefix_groups][3] of (first, count, shared_tokens), 4-byte aligned.  The
+ *                `count` sequences first .. first+count-1 of the batch (2 to 8 of them) hold the
+ *                same physical blocks in their first shared_tokens / block_size table entries: the
+ *                candidates of parallel sampling forked from one prompt, which share its blocks
+ *                until they write into them ([PagedAttention] §5.1).  Every (block, head) tile of
+ *                that prefix is then read once for the query rows of all `count` members (their
+ *                scores and P V on the tensor cores) instead of once per member; each member's
+ *                tokens after the prefix are attended on their own and the parts merge exactly
+ *                (log-sum-exp).  The result is the call's result without groups, up to rounding.
+ *                Rules: groups sorted by `first` and disjoint; shared_tokens a multiple of
+ *                block_size, at most every member's context_len (at most context_len - 1 with
+ *                k_new: the appended token lies in a block of the member's own); a group may not
+ *                span a multiple of 1024 sequences.  A group breaking them is attended without
+ *                sharing and sets KV_DEVERR_PREFIX.  That the members' table entries agree is the
+ *                caller's promise (the first member's entries are read).  Under
+ *                KV_DECODE_EARLY_TABLES the groups count as tables.  num_prefix_groups <= batch.
+ *                Needs an fp16 or FP8 pool with head_dim 128 (KV_FEATURE_TENSOR_MAPS),
+ *                num_q_heads equal to num_heads and window 0, else KV_ERR_UNSUPPORTED.  The
+ *                workspace size depends on whether groups are given (not on their contents):
+ *                paged_decode_workspace_size_ex reads num_prefix_groups.  Partitioning with
+ *                groups: partition_tokens 0 = about 16 partitions of max_context, 64 to 1024
+ *                tokens; an explicit value must be at least ceil(max_context / 31) rounded up to
+ *                a multiple of 32 (a member has at most 32 partitions). */
 #define KV_DECODE_WORKSPACE_ZEROED 1u
 #define KV_DECODE_PDL 2u
 #define KV_DECODE_EARLY_TABLES 4u
@@ -365,6 +390,8 @@ typedef struct {
     size_t workspace_bytes;
     kv_stream_t stream;
     unsigned flags;
+    const int32_t* prefix_groups;
+    int num_prefix_groups;
 } kv_decode_args;
 
 /* Workspace bytes for paged_decode_attention_ex with these arguments (0 on invalid ones). */

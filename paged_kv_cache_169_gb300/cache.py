@@ -180,13 +180,16 @@ class PagedKVCache:
                      k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
                      out: torch.Tensor | None = None, partition_tokens: int = 0,
                      workspace: torch.Tensor | None = None, stream=None, flags: int = 0,
-                     out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+                     out_dtype: torch.dtype = torch.float32,
+                     prefix_groups: torch.Tensor | None = None) -> torch.Tensor:
         """Every decode option in one call (paged_decode_attention_ex): grouped-query heads
         (q [batch, Hq, d]), optional fused append, and a sliding window of ``window`` tokens.
         ``flags``: abi.KV_DECODE_WORKSPACE_ZEROED (the workspace's counters are zero: a
         zero-filled workspace used only by decode calls since), abi.KV_DECODE_PDL,
         abi.KV_DECODE_EARLY_TABLES.  A float16 ``out`` (or ``out_dtype``) adds
-        abi.KV_DECODE_OUT_F16: the result is stored rounded to float16."""
+        abi.KV_DECODE_OUT_F16: the result is stored rounded to float16.
+        ``prefix_groups``: int32 CUDA tensor [n, 3] of (first sequence, member count, shared
+        tokens): sequences forked from one prompt read its shared blocks once per group."""
         batch, hq = q.shape[0], q.shape[1]
         if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
             raise ValueError("block_tables and context_lens must be int32")
@@ -205,6 +208,12 @@ class PagedKVCache:
         a.block_tables, a.max_blocks_per_seq = _dev_ptr(block_tables, "block_tables"), block_tables.shape[1]
         a.context_lens, a.batch, a.max_context = _dev_ptr(context_lens, "context_lens"), batch, max_context
         a.window, a.scale, a.partition_tokens = window, float(scale), partition_tokens
+        if prefix_groups is not None:
+            if prefix_groups.dtype != torch.int32 or prefix_groups.dim() != 2 or prefix_groups.shape[1] != 3:
+                raise ValueError("prefix_groups must be an int32 [n, 3] tensor")
+            if prefix_groups.shape[0] > 0:
+                a.prefix_groups = _dev_ptr(prefix_groups, "prefix_groups")
+                a.num_prefix_groups = prefix_groups.shape[0]
         if workspace is None:
             n = abi.paged_decode_workspace_size_ex(self.handle, a)
             if self._ws is None or self._ws.numel() < n:
@@ -217,12 +226,14 @@ class PagedKVCache:
         return out
 
     def zeroed_workspace(self, batch: int, max_context: int, partition_tokens: int = 0,
-                         num_q_heads: int = 0, window: int = 0) -> torch.Tensor:
+                         num_q_heads: int = 0, window: int = 0, prefix_groups: bool = False) -> torch.Tensor:
         """A new zero-filled workspace for attention_ex(..., flags=KV_DECODE_WORKSPACE_ZEROED),
-        valid for calls of this one shape (batch, query heads, max_context, partition, window)."""
+        valid for calls of this one shape (batch, query heads, max_context, partition, window,
+        with or without prefix groups)."""
         a = abi.kv_decode_args()
         a.num_q_heads, a.batch, a.max_context = num_q_heads, batch, max_context
         a.window, a.partition_tokens = window, partition_tokens
+        a.num_prefix_groups = 1 if prefix_groups else 0
         n = abi.paged_decode_workspace_size_ex(self.handle, a)
         return torch.zeros(n, dtype=torch.uint8, device=self.k[0].device)
 

@@ -105,7 +105,7 @@ const char* kv_status_str(int status) {
     }
 }
 
-int kv_version(void) { return 100; }
+int kv_version(void) { return 101; }
 
 int kv_pool_create(const kv_pool_desc* desc, void* const* k_layers, void* const* v_layers,
                    float* const* k_scales, float* const* v_scales, kv_pool** out) {
@@ -328,6 +328,12 @@ size_t paged_decode_workspace_size_ex(const kv_pool* pool, const kv_decode_args*
     const int hq = x->num_q_heads ? x->num_q_heads : pool->desc.num_heads;
     if (hq < 1 || hq % pool->desc.num_heads != 0) return 0;
     kvp::AttnPlan plan;
+    if (x->num_prefix_groups > 0) {
+        if (hq != pool->desc.num_heads || x->window != 0 ||
+            kvp::plan_attention_prefix(pool, x->batch, x->max_context, x->partition_tokens, &plan) != KV_OK)
+            return 0;
+        return plan.ws_bytes;
+    }
     if (kvp::plan_attention(pool, x->batch, x->max_context, x->partition_tokens, &plan,
                             hq / pool->desc.num_heads, x->window) != KV_OK)
         return 0;
@@ -363,8 +369,19 @@ int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* x) {
     if (x->flags & ~(KV_DECODE_WORKSPACE_ZEROED | KV_DECODE_PDL | KV_DECODE_EARLY_TABLES | KV_DECODE_OUT_F16 |
                      KV_DECODE_EARLY_POOL))
         return KV_ERR_INVALID_ARG;
+    if (x->num_prefix_groups < 0 || (x->num_prefix_groups > 0) != (x->prefix_groups != nullptr) ||
+        x->num_prefix_groups > x->batch || (reinterpret_cast<uintptr_t>(x->prefix_groups) & 3u) != 0)
+        return KV_ERR_INVALID_ARG;
     kvp::AttnPlan plan;
-    int rc = kvp::plan_attention(pool, x->batch, x->max_context, x->partition_tokens, &plan, group, x->window);
+    int rc;
+    if (x->num_prefix_groups > 0) {
+        if (group != 1 || x->window != 0) return KV_ERR_UNSUPPORTED;
+        rc = kvp::plan_attention_prefix(pool, x->batch, x->max_context, x->partition_tokens, &plan);
+        plan.groups = x->prefix_groups;
+        plan.n_groups = x->num_prefix_groups;
+    } else {
+        rc = kvp::plan_attention(pool, x->batch, x->max_context, x->partition_tokens, &plan, group, x->window);
+    }
     if (rc != KV_OK) return rc;
     if (x->workspace_bytes < plan.ws_bytes) return KV_ERR_INVALID_ARG;
     plan.flags = x->flags;

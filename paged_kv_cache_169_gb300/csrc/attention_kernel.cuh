@@ -78,6 +78,10 @@ struct AttnArgs {
     int early_pool;        // with early_tables: the first stages may be filled before it (KV_DECODE_EARLY_POOL)
     int out_f16;           // the result is stored as float16, rounded to nearest (KV_DECODE_OUT_F16)
     float qscale;          // scale * log2(e)
+    // shared prompt prefixes (Cfg PFX): [n_groups][3] of (first sequence, members, shared
+    // tokens), sequence indices of the whole call; s_base = this sub-launch's first sequence
+    const int32_t* groups;
+    int n_groups, s_base, fused;
 };
 
 // Launch the grouped-query instantiations (decode_attention_gqa.cu), group in {2, 4, 8}.
@@ -106,8 +110,16 @@ struct __align__(16) Meta {
     int patch_id, patch_off;   // F_PATCH: its physical block and offset inside the block
     int ids[4];             // physical block of each copy in the chunk (FP8: scale lookup)
     int lo;                 // sliding window: chunk rows below lo lie before the window
-    int pad[3];
+    int nq;                 // shared prefixes: query rows of the item (sequences s .. s+nq-1)
+    int pad[2];
 };
+
+// Shared prompt prefixes: per sequence of a launch, the tokens it shares with its group
+// (bits 0-23; 0: none) and, for the group's first sequence, the member count (bits 24-27).
+constexpr int kPfxTokMask = (1 << 24) - 1;
+// A sequence of a prefix group has at most this many partitions (shared part + private
+// part); they merge in one step.
+constexpr int kPfxMaxParts = 32;
 
 constexpr int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
@@ -137,11 +149,20 @@ template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_
 // copies per byte, which is what limits pools with small tiles (FP8, and fp16 with B = 8).
 // The two half-warps take one head each.  BR_ is then the block size (8 or 16), fixed at
 // compile time because each copy holds whole blocks of both heads.
-template <int D_, typename KV_, typename QT_, int G_ = 1, bool MMA_ = false, int HP_ = 1, int BR_ = 0>
+// PFX_ (tensor-core consumer, one query per head): shared prompt prefixes.  A work item is
+// either (group, head, partition of the shared prefix), whose K/V tiles serve the query rows
+// of up to G_ = 8 member sequences at once, or (sequence, head, partition of the tokens after
+// the prefix) with one query row.
+template <int D_, typename KV_, typename QT_, int G_ = 1, bool MMA_ = false, int HP_ = 1, int BR_ = 0,
+          bool PFX_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int G = G_;
     static constexpr bool MMA = MMA_;
+    static constexpr bool PFX = PFX_;
+    static_assert(!PFX || (MMA && G == 8), "shared prefixes: tensor-core consumer with 8 query rows");
+    // query rows of the output (and of q) per (sequence, KV head)
+    static constexpr int GO = PFX ? 1 : G_;
     static constexpr int HP = HP_;
     static constexpr int BR = BR_;
     static constexpr int GE = G_ * HP_;                   // output rows per work item
@@ -191,8 +212,9 @@ struct Cfg {
                                   : G == 1 ? (Tune<ESZ>::NC ? Tune<ESZ>::NC : NC_AUTO)
                                            : (G == 2 ? 12 : (G == 4 ? 8 : 6));
     // stages that fit beside the prefix table and the barriers
+    static constexpr int TABLES = (PFX ? 3 : 2) * kMaxBatch * 4;   // per-sequence launch tables
     static constexpr int NSW_FIT =
-        (227 * 1024 - 2 * kMaxBatch * 4 - 1024 - (MMA ? 2048 : 0)) /
+        (227 * 1024 - TABLES - 1024 - (MMA ? 2048 : 0)) /
         (NC * (STAGE + (int)sizeof(Meta) + QR_BYTES));
     static constexpr int NSW_CAP = (MMA && FP8) ? 6 : 4;   // FP8 stages are half as large
     static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > NSW_CAP ? NSW_CAP : NSW_FIT);
@@ -202,7 +224,7 @@ struct Cfg {
     static constexpr int QR_OFF = META_R + NC * NSW * (int)sizeof(Meta);   // MMA: one q slot per stage
     static constexpr int BAR_OFF = round_up(QR_OFF + NC * NSW * QR_BYTES, 128);
     static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
-    static constexpr int ZERO_OFF = PREFIX_OFF + 2 * kMaxBatch * 4;  // 128 zero bytes (FP8 mma: masked rows)
+    static constexpr int ZERO_OFF = PREFIX_OFF + TABLES;  // 128 zero bytes (FP8 mma: masked rows)
     static constexpr int MISC_OFF = ZERO_OFF + 128;             // launch-wide values (the partition size)
     static constexpr int ALIGN_SLACK = MMA ? 1024 : 0;           // to 1024-align the base
     static constexpr int SMEM = MISC_OFF + 16 + ALIGN_SLACK;
@@ -376,6 +398,7 @@ __device__ __forceinline__ void load_q(const char* qrow, int sub, float qs, floa
 struct __align__(16) Item {
     int s, h, p, tok0, ntok, nchunks, single, valid, last;   // last: final partition
     int lo;                                                    // masked rows at the start
+    int nq;                                                    // shared prefixes: query rows
 };
 
 // (s, h, p) of compact item index `it` (items ordered by sequence, head, partition).
@@ -410,6 +433,64 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
     r.nchunks = r.ntok > 0 ? (r.ntok + CT - 1) / CT : 1;
     r.single = np == 1;
     r.last = r.p == np - 1;
+    r.nq = 1;
+    return r;
+}
+
+// Shared prompt prefixes.  A prefix-group member's context is split in two: the shared
+// prefix [0, S) and its own tokens [S, ctx), each evenly as decode_item splits a context.
+// Its partitions are numbered shared first (0 .. ns-1), then its own (ns .. ns+no-1).
+__device__ __forceinline__ int pfx_shared_parts(int S, int P) { return S > 0 ? nparts_of(S, P) : 0; }
+__device__ __forceinline__ int pfx_own_parts(int ctx, int S, int P) {
+    return (S > 0 && ctx <= S) ? 0 : nparts_of(ctx - S, P);
+}
+__device__ __forceinline__ int even_part(int len, int np, int P) {
+    return np > 1 ? ((len + np - 1) / np + kPartAlign - 1) / kPartAlign * kPartAlign : P;
+}
+
+// Item `it` of a launch with prefix groups.  Items are ordered by sequence; a group's first
+// sequence lists the group's shared items (head, shared partition: nq = member count query
+// rows, sequences s .. s+nq-1) before its own items (head, own partition: one query row).
+template <int CT>
+__device__ __forceinline__ Item decode_item_pfx(int it, int n_items, const int* s_ctx, const int* s_end,
+                                                const int* s_pfx, int batch, int H, int P) {
+    Item r{};
+    r.valid = it < n_items;
+    if (!r.valid) return r;
+    int lo = 0, hi = batch - 1;          // first s with s_end[s] > it
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (s_end[mid] > it) hi = mid; else lo = mid + 1;
+    }
+    const int s = lo;
+    const int ctx = s_ctx[s];
+    const int S = s_pfx[s] & kPfxTokMask, k = s_pfx[s] >> 24;
+    const int ns = pfx_shared_parts(S, P);
+    const int shared_items = k ? H * ns : 0;
+    int rr = it - (s ? s_end[s - 1] : 0);
+    r.s = s;
+    if (rr < shared_items) {
+        r.h = rr / ns;
+        const int p = rr - r.h * ns;
+        const int ps = even_part(S, ns, P);
+        r.tok0 = p * ps;
+        r.ntok = min(ps, S - r.tok0);
+        r.p = p;
+        r.nq = k;
+    } else {
+        rr -= shared_items;
+        const int no = pfx_own_parts(ctx, S, P);
+        r.h = rr / no;
+        const int p = rr - r.h * no;
+        const int ps = even_part(ctx - S, no, P);
+        r.tok0 = S + p * ps;
+        r.ntok = min(ps, ctx - r.tok0);
+        r.p = ns + p;
+        r.nq = 1;
+        r.single = ns + no == 1;
+        r.last = p == no - 1;
+    }
+    r.nchunks = r.ntok > 0 ? (r.ntok + CT - 1) / CT : 1;
     return r;
 }
 
@@ -417,19 +498,21 @@ __device__ __forceinline__ Item decode_item(int it, int n_items, const int* s_ct
 // M = max m_p, L = sum l_p 2^(m_p - M), out = sum o_p 2^(m_p - M) / L.
 // The partials were written by other SMs; they are read through L2 (ld.global.cg).
 template <int D, int G, bool FINAL>
-__device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, int first, int count, int stride,
-                                               int lane) {
-    // merges partials first, first+stride, ... (count of them) of the G query heads
-    // sh0 .. sh0+G-1 at once: 32/G lanes per head, so every lane's loads are independent
-    // and all heads' loads are in flight together (a merge sits on the critical path).
-    // FINAL writes the normalised output; otherwise the merged, still unnormalised
-    // partial (with its m, l) replaces partial `first`.
-    constexpr int LPH = 32 / G;                     // lanes per query head
+__device__ __forceinline__ void merge_rows(const AttnArgs& a, int64_t row, int first, int count, int stride,
+                                           int lane) {
+    // merges partials first, first+stride, ... (count of them) of G rows at once, 32/G
+    // lanes per row (`row`: this lane group's (sequence, query head)), so every lane's
+    // loads are independent and all rows' loads are in flight together (a merge sits on
+    // the critical path).  A lane group with count 0 stores nothing.  FINAL writes the
+    // normalised output; otherwise the merged, still unnormalised partial (with its m, l)
+    // replaces partial `first`.
+    constexpr int LPH = 32 / G;                     // lanes per row
     constexpr int DL = D / LPH;                     // dims per lane
     constexpr int VEC = DL % 4 == 0 ? 4 : 2;
     constexpr int UNR = G == 1 ? 4 : 2;
-    const int g = lane / LPH, q = lane % LPH;
-    const int64_t base = (sh0 + g) * a.max_parts + first;
+    const int q = lane % LPH;
+    const bool act = count > 0;
+    const int64_t base = row * a.max_parts + first;
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + base;
     float mx = -CUDART_INF_F;
     for (int k = q; k < count; k += LPH) mx = fmaxf(mx, __ldcg(ml + static_cast<int64_t>(k) * stride).x);
@@ -440,11 +523,11 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
     for (int i = 0; i < DL; ++i) acc[i] = 0.f;
     #pragma unroll UNR
     for (int k = 0; k < count; ++k) {
-        const int64_t row = static_cast<int64_t>(k) * stride;
-        const float2 v = __ldcg(ml + row);
+        const int64_t kr = static_cast<int64_t>(k) * stride;
+        const float2 v = __ldcg(ml + kr);
         const float wgt = ex2_approx(v.x - mx);
         L = fmaf(v.y, wgt, L);
-        const float* o = a.part_o + (base + row) * D;
+        const float* o = a.part_o + (base + kr) * D;
         #pragma unroll
         for (int i = 0; i < DL / VEC; ++i) {
             if constexpr (VEC == 4) {
@@ -458,8 +541,9 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
         }
     }
     const float inv = FINAL ? 1.f / L : 1.f;
+    if (FINAL && !act) return;
     if (FINAL && a.out_f16) {                          // rounded once, from the float32 result
-        __half* oh = static_cast<__half*>(a.out) + (sh0 + g) * D;
+        __half* oh = static_cast<__half*>(a.out) + row * D;
         #pragma unroll
         for (int i = 0; i < DL / VEC; ++i) {
             if constexpr (VEC == 4) {
@@ -475,9 +559,10 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
         }
         return;
     }
-    float* out = FINAL ? static_cast<float*>(a.out) + (sh0 + g) * D : a.part_o + base * D;
+    float* out = FINAL ? static_cast<float*>(a.out) + row * D : a.part_o + base * D;
     if (!FINAL) {
         __syncwarp();                                  // every lane has read partial `first`
+        if (!act) return;
         if (q == 0) reinterpret_cast<float2*>(a.part_ml)[base] = make_float2(mx, L);
     }
     #pragma unroll
@@ -489,6 +574,13 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
             reinterpret_cast<float2*>(out)[i * LPH + q] = make_float2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
         }
     }
+}
+
+// The G consecutive rows sh0 .. sh0+G-1 (the query heads of one K/V head).
+template <int D, int G, bool FINAL>
+__device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, int first, int count, int stride,
+                                               int lane) {
+    merge_rows<D, G, FINAL>(a, sh0 + lane / (32 / G), first, count, stride, lane);
 }
 
 // Partition p of (sequence, KV head) shk has written its partials: publish them and take
@@ -539,6 +631,34 @@ __device__ __forceinline__ void ticket_resolve(const AttnArgs& a, Ticket& tk, in
     if (lane == 0) a.arrivals[tk.shk] = 0;                             // left zero for the next call
     __syncwarp();
     merge_partials<D, G, true>(a, tk.shk * G, 0, count, stride, lane);
+}
+
+// Shared prefixes: an item writes a partial for each of its query rows (a shared item for
+// every member of the group), so lane r takes the ticket of row r; rows merge one by one,
+// in one step (a member has at most kPfxMaxParts partitions).
+struct PfxTicket {
+    unsigned prev;          // the row's arrival count before this partition (in flight until read)
+    int sq, np;             // the row's (sequence, head) and its number of partitions
+    bool pending;
+};
+
+template <int D>
+__device__ __forceinline__ void pfx_ticket_resolve(const AttnArgs& a, PfxTicket& tk, int lane) {
+    const bool last = tk.pending && tk.prev == static_cast<unsigned>(tk.np - 1);
+    tk.pending = false;
+    const unsigned m = __ballot_sync(FULL, last);
+    if (!m) return;
+    if (last) a.arrivals[tk.sq] = 0;                                   // left zero for the next call
+    __syncwarp();
+    if (__popc(m) == 1) {                          // one row: all 32 lanes on it
+        const int r = __ffs(m) - 1;
+        merge_rows<D, 1, true>(a, __shfl_sync(FULL, tk.sq, r), 0, __shfl_sync(FULL, tk.np, r), 1, lane);
+    } else {                                       // rows side by side, 4 lanes each (row r: lanes 4r..4r+3)
+        const int r = lane >> 2;
+        const int sq = __shfl_sync(FULL, tk.sq, r);
+        const int np = __shfl_sync(FULL, tk.np, r);
+        merge_rows<D, 8, true>(a, sq, 0, ((m >> r) & 1) ? np : 0, 1, lane);
+    }
 }
 
 // Fused append: lane's D/32 elements of one new-token row (src, in_bytes per element)
@@ -641,6 +761,8 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     #pragma unroll
     for (int i = 0; i < 8; ++i) { ot[i][0] = ot[i][1] = ot[i][2] = ot[i][3] = 0.f; }
     Ticket tk{};
+    PfxTicket ptk{};
+    const int* s_pfx = s_ctx + 2 * kMaxBatch;       // shared prefixes (PFX launches only)
 
     for (int j = 0;; ++j) {
         const int st = j % NSW;
@@ -655,6 +777,9 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
         const int flags = mp->flags;
         if (flags & F_TERM) break;
         const int nt = mp->ntok, lo = mp->lo, ms = mp->s, mh = mp->h, mpart = mp->p;
+        // query rows of the item: G heads of one sequence, or (shared prefixes) one head of
+        // the nq sequences ms .. ms+nq-1
+        const int nq = C::PFX ? mp->nq : G;
         uint32_t kbase = smem_u32(stg + C::K_OFF), vbase = smem_u32(stg + C::V_OFF);
         if (flags & F_FIRST) {
             m2[0] = m2[1] = -CUDART_INF_F;
@@ -663,10 +788,11 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             for (int i = 0; i < 8; ++i) { ot[i][0] = ot[i][1] = ot[i][2] = ot[i][3] = 0.f; }
             // B fragments of the G query rows (fp16: staged with the item's first chunk;
             // FP8: read from global memory once per item)
-            const bool real = g < G && nt > 0;
+            const bool real = g < nq && nt > 0;
+            const int64_t qr = C::PFX ? static_cast<int64_t>(ms + (real ? g : 0)) * a.H + mh
+                                      : (static_cast<int64_t>(ms) * a.H + mh) * G + (real ? g : 0);
             const uint32_t* qrow = C::FP8
-                ? reinterpret_cast<const uint32_t*>(static_cast<const char*>(a.q) +
-                                                    ((static_cast<int64_t>(ms) * a.H + mh) * G + (real ? g : 0)) * D * 2)
+                ? reinterpret_cast<const uint32_t*>(static_cast<const char*>(a.q) + qr * D * 2)
                 : reinterpret_cast<const uint32_t*>(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES +
                                                     (real ? g : 0) * D * 2);
             #pragma unroll
@@ -878,8 +1004,68 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars[C::NC * NSW + w * NSW + st]));
-        ticket_resolve<D, G>(a, tk, lane);            // the previous item's ticket
-        if (flags & F_LAST) {
+        if constexpr (C::PFX) pfx_ticket_resolve<D>(a, ptk, lane);   // the previous item's tickets
+        else ticket_resolve<D, G>(a, tk, lane);
+        if (C::PFX && (flags & F_LAST)) {
+            float la = l2[0], lb = l2[1];
+            #pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                la += __shfl_xor_sync(FULL, la, off);
+                lb += __shfl_xor_sync(FULL, lb, off);
+            }
+            // query row r = 2t + h2 belongs to sequence ms + r: its result directly when that
+            // sequence has one partition, else its partial and (lane r) its ticket
+            auto parts_of_row = [&](int r) {
+                const int sm = ms + r, S = s_pfx[sm] & kPfxTokMask;
+                return pfx_shared_parts(S, P_eff) + pfx_own_parts(s_ctx[sm], S, P_eff);
+            };
+            #pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int r = 2 * t + h2;
+                if (r >= nq) continue;
+                const int64_t sq = static_cast<int64_t>(ms + r) * a.H + mh;
+                if (parts_of_row(r) == 1) {
+                    const float inv = nt > 0 ? 1.f / (h2 ? lb : la) : 0.f;
+                    if (a.out_f16) {
+                        __half* dh = static_cast<__half*>(a.out) + sq * D;
+                        #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            dh[16 * i + g] = __float2half_rn(ot[i][h2] * inv);
+                            dh[16 * i + 8 + g] = __float2half_rn(ot[i][2 + h2] * inv);
+                        }
+                    } else {
+                        float* dst = static_cast<float*>(a.out) + sq * D;
+                        #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            dst[16 * i + g] = ot[i][h2] * inv;
+                            dst[16 * i + 8 + g] = ot[i][2 + h2] * inv;
+                        }
+                    }
+                } else {
+                    const int64_t idx = sq * a.max_parts + mpart;
+                    if (g == 0) {
+                        a.part_ml[2 * idx] = m2[h2];
+                        a.part_ml[2 * idx + 1] = h2 ? lb : la;
+                    }
+                    float* dst = a.part_o + idx * D;
+                    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        dst[16 * i + g] = ot[i][h2];
+                        dst[16 * i + 8 + g] = ot[i][2 + h2];
+                    }
+                }
+            }
+            __syncwarp();                               // every row's partial is written
+            if (lane < nq) {
+                const int np = parts_of_row(lane);
+                if (np > 1) {
+                    ptk.sq = (ms + lane) * a.H + mh;
+                    ptk.np = np;
+                    ptk.prev = atom_add_acq_rel_gpu(a.arrivals + ptk.sq, 1u);
+                    ptk.pending = true;
+                }
+            }
+        } else if (flags & F_LAST) {
             float la = l2[0], lb = l2[1];
             #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -927,7 +1113,8 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             }
         }
     }
-    ticket_resolve<D, G>(a, tk, lane);
+    if constexpr (C::PFX) pfx_ticket_resolve<D>(a, ptk, lane);
+    else ticket_resolve<D, G>(a, tk, lane);
 }
 
 template <typename C>
@@ -941,6 +1128,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);   // full[NC*NSW], empty[NC*NSW]
     int* s_ctx = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
     int* s_end = s_ctx + kMaxBatch;
+    int* s_pfx = s_ctx + 2 * kMaxBatch;         // shared prefixes (PFX launches only)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int HU = a.H / C::HP;                 // work units (single heads or head pairs) per sequence
 
@@ -970,9 +1158,37 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
             c = c < 0 ? 0 : a.ctx_limit;
         }
         s_ctx[s] = c;
-        s_end[s] = HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), part_of(a.P, a, s));
+        if constexpr (C::PFX) s_pfx[s] = 0;
+        else s_end[s] = HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), part_of(a.P, a, s));
     }
     __syncthreads();
+    if constexpr (C::PFX) {
+        // This sub-launch's prefix groups: the shared token count of every member, and the
+        // member count at the first member.  A group must list 2 to 8 sequences inside this
+        // sub-launch, follow the previous group without overlap, share whole blocks, and
+        // leave every member at least its newest token of its own when this call appends;
+        // one that does not is attended without sharing and flagged.
+        for (int gi = tid; gi < a.n_groups; gi += C::THREADS) {
+            const int g0 = a.groups[3 * gi], k = a.groups[3 * gi + 1], S = a.groups[3 * gi + 2];
+            const int first = g0 - a.s_base;
+            if (first < 0 || first >= a.batch) continue;         // another sub-launch's group
+            bool ok = k >= 2 && k <= 8 && first + k <= a.batch && S >= 0 && S % a.B == 0 && S <= kPfxTokMask;
+            if (ok && gi > 0) ok = a.groups[3 * gi - 3] + a.groups[3 * gi - 2] <= g0;
+            for (int m = 0; ok && m < k; ++m) ok = S + a.fused <= s_ctx[first + m];
+            if (!ok) {
+                if (blockIdx.x == 0) atomicOr(a.err, KV_DEVERR_PREFIX);
+                continue;
+            }
+            if (S == 0) continue;
+            for (int m = 0; m < k; ++m) s_pfx[first + m] = S | (m == 0 ? k << 24 : 0);
+        }
+        __syncthreads();
+        for (int s = tid; s < a.batch; s += C::THREADS) {
+            const int S = s_pfx[s] & kPfxTokMask, k = s_pfx[s] >> 24;
+            s_end[s] = (k ? a.H * pfx_shared_parts(S, a.P) : 0) + a.H * pfx_own_parts(s_ctx[s], S, a.P);
+        }
+        __syncthreads();
+    }
     int* s_misc = reinterpret_cast<int*>(smem + C::MISC_OFF);
     if (warp == 0) {
         // A launch whose items all fit in one round balances best with the smallest
@@ -1035,8 +1251,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         const unsigned first_claim = gridDim.x * NC;
         auto claim = [&]() { pending = atomicAdd(a.counter, 1u) + first_claim; claimed = true; };
         auto decode = [&](unsigned idx) {
-            return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, HU, P_eff, a.s_fine,
-                                   a.P_fine, a.window, rpc);
+            if constexpr (C::PFX)
+                return decode_item_pfx<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, s_pfx, a.batch, a.H, P_eff);
+            else
+                return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, HU, P_eff, a.s_fine,
+                                       a.P_fine, a.window, rpc);
         };
         int ids[CBMAX];
         auto load_ids = [&](const Item& it, int chunk) {
@@ -1056,10 +1275,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         }
         // the query rows of cur, into stage st (they complete on that stage's barrier)
         auto copy_q = [&](int st) {
-            const char* qsrc = static_cast<const char*>(a.q) + (static_cast<int64_t>(cur.s) * HU + cur.h) * C::Q_BYTES;
             const uint32_t qdst = C::QR_BYTES ? smem_u32(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES)
                                               : smem_u32(stage_ptr(w, st)) + C::Q_OFF;
-            bulk_g2s(qdst, qsrc, C::Q_BYTES, full_bar(w, st));
+            if constexpr (C::PFX) {
+                // one row per member sequence (rows of one head, H rows apart in q)
+                constexpr uint32_t RB = C::D * sizeof(typename C::QT);
+                for (int r = 0; r < cur.nq; ++r)
+                    bulk_g2s(qdst + r * RB, static_cast<const char*>(a.q) + (static_cast<int64_t>(cur.s + r) * a.H + cur.h) * RB,
+                             RB, full_bar(w, st));
+            } else {
+                const char* qsrc = static_cast<const char*>(a.q) + (static_cast<int64_t>(cur.s) * HU + cur.h) * C::Q_BYTES;
+                bulk_g2s(qdst, qsrc, C::Q_BYTES, full_bar(w, st));
+            }
         };
         // Fill stage st with chunk c of cur (or the end marker) and advance.  pre: before
         // griddepcontrol.wait (KV_DECODE_EARLY_POOL): K and V tiles only, the query copy
@@ -1085,12 +1312,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                     }
                 }
                 const bool with_q = (c == 0) && nt > 0 && (C::Q_STAGE > 0 || C::QR_BYTES > 0);
-                const uint32_t bytes = nblk * 2 * tile + (with_q ? C::Q_BYTES : 0);
+                const uint32_t q_bytes = C::PFX ? cur.nq * C::D * sizeof(typename C::QT) : C::Q_BYTES;
+                const uint32_t bytes = nblk * 2 * tile + (with_q ? q_bytes : 0);
                 meta->s = cur.s;
                 meta->h = cur.h;
                 meta->p = cur.p;
                 meta->ntok = nt;
                 meta->lo = c == 0 ? cur.lo : 0;
+                meta->nq = cur.nq;
                 // fused append: the sequence's newest token is the last row of the
                 // last chunk of its last partition
                 const bool patch = a.k_new != nullptr && cur.last && c == cur.nchunks - 1 && nt > 0;
@@ -1500,13 +1729,13 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
         attr_done |= bit;
     }
     const int total = args.batch;
-    const size_t qrow = static_cast<size_t>(args.H) * C::G * C::D * sizeof(typename C::QT);
+    const size_t qrow = static_cast<size_t>(args.H) * C::GO * C::D * sizeof(typename C::QT);
     for (int s0 = 0, sub = 0; s0 < total; s0 += kMaxBatch, ++sub) {
         AttnArgs sa = args;
         sa.batch = total - s0 < kMaxBatch ? total - s0 : kMaxBatch;
         sa.q = static_cast<const char*>(args.q) + s0 * qrow;
         sa.out = static_cast<char*>(args.out) +
-                 static_cast<int64_t>(s0) * args.H * C::G * C::D * (args.out_f16 ? 2 : 4);
+                 static_cast<int64_t>(s0) * args.H * C::GO * C::D * (args.out_f16 ? 2 : 4);
         sa.tables = args.tables + static_cast<int64_t>(s0) * args.max_blocks;
         sa.lens = args.lens + s0;
         if (args.k_new) {
@@ -1514,7 +1743,7 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
             sa.k_new = args.k_new + nofs;
             sa.v_new = args.v_new + nofs;
         }
-        const int64_t pofs = static_cast<int64_t>(s0) * args.H * C::G * args.max_parts;
+        const int64_t pofs = static_cast<int64_t>(s0) * args.H * C::GO * args.max_parts;
         if (args.part_ml) {
             sa.part_ml = args.part_ml + 2 * pofs;
             sa.part_o = args.part_o + pofs * C::D;
@@ -1522,6 +1751,7 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
             if (args.grp_arrivals) sa.grp_arrivals = args.grp_arrivals + static_cast<int64_t>(s0) * args.H * args.n_grp;
         }
         sa.s_fine = args.s_fine - s0 > 0 ? args.s_fine - s0 : 0;
+        sa.s_base = s0;
         sa.counter = counters + sub;
         sa.exit_counter = counters + kMaxSub + sub;
         const int64_t upper = static_cast<int64_t>(sa.batch) * (args.H / C::HP) * args.max_parts;

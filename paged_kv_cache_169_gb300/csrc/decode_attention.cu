@@ -171,6 +171,60 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     return KV_OK;
 }
 
+int plan_attention_prefix(const kv_pool* pool, int batch, int max_context, int partition_tokens,
+                          AttnPlan* plan) {
+    const kv_pool_desc& d = pool->desc;
+    if (batch < 0 || max_context < 0 || batch > kMaxBatch * kMaxSub) return KV_ERR_INVALID_ARG;
+    if (!pool->tmaps || d.head_dim != 128 || (d.dtype != KV_F16 && d.dtype != KV_FP8_E4M3))
+        return KV_ERR_UNSUPPORTED;
+    // A member's context splits at the end of its shared prefix into at most
+    // ceil(max_context / P) + 1 partitions, which must fit one merge step.
+    const int64_t pmin64 = ((static_cast<int64_t>(max_context) + kPfxMaxParts - 2) / (kPfxMaxParts - 1) +
+                            kPartAlign - 1) / kPartAlign * kPartAlign;
+    const int pmin = static_cast<int>(pmin64 < kPartAlign ? kPartAlign : pmin64);
+    int P;
+    if (partition_tokens > 0) {
+        if (partition_tokens % kPartAlign != 0 || partition_tokens < pmin || partition_tokens > (1 << 24))
+            return KV_ERR_INVALID_ARG;
+        P = partition_tokens;
+    } else if (partition_tokens == 0) {
+        // library choice: short items, so a group's shared prefix (read once for all its
+        // members) spreads over many SMs: about 16 partitions of the longest context,
+        // 64 to 1024 tokens each
+        int64_t p = (static_cast<int64_t>(max_context) + 15) / 16;
+        p = (p + kPartAlign - 1) / kPartAlign * kPartAlign;
+        if (p < 64) p = 64;
+        if (p > 1024) p = 1024;
+        P = static_cast<int>(p < pmin ? pmin : p);
+    } else {
+        return KV_ERR_INVALID_ARG;
+    }
+    plan->partition = P;
+    plan->fine_partition = P;
+    plan->fine_from = batch;
+    plan->alt_partition = P;
+    plan->max_parts = max_context <= 0 ? 1 : (max_context + P - 1) / P + 1;
+    const int64_t launch_items = static_cast<int64_t>(batch < kMaxBatch ? batch : kMaxBatch) *
+                                 d.num_heads * plan->max_parts;
+    if (launch_items > (int64_t{1} << 30)) return KV_ERR_INVALID_ARG;
+    plan->consumers = d.dtype == KV_F16 ? consumers_of<Cfg<128, __half, __half, 8, true, 1, 0, true>>()
+                                        : consumers_of<Cfg<128, uint8_t, __half, 8, true, 1, 0, true>>();
+    plan->group = 1;
+    plan->window = 0;
+    plan->flags = 0;
+    plan->groups = nullptr;
+    plan->n_groups = 0;
+    size_t ws = kCounterBytes;
+    if (plan->max_parts > 1) {
+        const size_t n = static_cast<size_t>(batch) * d.num_heads * plan->max_parts;
+        ws += plan->arrivals_bytes(batch, d.num_heads);
+        ws += align256(n * 2 * sizeof(float));
+        ws += align256(n * d.head_dim * sizeof(float));
+    }
+    plan->ws_bytes = ws;
+    return KV_OK;
+}
+
 int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,
                      const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                      int batch, int max_context, float scale, const AttnPlan& plan,
@@ -238,6 +292,18 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     if (pool->tmaps) {                             // the layer's swizzled tile maps
         a.kmap = pool->tmaps[2 * layer];
         a.vmap = pool->tmaps[2 * layer + 1];
+    }
+    a.fused = k_new != nullptr ? 1 : 0;
+
+    if (plan.n_groups > 0) {                       // shared prompt prefixes
+        if (!pool->tmaps || group != 1 || plan.window != 0) return KV_ERR_UNSUPPORTED;
+        a.groups = plan.groups;
+        a.n_groups = plan.n_groups;
+        if (d.dtype == KV_F16)
+            return launch_typed<Cfg<128, __half, __half, 8, true, 1, 0, true>>(pool, a, plan, counters, stream);
+        if (d.dtype == KV_FP8_E4M3)
+            return launch_typed<Cfg<128, uint8_t, __half, 8, true, 1, 0, true>>(pool, a, plan, counters, stream);
+        return KV_ERR_UNSUPPORTED;
     }
 
     if (group != 1) return launch_attention_grouped(group, pool, a, plan, counters, stream);

@@ -57,6 +57,8 @@ struct AttnPlan {
     int consumers;       // consumer warps per CTA
     int group;           // query heads per KV head
     int window;          // > 0: sliding window of the last `window` tokens
+    const int32_t* groups = nullptr;   // shared prompt prefixes: device [n_groups][3], or none
+    int n_groups = 0;
     size_t ws_bytes;     // workspace bytes
     // zero-initialised counters after the kCounterBytes of work counters: the per-(sequence, head)
     // arrivals, then the per-partition-group arrivals
@@ -72,6 +74,10 @@ bool valid_group(const kv_pool_desc& d, int group);
 int head_group(const kv_pool_desc& d, int group);
 int plan_attention(const kv_pool* pool, int batch, int max_context, int partition_tokens,
                    AttnPlan* plan, int group = 1, int window = 0);
+// Plan of a call with shared prompt prefixes (one query per head, tensor-map pools only;
+// KV_ERR_UNSUPPORTED otherwise).  The caller sets plan->groups and n_groups.
+int plan_attention_prefix(const kv_pool* pool, int batch, int max_context, int partition_tokens,
+                          AttnPlan* plan);
 int launch_attention(const kv_pool* pool, int layer, const void* q, float* out,
                      const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                      int batch, int max_context, float scale, const AttnPlan& plan,
