@@ -213,8 +213,11 @@ struct Cfg {
                                            : (G == 2 ? 12 : (G == 4 ? 8 : 6));
     // stages that fit beside the prefix table and the barriers
     static constexpr int TABLES = (PFX ? 3 : 2) * kMaxBatch * 4;   // per-sequence launch tables
+    // beside the stages: the tables and the reserve (alignment slack, barriers, zero line,
+    // launch-wide values)
+    static constexpr int RESERVE = 1024 + (MMA ? 2048 : 0);
     static constexpr int NSW_FIT =
-        (227 * 1024 - TABLES - 1024 - (MMA ? 2048 : 0)) /
+        (227 * 1024 - TABLES - RESERVE) /
         (NC * (STAGE + (int)sizeof(Meta) + QR_BYTES));
     static constexpr int NSW_CAP = (MMA && FP8) ? 6 : 4;   // FP8 stages are half as large
     static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > NSW_CAP ? NSW_CAP : NSW_FIT);
@@ -634,13 +637,61 @@ __device__ __forceinline__ void ticket_resolve(const AttnArgs& a, Ticket& tk, in
 }
 
 // Shared prefixes: an item writes a partial for each of its query rows (a shared item for
-// every member of the group), so lane r takes the ticket of row r; rows merge one by one,
-// in one step (a member has at most kPfxMaxParts partitions).
+// every member of the group), so lane r takes the ticket of row r.  A member has at most
+// kPfxMaxParts partitions, merged in one step.
 struct PfxTicket {
     unsigned prev;          // the row's arrival count before this partition (in flight until read)
     int sq, np;             // the row's (sequence, head) and its number of partitions
     bool pending;
 };
+
+// One row's merge with all 32 lanes (head_dim 128: a float4 of the row per lane) for at
+// most kPfxMaxParts partials.  Lane k loads partial k's (m, l) while the rows of the first
+// eight partials are already in flight, so up to eight partials cost one L2 round trip.
+template <int D>
+__device__ __forceinline__ void merge_row_fast(const AttnArgs& a, int64_t row, int count, int lane) {
+    static_assert(D == 128, "a float4 of the row per lane");
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + row * a.max_parts;
+    const float4* o = reinterpret_cast<const float4*>(a.part_o + row * a.max_parts * D) + lane;
+    const float2 v = lane < count ? __ldcg(ml + lane) : make_float2(-CUDART_INF_F, 0.f);
+    // the weights and the denominator are summed in partition order, as merge_rows does,
+    // so a row's result does not depend on which of the two merged it
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wk = 0.f, L = 0.f;
+    #pragma unroll 1
+    for (int k0 = 0; k0 < count; k0 += 8) {
+        float4 x[8];
+        #pragma unroll
+        for (int k = 0; k < 8; ++k)
+            x[k] = k0 + k < count ? __ldcg(o + (k0 + k) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k0 == 0) {
+            const float mx = warp_max(v.x);
+            wk = lane < count ? ex2_approx(v.x - mx) : 0.f;
+        }
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float w = __shfl_sync(FULL, wk, (k0 + k) & 31);
+            const float lk = __shfl_sync(FULL, v.y, (k0 + k) & 31);
+            if (k0 + k < count) L = fmaf(lk, w, L);
+            acc.x = fmaf(w, x[k].x, acc.x);
+            acc.y = fmaf(w, x[k].y, acc.y);
+            acc.z = fmaf(w, x[k].z, acc.z);
+            acc.w = fmaf(w, x[k].w, acc.w);
+        }
+    }
+    const float inv = 1.f / L;
+    if (a.out_f16) {                                   // rounded once, from the float32 result
+        const __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        const __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
+        uint2 wv;
+        wv.x = *reinterpret_cast<const unsigned*>(&lo);
+        wv.y = *reinterpret_cast<const unsigned*>(&hi);
+        reinterpret_cast<uint2*>(static_cast<__half*>(a.out) + row * D)[lane] = wv;
+    } else {
+        reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * D)[lane] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+}
 
 template <int D>
 __device__ __forceinline__ void pfx_ticket_resolve(const AttnArgs& a, PfxTicket& tk, int lane) {
@@ -652,7 +703,7 @@ __device__ __forceinline__ void pfx_ticket_resolve(const AttnArgs& a, PfxTicket&
     __syncwarp();
     if (__popc(m) == 1) {                          // one row: all 32 lanes on it
         const int r = __ffs(m) - 1;
-        merge_rows<D, 1, true>(a, __shfl_sync(FULL, tk.sq, r), 0, __shfl_sync(FULL, tk.np, r), 1, lane);
+        merge_row_fast<D>(a, __shfl_sync(FULL, tk.sq, r), __shfl_sync(FULL, tk.np, r), lane);
     } else {                                       // rows side by side, 4 lanes each (row r: lanes 4r..4r+3)
         const int r = lane >> 2;
         const int sq = __shfl_sync(FULL, tk.sq, r);

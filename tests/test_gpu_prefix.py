@@ -202,6 +202,10 @@ def test_prefix_groups_against_oracle(dtype, B, fused):
         out = cache.attention_ex(0, q, c["bt"], c["cl"], max_ctx, c["scale"], partition_tokens=P,
                                  prefix_groups=grp, **kw)
         worst = max(worst, max_abs(out.cpu().numpy(), c["want"]))
+        # the same call again gives the same bits, whichever warps finish last and merge
+        again = cache.attention_ex(0, q, c["bt"], c["cl"], max_ctx, c["scale"], partition_tokens=P,
+                                   prefix_groups=grp, **kw)
+        assert torch.equal(again, out)
         # float16 output: the float32 result rounded to nearest even
         o16 = cache.attention_ex(0, q, c["bt"], c["cl"], max_ctx, c["scale"], partition_tokens=P,
                                  prefix_groups=grp, out_dtype=torch.float16, **kw)
