@@ -116,9 +116,9 @@ def traffic_record(kernel_srcs):
 
 # ----------------------------------------------------------------------------- clocks
 def default_launch_flags(workload: str) -> str:
-    """All four launch flags, except for parallel sampling: its steps measured 3.5 % slower
-    with the early K/V tiles (and its copy-on-write steps may not use them)."""
-    return "early" if workload == "parallel" else "earlypool"
+    """All four launch flags on every workload (a parallel-sampling step right after its
+    copy-on-write drops the early K/V tiles: the copy kernel wrote rows it reads)."""
+    return "earlypool"
 
 
 class ClockSampler:
@@ -915,7 +915,7 @@ def main():
                          "pdl: zeroed + programmatic dependent launch; early: pdl + tables and lengths "
                          "read before the previous launch ends (they are written before the timed loop); "
                          "earlypool: early + the first K/V tiles fetched before the previous launch ends "
-                         "(default; parallel: early, measured faster there)")
+                         "(default)")
     args = ap.parse_args()
     if args.launch_flags is None:
         args.launch_flags = default_launch_flags(args.workload)

@@ -54,7 +54,7 @@ void make_tensor_maps(kv_pool* p) {
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
     Encode encode = reinterpret_cast<Encode>(fn);
     const int L = d.num_layers;
-    void* raw = std::malloc(2 * L * sizeof(CUtensorMap) + 64);
+    void* raw = std::malloc(4 * L * sizeof(CUtensorMap) + 64);
     if (!raw) return;
     CUtensorMap* maps = reinterpret_cast<CUtensorMap*>((reinterpret_cast<uintptr_t>(raw) + 63) & ~uintptr_t(63));
     // a token row of one head (128 halves) seen as two 64-half halves: the copied tile of
@@ -68,23 +68,36 @@ void make_tensor_maps(kv_pool* p) {
     const cuuint64_t dims8[2] = {128, rows};
     const cuuint64_t strides8[1] = {128};
     const cuuint32_t box8[2] = {128, static_cast<cuuint32_t>(d.block_size < 32 ? d.block_size : 32)};
-    for (int l = 0; l < L; ++l) {
-        for (int kv = 0; kv < 2; ++kv) {
-            void* base = kv == 0 ? p->k_layers[l] : p->v_layers[l];
-            const CUresult rc =
-                fp8 ? encode(&maps[2 * l + kv], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims8, strides8, box8, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)
-                    : encode(&maps[2 * l + kv], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (rc != CUDA_SUCCESS) {
-                std::free(raw);
-                return;
+    // head-pair stages: a whole block of two adjacent heads (2*B consecutive rows) per copy
+    const bool pairs = fp8 || d.block_size <= 16;
+    const cuuint32_t boxp[3] = {64, static_cast<cuuint32_t>(2 * d.block_size), 2};
+    const cuuint32_t boxp8[2] = {128, static_cast<cuuint32_t>(2 * d.block_size)};
+    for (int set = 0; set < (pairs ? 2 : 1); ++set) {
+        for (int l = 0; l < L; ++l) {
+            for (int kv = 0; kv < 2; ++kv) {
+                void* base = kv == 0 ? p->k_layers[l] : p->v_layers[l];
+                CUtensorMap* m = &maps[set * 2 * L + 2 * l + kv];
+                const CUresult rc =
+                    fp8 ? encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims8, strides8, set ? boxp8 : box8, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)
+                        : encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, set ? boxp : box, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (rc != CUDA_SUCCESS) {
+                    if (set == 0) {
+                        std::free(raw);
+                        return;
+                    }
+                    p->tmaps = maps;                   // single-head maps only
+                    p->tmaps_raw = raw;
+                    return;
+                }
             }
         }
     }
     p->tmaps = maps;
+    p->pmaps = pairs ? maps + 2 * L : nullptr;
     p->tmaps_raw = raw;
 }
 

@@ -153,19 +153,26 @@ template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_
 // either (group, head, partition of the shared prefix), whose K/V tiles serve the query rows
 // of up to G_ = 8 member sequences at once, or (sequence, head, partition of the tokens after
 // the prefix) with one query row.
+// PR_ (tensor-core consumer): head-pair stages.  One copy brings a block's tiles of two
+// adjacent K/V heads (adjacent in the pool), and the stage is shared by two consumer warps,
+// one head each: copies of 2B rows instead of B, half as many copies per byte (the copy
+// rate per SM bounds small tiles).  Needs whole blocks per copy (B <= CT).
 template <int D_, typename KV_, typename QT_, int G_ = 1, bool MMA_ = false, int HP_ = 1, int BR_ = 0,
-          bool PFX_ = false>
+          bool PFX_ = false, bool PR_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int G = G_;
     static constexpr bool MMA = MMA_;
     static constexpr bool PFX = PFX_;
+    static constexpr bool PR = PR_;
+    static_assert(!PR || MMA, "head-pair stages: tensor-core consumer");
     static_assert(!PFX || (MMA && G == 8), "shared prefixes: tensor-core consumer with 8 query rows");
     // query rows of the output (and of q) per (sequence, KV head)
     static constexpr int GO = PFX ? 1 : G_;
     static constexpr int HP = HP_;
     static constexpr int BR = BR_;
     static constexpr int GE = G_ * HP_;                   // output rows per work item
+    static constexpr int KVH = HP_ * (PR_ ? 2 : 1);       // K/V heads per work item (per copy)
     static_assert(!MMA || (sizeof(KV_) <= 2 && D_ == 128 && G_ >= 2), "tensor-core path: fp16 or FP8, d 128, G >= 2");
     static_assert(HP == 1 || ((HP == 2 || HP == 4) && G == 1 && !MMA && (BR == 8 || BR == 16)),
                   "head groups: one query per head");
@@ -186,7 +193,7 @@ struct Cfg {
     static_assert(TPL <= LPR, "the transpose-reduce leaves one token per lane");
     static constexpr int CBMAX = CT >= 8 ? CT / 8 : 1;    // blocks per chunk at B = 8
     static constexpr int ROW = D * ESZ;                   // bytes of one token row of one head
-    static constexpr int KV_BYTES = CT * ROW * HP;        // bytes of K (or V) per chunk
+    static constexpr int KV_BYTES = CT * ROW * KVH;       // bytes of K (or V) per chunk
     static constexpr int Q_BYTES = GE * D * sizeof(QT);   // the query rows of one item
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = KV_BYTES;
@@ -199,7 +206,8 @@ struct Cfg {
     // tensor maps, and the mma fragments are built straight from the E4M3 codes
     static constexpr bool SWZ_K = MMA && FP8;
     static constexpr int Q_STAGE = MMA ? 0 : Q_BYTES;
-    static constexpr int QR_BYTES = SWZ_STAGE ? Q_BYTES : 0;
+    // head-pair stages take their query rows from global memory (no per-stage slot)
+    static constexpr int QR_BYTES = SWZ_STAGE && !PR ? Q_BYTES : 0;
     static constexpr int STAGE = round_up(Q_OFF + Q_STAGE, (SWZ_STAGE || SWZ_K) ? 1024 : 128);
     static constexpr int NC_AUTO = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
     // more query heads per warp need more registers: fewer consumer warps
@@ -208,9 +216,16 @@ struct Cfg {
 #else
     static constexpr int NC_MMA = 7;               // 8 warps: the register cap stays at 255
 #endif
-    static constexpr int NC = MMA ? NC_MMA
-                                  : G == 1 ? (Tune<ESZ>::NC ? Tune<ESZ>::NC : NC_AUTO)
-                                           : (G == 2 ? 12 : (G == 4 ? 8 : 6));
+#if defined(KVP_PR_RINGS)
+    static constexpr int NR_PAIR = KVP_PR_RINGS;   // tuning sweeps only
+#else
+    static constexpr int NR_PAIR = 4;              // head-pair stages: 4 rings, 8 consumer warps
+#endif
+    static constexpr int NC = PR ? 2 * NR_PAIR
+                                 : MMA ? NC_MMA
+                                       : G == 1 ? (Tune<ESZ>::NC ? Tune<ESZ>::NC : NC_AUTO)
+                                                : (G == 2 ? 12 : (G == 4 ? 8 : 6));
+    static constexpr int NR = PR ? NR_PAIR : NC;   // rings (one producer lane each)
     // stages that fit beside the prefix table and the barriers
     static constexpr int TABLES = (PFX ? 3 : 2) * kMaxBatch * 4;   // per-sequence launch tables
     // beside the stages: the tables and the reserve (alignment slack, barriers, zero line,
@@ -218,15 +233,15 @@ struct Cfg {
     static constexpr int RESERVE = 1024 + (MMA ? 2048 : 0);
     static constexpr int NSW_FIT =
         (227 * 1024 - TABLES - RESERVE) /
-        (NC * (STAGE + (int)sizeof(Meta) + QR_BYTES));
+        (NR * (STAGE + (int)sizeof(Meta) + QR_BYTES));
     static constexpr int NSW_CAP = (MMA && FP8) ? 6 : 4;   // FP8 stages are half as large
     static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > NSW_CAP ? NSW_CAP : NSW_FIT);
     static_assert(NSW >= 2, "at least double buffering");
     static constexpr int THREADS = (NC + 1) * 32;
-    static constexpr int META_R = NC * NSW * STAGE;                   // one Meta per stage
-    static constexpr int QR_OFF = META_R + NC * NSW * (int)sizeof(Meta);   // MMA: one q slot per stage
-    static constexpr int BAR_OFF = round_up(QR_OFF + NC * NSW * QR_BYTES, 128);
-    static constexpr int PREFIX_OFF = BAR_OFF + 2 * NC * NSW * 8;
+    static constexpr int META_R = NR * NSW * STAGE;                   // one Meta per stage
+    static constexpr int QR_OFF = META_R + NR * NSW * (int)sizeof(Meta);   // MMA: one q slot per stage
+    static constexpr int BAR_OFF = round_up(QR_OFF + NR * NSW * QR_BYTES, 128);
+    static constexpr int PREFIX_OFF = BAR_OFF + 2 * NR * NSW * 8;
     static constexpr int ZERO_OFF = PREFIX_OFF + TABLES;  // 128 zero bytes (FP8 mma: masked rows)
     static constexpr int MISC_OFF = ZERO_OFF + 128;             // launch-wide values (the partition size)
     static constexpr int ALIGN_SLACK = MMA ? 1024 : 0;           // to 1024-align the base
@@ -790,6 +805,9 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     constexpr int NSW = C::NSW, D = C::D, G = C::G, CT = C::CT;
     static_assert((CT == 16 || (C::FP8 && CT == 32)) && D == 128, "tensor-core consumer shape");
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    // head-pair stages: warps 2r and 2r+1 share ring r, taking the pair's heads 0 and 1
+    const int wr = C::PR ? (w >> 1) : w;             // this warp's ring
+    const int e = C::PR ? (w & 1) : 0;               // this warp's head of the item's pair
     // S^T = K Q^T and O^T += V^T P^T: the 16 tokens of a chunk (and 16 dims of an output
     // tile) are the mma's M side, the query heads (padded to 8) its N side, so no mma row
     // is padding.  Lane (g, t): token rows g and g+8, query columns 2t and 2t+1.
@@ -798,11 +816,21 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     // laid out half-major [2][rpc][64 halves], 128-byte swizzled by the tensor-map copies
     // (rpc = min(B, 16)).  FP8 stages hold plain [rows][128 codes], also 128-byte swizzled:
     // 16-byte piece c of row r sits at piece c ^ (r % 8).
-    const int rs = (a.B < CT ? a.B : CT) == 16 ? 4 : 3;
-    auto tile_off = [rs](int tok, int x) -> uint32_t {
+    // With head-pair stages a copy holds 2*rpc rows (head 0's rpc rows, then head 1's), so
+    // this warp's token tok of a copy sits e*rpc rows further.
+    const int rpc_ = a.B < CT ? a.B : CT;
+    const int rs = rpc_ == 32 ? 5 : (rpc_ == 16 ? 4 : 3);
+    const int cs = rs + (C::PR ? 1 : 0);             // log2 rows of one copy (per half for fp16)
+    const int erow = C::PR ? (e << rs) : 0;
+    auto tile_off = [rs, cs, erow](int tok, int x) -> uint32_t {
         const int rpc = 1 << rs;
-        return swz128(static_cast<uint32_t>(((tok >> rs) << (rs + 8)) + ((((x >> 7) << rs) + (tok & (rpc - 1))) << 7) +
-                                            (x & 127)));
+        return swz128(static_cast<uint32_t>(((tok >> rs) << (cs + 8)) +
+                                            ((((x >> 7) << cs) + erow + (tok & (rpc - 1))) << 7) + (x & 127)));
+    };
+    // FP8 stages: the stage row of this warp's token tok (rows % 8 are those of tok)
+    auto row8 = [rs, erow](int tok) -> int {
+        if constexpr (C::PR) return ((tok >> rs) << (rs + 1)) + erow + (tok & ((1 << rs) - 1));
+        else return tok;
     };
     uint32_t qa[8][2];                 // B fragments of Q^T: query g, dims 16k+2t.. and 16k+8+2t..
     float ot[8][4];                    // O^T tile i: dims 16i+g / 16i+g+8, queries 2t / 2t+1
@@ -818,16 +846,17 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
     for (int j = 0;; ++j) {
         const int st = j % NSW;
         const uint32_t par = (j / NSW) & 1;
-        const uint32_t fb = smem_u32(&bars[w * NSW + st]);
+        const uint32_t fb = smem_u32(&bars[wr * NSW + st]);
         if (!mbar_wait_bounded(fb, par, a.err)) {
             mbar_wait_bounded(fb, par, a.err);      // let copies in flight land, then leave
             break;
         }
-        char* stg = smem + (w * NSW + st) * C::STAGE;
-        const Meta* mp = reinterpret_cast<const Meta*>(smem + C::META_R + (w * NSW + st) * sizeof(Meta));
+        char* stg = smem + (wr * NSW + st) * C::STAGE;
+        const Meta* mp = reinterpret_cast<const Meta*>(smem + C::META_R + (wr * NSW + st) * sizeof(Meta));
         const int flags = mp->flags;
         if (flags & F_TERM) break;
-        const int nt = mp->ntok, lo = mp->lo, ms = mp->s, mh = mp->h, mpart = mp->p;
+        const int nt = mp->ntok, lo = mp->lo, ms = mp->s, mpart = mp->p;
+        const int mh = C::PR ? 2 * mp->h + e : mp->h;   // this warp's K/V head
         // query rows of the item: G heads of one sequence, or (shared prefixes) one head of
         // the nq sequences ms .. ms+nq-1
         const int nq = C::PFX ? mp->nq : G;
@@ -838,13 +867,13 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             #pragma unroll
             for (int i = 0; i < 8; ++i) { ot[i][0] = ot[i][1] = ot[i][2] = ot[i][3] = 0.f; }
             // B fragments of the G query rows (fp16: staged with the item's first chunk;
-            // FP8: read from global memory once per item)
+            // FP8 and head-pair stages: read from global memory once per item)
             const bool real = g < nq && nt > 0;
             const int64_t qr = C::PFX ? static_cast<int64_t>(ms + (real ? g : 0)) * a.H + mh
                                       : (static_cast<int64_t>(ms) * a.H + mh) * G + (real ? g : 0);
-            const uint32_t* qrow = C::FP8
+            const uint32_t* qrow = (C::FP8 || C::PR)
                 ? reinterpret_cast<const uint32_t*>(static_cast<const char*>(a.q) + qr * D * 2)
-                : reinterpret_cast<const uint32_t*>(smem + C::QR_OFF + (w * NSW + st) * C::QR_BYTES +
+                : reinterpret_cast<const uint32_t*>(smem + C::QR_OFF + (wr * NSW + st) * C::QR_BYTES +
                                                     (real ? g : 0) * D * 2);
             #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -867,9 +896,9 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             const int64_t sh = static_cast<int64_t>(ms) * a.H + mh;
             const int64_t grow = (static_cast<int64_t>(mp->patch_id) * a.H + mh) * a.B + mp->patch_off;
             // K and V rows sit 128-byte swizzled in the stage (16-byte piece c of row r at c ^ (r % 8))
-            patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, stg + C::K_OFF + r * C::ROW,
+            patch_row<C>(a.k_new + sh * D * a.in_bytes, a.in_bytes, stg + C::K_OFF + row8(r) * C::ROW,
                          a.kpool + grow * C::ROW, __ldg(a.kscale + mp->patch_id), lane, r & 7);
-            patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, stg + C::V_OFF + r * C::ROW,
+            patch_row<C>(a.v_new + sh * D * a.in_bytes, a.in_bytes, stg + C::V_OFF + row8(r) * C::ROW,
                          a.vpool + grow * C::ROW, __ldg(a.vscale + mp->patch_id), lane, r & 7);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
@@ -939,11 +968,12 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                 // no bank conflicts.
                 uint4 kw[2][2];
                 if constexpr (C::FP8) {
-                    const char* kr0 = stg + C::K_OFF + (t16 + g) * C::ROW;
+                    const char* kr0 = stg + C::K_OFF + row8(t16 + g) * C::ROW;
+                    const char* kr1 = stg + C::K_OFF + row8(t16 + g + 8) * C::ROW;
                     #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         kw[0][j] = *reinterpret_cast<const uint4*>(kr0 + (((2 * t + j) ^ g) << 4));
-                        kw[1][j] = *reinterpret_cast<const uint4*>(kr0 + 8 * C::ROW + (((2 * t + j) ^ g) << 4));
+                        kw[1][j] = *reinterpret_cast<const uint4*>(kr1 + (((2 * t + j) ^ g) << 4));
                     }
                 }
                 #pragma unroll
@@ -1029,7 +1059,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
                     #pragma unroll
                     for (int pp = 0; pp < 4; ++pp) {
                         const int tile = 2 * pp + (lane >> 4);
-                        const uint32_t addr = vzero ? zaddr : vbase + vr * C::ROW + ((tile ^ (vr & 7)) << 4);
+                        const uint32_t addr = vzero ? zaddr : vbase + row8(vr) * C::ROW + ((tile ^ (vr & 7)) << 4);
                         uint32_t r[4];
                         ldsm_b8_x2_t(addr, r);
                         mma_16816(ot[2 * pp], e4m3x2_to_half2_bits(static_cast<uint16_t>(r[0] & 0xffffu)),
@@ -1054,7 +1084,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars[C::NC * NSW + w * NSW + st]));
+        if (lane == 0) mbar_arrive(smem_u32(&bars[C::NR * NSW + wr * NSW + st]));
         if constexpr (C::PFX) pfx_ticket_resolve<D>(a, ptk, lane);   // the previous item's tickets
         else ticket_resolve<D, G>(a, tk, lane);
         if (C::PFX && (flags & F_LAST)) {
@@ -1170,21 +1200,23 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
 
 template <typename C>
 __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(const __grid_constant__ AttnArgs a) {
-    constexpr int NC = C::NC, NSW = C::NSW, D = C::D, CT = C::CT, TPL = C::TPL, DPL = C::DPL;
+    constexpr int NC = C::NC, NR = C::NR, NSW = C::NSW, D = C::D, CT = C::CT, TPL = C::TPL, DPL = C::DPL;
     constexpr int CBMAX = C::CBMAX;
     extern __shared__ __align__(128) char smem_raw[];
     // swizzled stages need a 1024-byte aligned base (the slack is part of C::SMEM)
     char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) * (C::MMA ? 1 : 0);
     static_assert(!C::MMA || (C::STAGE % 1024 == 0 || !C::SWZ_STAGE), "swizzled stages 1024-aligned");
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);   // full[NC*NSW], empty[NC*NSW]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);   // full[NR*NSW], empty[NR*NSW]
     int* s_ctx = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
     int* s_end = s_ctx + kMaxBatch;
     int* s_pfx = s_ctx + 2 * kMaxBatch;         // shared prefixes (PFX launches only)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int HU = a.H / C::HP;                 // work units (single heads or head pairs) per sequence
+    const int HU = a.H / C::KVH;                // work units (single K/V heads or head groups) per sequence
 
     if (tid == 0) {
-        for (int i = 0; i < 2 * NC * NSW; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        // full barriers: the producer's arrival (with the copies' bytes); empty barriers: the
+        // release by the stage's consumer warp (both warps of a head pair)
+        for (int i = 0; i < 2 * NR * NSW; ++i) mbar_init(smem_u32(&bars[i]), i < NR * NSW ? 1 : NC / NR);
         fence_mbar_init();
     }
     if (tid < 32) reinterpret_cast<uint32_t*>(smem + C::ZERO_OFF)[tid] = 0u;   // read after the prologue's sync
@@ -1236,7 +1268,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         __syncthreads();
         for (int s = tid; s < a.batch; s += C::THREADS) {
             const int S = s_pfx[s] & kPfxTokMask, k = s_pfx[s] >> 24;
-            s_end[s] = (k ? a.H * pfx_shared_parts(S, a.P) : 0) + a.H * pfx_own_parts(s_ctx[s], S, a.P);
+            s_end[s] = (k ? HU * pfx_shared_parts(S, a.P) : 0) + HU * pfx_own_parts(s_ctx[s], S, a.P);
         }
         __syncthreads();
     }
@@ -1252,7 +1284,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 alt += HU * nparts_of(c - attend_first(c, a.window, a.B < CT ? a.B : CT), a.P_alt);
             }
             alt = __reduce_add_sync(FULL, alt);
-            if (alt <= static_cast<int>(gridDim.x) * NC) {
+            if (alt <= static_cast<int>(gridDim.x) * NR) {
                 P_eff = a.P_alt;
                 for (int s = lane; s < a.batch; s += 32) {
                     const int c = s_ctx[s];
@@ -1280,17 +1312,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
     const int P_eff = s_misc[0];                // the launch's partition size
 
     auto full_bar = [&](int w, int st) { return smem_u32(&bars[w * NSW + st]); };
-    auto empty_bar = [&](int w, int st) { return smem_u32(&bars[NC * NSW + w * NSW + st]); };
+    auto empty_bar = [&](int w, int st) { return smem_u32(&bars[NR * NSW + w * NSW + st]); };
     auto stage_ptr = [&](int w, int st) { return smem + (w * NSW + st) * C::STAGE; };
 
     if (warp == NC) {
         // ================================================================ producer
-        // Lane w feeds consumer w; lanes >= NC only take part in warp votes.
-        const bool mine = lane < NC;
+        // Lane w feeds ring w (consumer w, or the head pair of consumers 2w, 2w+1); lanes
+        // >= NR only take part in warp votes.
+        const bool mine = lane < NR;
         const int w = mine ? lane : 0;
         const int rpc = a.B < CT ? a.B : CT;           // token rows per copy (whole block if B <= CT)
-        // bytes per copy: rpc rows of each of the item's HP heads (adjacent in the pool)
-        const uint32_t tile = static_cast<uint32_t>(rpc) * C::ROW * C::HP;
+        // bytes per copy: rpc rows of each of the item's KVH heads (adjacent in the pool)
+        const uint32_t tile = static_cast<uint32_t>(rpc) * C::ROW * C::KVH;
         // Items are claimed one at a time: the next one only while the current item's last
         // two chunks are filled (its atomic then has a chunk's time to return), so no lane
         // holds more than two items and the tail stays balanced when items are few.
@@ -1299,11 +1332,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
         // the first item of every lane is fixed, so the first copies need no atomic round
         // trip; claimed items are numbered after them.  Lane-major order spreads a job with
         // fewer items than consumer warps evenly over the SMs.
-        const unsigned first_claim = gridDim.x * NC;
+        const unsigned first_claim = gridDim.x * NR;
         auto claim = [&]() { pending = atomicAdd(a.counter, 1u) + first_claim; claimed = true; };
         auto decode = [&](unsigned idx) {
             if constexpr (C::PFX)
-                return decode_item_pfx<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, s_pfx, a.batch, a.H, P_eff);
+                return decode_item_pfx<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, s_pfx, a.batch, HU, P_eff);
             else
                 return decode_item<CT>(static_cast<int>(idx), n_items, s_ctx, s_end, a.batch, HU, P_eff, a.s_fine,
                                        a.P_fine, a.window, rpc);
@@ -1393,7 +1426,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(cons
                 #pragma unroll
                 for (int j = 0; j < CBMAX; ++j) {
                     if (j < nblk) {
-                        const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h * C::HP) * a.B +
+                        const int64_t toff = ((static_cast<int64_t>(ids[j]) * a.H + cur.h * C::KVH) * a.B +
                                               row0) * C::ROW;
                         if constexpr (C::SWZ_STAGE) {
                             // rpc token rows of one head as [2][rows][64], 128-byte swizzled
@@ -1805,8 +1838,8 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
         sa.s_base = s0;
         sa.counter = counters + sub;
         sa.exit_counter = counters + kMaxSub + sub;
-        const int64_t upper = static_cast<int64_t>(sa.batch) * (args.H / C::HP) * args.max_parts;
-        int64_t grid = (upper + C::NC - 1) / C::NC;
+        const int64_t upper = static_cast<int64_t>(sa.batch) * (args.H / C::KVH) * args.max_parts;
+        int64_t grid = (upper + C::NR - 1) / C::NR;
         if (grid > pool->num_sms) grid = pool->num_sms;
         if (grid < 1) grid = 1;
         if (plan.flags & KV_DECODE_PDL) {

@@ -10,10 +10,16 @@ namespace {
 template <typename C>
 int consumers_of() { return C::NC; }
 
+template <typename C>
+int rings_of() { return C::NR; }
+
 template <int G>
 int consumers_for_g(const kv_pool* pool) {
     const kv_pool_desc& d = pool->desc;
     if constexpr (G > 1) {                         // grouped-query tensor-core configuration
+        // head-pair stages (FP8): rings of two warps, each ring's items covering two K/V heads
+        if (d.dtype == KV_FP8_E4M3 && d.head_dim == 128 && pool->tmaps && pair_stages(pool, false))
+            return rings_of<Cfg<128, uint8_t, __half, G, true, 1, 0, false, true>>();
         if (d.dtype == KV_F16 && d.head_dim == 128 && pool->tmaps)
             return consumers_of<Cfg<128, __half, __half, G, true>>();
         if (d.dtype == KV_FP8_E4M3 && d.head_dim == 128 && pool->tmaps)
@@ -50,7 +56,28 @@ int head_group(const kv_pool_desc& d, int group) {
 #endif
 }
 
+bool pair_stages(const kv_pool* pool, bool prefix) {
+#if defined(KVP_NO_PAIR_STAGES)
+    (void)pool;
+    (void)prefix;
+    return false;                                  // tuning builds only
+#else
+    // Measured (GB300): shared-prefix launches +16 % (8 KiB instead of 4 KiB copies lift
+    // the per-SM copy rate that bounds them), FP8 grouped-query +4 %; fp16 grouped-query
+    // decode is bound by HBM already and ran 1 % slower, so it keeps one head per stage.
+    if (!pool->tmaps || !pool->pmaps || pool->desc.num_heads % 2 != 0) return false;
+    return prefix || pool->desc.dtype == KV_FP8_E4M3;
+#endif
+}
+
 namespace {
+
+// K/V heads covered by one work item of this launch shape: head groups of the single-query
+// CUDA-core consumer, or the head pairs of the tensor-core consumer
+int kv_heads_per_item(const kv_pool* pool, int group) {
+    if (group > 1 && pool->tmaps && pool->desc.head_dim == 128 && pair_stages(pool, false)) return 2;
+    return head_group(pool->desc, group);
+}
 
 int consumers_for(const kv_pool* pool, int group) {
     const int hp = head_group(pool->desc, group);
@@ -97,7 +124,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     } else if (partition_tokens == 0) {
         // work items are (sequence, KV head or head pair, partition), handed out dynamically
         const int64_t units = static_cast<int64_t>(batch > 0 ? batch : 1) * d.num_heads /
-                              head_group(d, group);
+                              kv_heads_per_item(pool, group);
         const int64_t warps = static_cast<int64_t>(pool->num_sms) * nc;
         int64_t parts;
         if (group == 1) {
@@ -138,7 +165,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
         // half-size partitions (measured: ragged 256 sequences +1 % fp16, +4 % FP8; with
         // 256-token items it gained nothing and the doubled split count of long contexts
         // cost 3 %).
-        const int hu = d.num_heads / head_group(d, group);
+        const int hu = d.num_heads / kv_heads_per_item(pool, group);
         const int64_t warps = static_cast<int64_t>(pool->num_sms) * nc;
         const int64_t items = static_cast<int64_t>(batch) * hu * ((span + P - 1) / P);
         if (items >= 2 * warps) {
@@ -160,6 +187,7 @@ int plan_attention(const kv_pool* pool, int batch, int max_context, int partitio
     plan->group = group;
     plan->window = window;
     plan->flags = 0;
+    plan->pairs = group > 1 && kv_heads_per_item(pool, group) == 2;
     size_t ws = kCounterBytes;                      // work and exit counters
     if (plan->max_parts > 1) {
         const size_t n = static_cast<size_t>(batch) * d.num_heads * group * plan->max_parts;
@@ -207,8 +235,13 @@ int plan_attention_prefix(const kv_pool* pool, int batch, int max_context, int p
     const int64_t launch_items = static_cast<int64_t>(batch < kMaxBatch ? batch : kMaxBatch) *
                                  d.num_heads * plan->max_parts;
     if (launch_items > (int64_t{1} << 30)) return KV_ERR_INVALID_ARG;
-    plan->consumers = d.dtype == KV_F16 ? consumers_of<Cfg<128, __half, __half, 8, true, 1, 0, true>>()
-                                        : consumers_of<Cfg<128, uint8_t, __half, 8, true, 1, 0, true>>();
+    plan->pairs = pair_stages(pool, true);
+    if (plan->pairs)
+        plan->consumers = d.dtype == KV_F16 ? rings_of<Cfg<128, __half, __half, 8, true, 1, 0, true, true>>()
+                                            : rings_of<Cfg<128, uint8_t, __half, 8, true, 1, 0, true, true>>();
+    else
+        plan->consumers = d.dtype == KV_F16 ? consumers_of<Cfg<128, __half, __half, 8, true, 1, 0, true>>()
+                                            : consumers_of<Cfg<128, uint8_t, __half, 8, true, 1, 0, true>>();
     plan->group = 1;
     plan->window = 0;
     plan->flags = 0;
@@ -290,8 +323,9 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
     a.qscale = scale * 1.4426950408889634f;        // log2(e): softmax evaluated with 2^x
     a.window = plan.window;
     if (pool->tmaps) {                             // the layer's swizzled tile maps
-        a.kmap = pool->tmaps[2 * layer];
-        a.vmap = pool->tmaps[2 * layer + 1];
+        const CUtensorMap* maps = plan.pairs ? pool->pmaps : pool->tmaps;
+        a.kmap = maps[2 * layer];
+        a.vmap = maps[2 * layer + 1];
     }
     a.fused = k_new != nullptr ? 1 : 0;
 
@@ -299,6 +333,15 @@ int launch_attention_append(const kv_pool* pool, int layer, const void* q, const
         if (!pool->tmaps || group != 1 || plan.window != 0) return KV_ERR_UNSUPPORTED;
         a.groups = plan.groups;
         a.n_groups = plan.n_groups;
+        if (plan.pairs) {
+            if (d.dtype == KV_F16)
+                return launch_typed<Cfg<128, __half, __half, 8, true, 1, 0, true, true>>(pool, a, plan, counters,
+                                                                                          stream);
+            if (d.dtype == KV_FP8_E4M3)
+                return launch_typed<Cfg<128, uint8_t, __half, 8, true, 1, 0, true, true>>(pool, a, plan, counters,
+                                                                                           stream);
+            return KV_ERR_UNSUPPORTED;
+        }
         if (d.dtype == KV_F16)
             return launch_typed<Cfg<128, __half, __half, 8, true, 1, 0, true>>(pool, a, plan, counters, stream);
         if (d.dtype == KV_FP8_E4M3)

@@ -23,6 +23,9 @@ int launch_g(const kv_pool* pool, const AttnArgs& a, const AttnPlan& plan, unsig
         if (d.head_dim == 128) {
             // tensor cores when the pool has its swizzled tensor maps (K and V fragments
             // converted in registers from the E4M3 codes), else CUDA cores
+            if (pool->tmaps && plan.pairs)           // head-pair stages
+                return launch_typed<Cfg<128, uint8_t, __half, G, true, 1, 0, false, true>>(pool, a, plan, counters,
+                                                                                            stream);
             if (pool->tmaps) return launch_typed<Cfg<128, uint8_t, __half, G, true>>(pool, a, plan, counters, stream);
             return launch_typed<Cfg<128, uint8_t, __half, G>>(pool, a, plan, counters, stream);
         }

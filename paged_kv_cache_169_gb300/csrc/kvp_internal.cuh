@@ -21,6 +21,9 @@ struct kv_pool {
     // [rows = num_blocks*H*B][2][64] halves with a {64, 2, min(B,16)} box and 128-byte
     // swizzle (the grouped-query tensor-core path); nullptr when unavailable
     CUtensorMap* tmaps;  // [2 * num_layers], 64-byte aligned
+    // the same views with boxes of 2*B rows (a block's tiles of two adjacent heads) for the
+    // head-pair stages: fp16 pools with B <= 16 and FP8 pools; nullptr otherwise
+    CUtensorMap* pmaps;  // [2 * num_layers]
     void* tmaps_raw;
 };
 
@@ -57,6 +60,7 @@ struct AttnPlan {
     int consumers;       // consumer warps per CTA
     int group;           // query heads per KV head
     int window;          // > 0: sliding window of the last `window` tokens
+    bool pairs = false;  // tensor-core consumer with head-pair stages
     const int32_t* groups = nullptr;   // shared prompt prefixes: device [n_groups][3], or none
     int n_groups = 0;
     size_t ws_bytes;     // workspace bytes
@@ -70,6 +74,9 @@ struct AttnPlan {
 };
 // group: query heads per KV head (1, or 2/4/8 for fp16 and FP8 pools)
 bool valid_group(const kv_pool_desc& d, int group);
+// whether a tensor-core launch on this pool (prefix: with shared prompt prefixes) uses
+// head-pair stages
+bool pair_stages(const kv_pool* pool, bool prefix);
 // heads per work item of this pool's single-query decode (1, 2 or 4)
 int head_group(const kv_pool_desc& d, int group);
 int plan_attention(const kv_pool* pool, int batch, int max_context, int partition_tokens,

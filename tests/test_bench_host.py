@@ -54,4 +54,4 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
 def test_default_launch_flags():
     assert bench.LAUNCH_FLAGS[bench.default_launch_flags("llama13b")] == 1 | 2 | 4 | 16
     assert bench.LAUNCH_FLAGS[bench.default_launch_flags("decode7b")] == 1 | 2 | 4 | 16
-    assert bench.LAUNCH_FLAGS[bench.default_launch_flags("parallel")] == 1 | 2 | 4
+    assert bench.LAUNCH_FLAGS[bench.default_launch_flags("parallel")] == 1 | 2 | 4 | 16

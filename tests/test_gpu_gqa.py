@@ -65,6 +65,25 @@ def test_gqa_against_oracle(G, dtype, d, B):
     assert cache.device_error() == 0
 
 
+@pytest.mark.parametrize("G", [2, 8])
+@pytest.mark.parametrize("dtype", ["f16", "fp8"])
+def test_gqa_odd_kv_head_count(G, dtype):
+    """Three K/V heads: FP8 pools cannot pair heads per stage here (pairs need an even
+    count), so this runs the one-head-per-stage tensor-core shape that even counts skip."""
+    lens = [0, 1, 17, 513, 1400]
+    w, cache, alloc, seqs, ks, vs = _setup(G, 3, 128, 16, dtype, 90 + G, lens)
+    prefill(cache, alloc, seqs, ks, vs)
+    bt, cl, _ = tables_for(alloc, seqs, max(-(-n // 16) for n in lens))
+    q = W.host_queries(w)
+    kd, vd = _oracle_values(dtype, ks, vs)
+    want = OA.decode_attention_gqa(q, kd, vd, w.scale)
+    for P in (0, 64):
+        out = cache.attention_gqa(0, torch.from_numpy(q).cuda(), bt, cl, max(lens), w.scale,
+                                  partition_tokens=P).cpu().numpy()
+        assert max_abs(out, want) <= tol_for("f16"), (P, max_abs(out, want))
+    assert cache.device_error() == 0
+
+
 @pytest.mark.parametrize("G,dtype", [(4, "f16"), (8, "fp8"), (2, "f16")])
 def test_gqa_fused_append_equals_append_then_attention(G, dtype):
     lens = [1, 33, 300, 1025]

@@ -217,6 +217,18 @@ def test_prefix_groups_against_oracle(dtype, B, fused):
     assert cache.device_error() == 0
 
 
+@pytest.mark.parametrize("dtype", ["f16", "fp8"])
+def test_prefix_groups_odd_head_count(dtype):
+    """Three heads: the head-pair stages need an even count, so this runs the one-head-per-
+    stage shape of the shared-prefix launch."""
+    c = _build_batch(dtype, 16, False, seed=680, H=3)
+    grp = _groups(c["groups"])
+    out = c["cache"].attention_ex(0, torch.from_numpy(c["q"]).cuda(), c["bt"], c["cl"], max(c["lens"]),
+                                  c["scale"], prefix_groups=grp)
+    assert max_abs(out.cpu().numpy(), c["want"]) <= tol_for("f16")
+    assert c["cache"].device_error() == 0
+
+
 def _simple_batch(lens_prompt=64, members=6, own=(3, 20, 1, 7, 40, 2), B=16, H=2, seed=700):
     d = 128
     nb = 64
