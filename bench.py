@@ -631,6 +631,73 @@ def abi_workspace_bytes(cache, batch, max_ctx, partition, prefix_groups):
     return abi.paged_decode_workspace_size_ex(cache.handle, a)
 
 
+def host_step_loop(cache, alloc, seqs, q_h, k_h, v_h, max_blocks, max_ctx, scale, stream, groups=None,
+                   partition=0):
+    """The decode loop as a caller runs it, through the C ABI, every step:
+      1. the host allocator reserves each sequence's next slot (kv_alloc_append_slots), which
+         plans a block copy when the slot lies in a shared block;
+      2. it writes the block tables and lengths into pinned host memory
+         (kv_alloc_build_tables);
+      3. tables, lengths, the planned block pairs and the step's q / new K / new V are
+         copied to the device;
+      4. the planned block copies run (kv_copy_blocks);
+      5. the fused append + attention runs (paged_decode_attention_ex: zeroed workspace and
+         programmatic dependent launch; a host copy precedes every call, so no early flags);
+      6. the outputs are copied back to pinned host memory.
+    q_h, k_h, v_h: pinned host [steps, batch, H, d].  Returns (ms for all steps, H2D bytes,
+    D2H bytes, block copies, the pinned outputs)."""
+    import ctypes
+    import torch
+    from paged_kv_cache_169_gb300 import abi
+
+    S, n = q_h.shape[0], q_h.shape[1]
+    dev = cache.k[0].device
+    pin_bt = torch.empty((S, n, max_blocks), dtype=torch.int32).pin_memory()
+    pin_cl = torch.empty((S, n), dtype=torch.int32).pin_memory()
+    pin_pairs = torch.empty((S, n, 2), dtype=torch.int32).pin_memory()
+    pin_out = torch.empty(q_h.shape, dtype=torch.float32).pin_memory()
+    d_bt = torch.empty((n, max_blocks), dtype=torch.int32, device=dev)
+    d_cl = torch.empty(n, dtype=torch.int32, device=dev)
+    d_pairs = torch.empty((n, 2), dtype=torch.int32, device=dev)
+    d_q, d_k, d_v = (torch.empty(q_h.shape[1:], dtype=q_h.dtype, device=dev) for _ in range(3))
+    d_out = torch.empty(q_h.shape[1:], dtype=torch.float32, device=dev)
+    ws = cache.zeroed_workspace(n, max_ctx, partition, prefix_groups=groups is not None)
+    seq_arr = (ctypes.c_int32 * n)(*seqs)
+    flags = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL
+    h2d = d2h = copies = 0
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(S):
+            pairs = []
+            for sid in seqs:
+                _, cow = alloc.append_slots(sid, 1)
+                if cow:
+                    pairs.append(cow)
+            abi.kv_alloc_build_tables_into(alloc.handle, seq_arr, n, pin_bt[i].data_ptr(), max_blocks,
+                                           pin_cl[i].data_ptr())
+            d_bt.copy_(pin_bt[i], non_blocking=True)
+            d_cl.copy_(pin_cl[i], non_blocking=True)
+            d_q.copy_(q_h[i], non_blocking=True)
+            d_k.copy_(k_h[i], non_blocking=True)
+            d_v.copy_(v_h[i], non_blocking=True)
+            h2d += (pin_bt[i].numel() + pin_cl[i].numel()) * 4 + 3 * q_h[i].numel() * q_h.element_size()
+            if pairs:
+                pin_pairs[i, :len(pairs)] = torch.tensor(pairs, dtype=torch.int32)
+                d_pairs[:len(pairs)].copy_(pin_pairs[i, :len(pairs)], non_blocking=True)
+                cache.copy_blocks(d_pairs[:len(pairs)], stream=stream)
+                h2d += len(pairs) * 8
+                copies += len(pairs)
+            cache.attention_ex(0, d_q, d_bt, d_cl, max_ctx, scale, k_new=d_k, v_new=d_v, out=d_out,
+                               partition_tokens=partition, workspace=ws, stream=stream, flags=flags,
+                               prefix_groups=groups)
+            pin_out[i].copy_(d_out, non_blocking=True)
+            d2h += d_out.numel() * 4
+        ev[1].record(stream)
+    stream.synchronize()
+    return ev[0].elapsed_time(ev[1]), h2d, d2h, copies, pin_out
+
+
 def _flush_l2(buf):
     buf.add_(1)                                         # 256 MB write: evicts the 129 MB L2
 
@@ -716,7 +783,8 @@ def run_decode_steps(args):
     graph_ms = timed(graph.replay)
     clk = clocks.stop()
     eager_ms = timed(loop)
-    # end to end: the 64 steps' q / k / v from pinned host memory, the outputs back
+    # end to end: the 64 steps' q / k / v from pinned host memory, the outputs back, around
+    # the replayed graph
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, kn, vn))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
@@ -727,7 +795,25 @@ def run_decode_steps(args):
         graph.replay()
         hout.copy_(out, non_blocking=True)
 
-    e2e_ms = timed(e2e)
+    graph_e2e_ms = timed(e2e)
+    # end to end with the host step of every decode step (host_step_loop): the host
+    # allocator holds the 8 sequences at their lengths before the loop (the prefill, not
+    # timed; its tables map the same pool) and reserves one slot per sequence per step
+    from paged_kv_cache_169_gb300.cache import BlockAllocator
+    runs = []
+    for rep in range(1 + max(2, min(args.steps, 5))):
+        alloc = BlockAllocator(w.num_blocks, BS, W.free_order(w))
+        seqs = [alloc.new_seq() for _ in init]
+        for sid, n in zip(seqs, init):
+            alloc.append_slots(sid, n)
+        with torch.cuda.stream(stream):
+            _flush_l2(flush)
+        run_ms, h2d, d2h, _, _ = host_step_loop(cache, alloc, seqs, hq, hk, hv, max(nbs), max_ctx, w.scale, stream,
+                                                partition=args.partition)
+        alloc.close()
+        if rep:
+            runs.append(run_ms)
+    e2e_ms = sum(runs) / len(runs)
     if cache.device_error():
         raise SystemExit("device error during the decode loop")
     peak, peak_src = measured_peak()
@@ -745,8 +831,14 @@ def run_decode_steps(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_replay": step_bytes},
         "e2e": {"value": step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 4,
-                "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "step": "64 decode steps through the C ABI, each: allocator slot reservation, tables into "
+                        "pinned memory, H2D of tables, lengths, q and new K/V, the fused call, D2H of the "
+                        "outputs"},
+        "e2e_graph": {"value": step_bytes / (graph_e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                      "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 4,
+                      "ms_per_step": graph_e2e_ms,
+                      "step": "the 64 steps' q / new K / new V copied in, the graph replayed, outputs copied out"},
         "gpu_launches": S, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -867,6 +959,29 @@ def run_parallel(args):
     eager_ms = timed(loop)
     if cache.device_error():
         raise SystemExit("device error during parallel sampling")
+    # end to end with the host step of every decode step (host_step_loop), from the forked
+    # state each time (the fork itself is the prefill, not timed); the first run warms up
+    pin_q, pin_k, pin_v = (t.cpu().pin_memory() for t in (q, kn, vn))
+    runs = []
+    for rep in range(1 + max(2, min(args.steps, 5))):
+        a2 = BlockAllocator(w.num_blocks, BS, W.free_order(w))
+        r2 = a2.new_seq()
+        a2.append_slots(r2, prompt)
+        c2 = [r2] + [a2.fork(r2) for _ in range(C - 1)]
+        with torch.cuda.stream(stream):
+            _flush_l2(flush)
+        run_ms, h2d, d2h, n_copies, host_out = host_step_loop(cache, a2, c2, pin_q, pin_k, pin_v, max_blocks, max_ctx,
+                                                              w.scale, stream, groups=groups,
+                                                              partition=args.partition)
+        a2.close()
+        if rep:
+            runs.append(run_ms)
+    e2e_ms = sum(runs) / len(runs)
+    # the same decisions and inputs as the timed graph: the same result, bit for bit
+    if n_copies != n_cow or not torch.equal(host_out.view(torch.int32), out.cpu().view(torch.int32)):
+        raise SystemExit("host-step loop: results differ from the timed loop's")
+    if cache.device_error():
+        raise SystemExit("device error during parallel sampling")
     peak, peak_src = measured_peak()
     uniq_gbs = unique / (ms / 1e3) / 1e9
     line = {
@@ -881,6 +996,11 @@ def run_parallel(args):
                    "step": "128 x (block copies + fused append + attention), one CUDA graph per timed step"},
         "seq_steps_per_s": C * S / (ms / 1e3),
         "eager": {"ms_per_128_steps": eager_ms, "unique_GB/s": unique / (eager_ms / 1e3) / 1e9},
+        "e2e": {"value": unique / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "step": "128 decode steps through the C ABI, each: allocator slot reservation (copy-on-write "
+                        "plan), tables into pinned memory, H2D of tables, lengths, block pairs, q and new K/V, "
+                        "kv_copy_blocks when planned, the fused call, D2H of the outputs"},
         "logical_GB/s": logical / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": uniq_gbs, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": uniq_gbs / peak, "traffic": None, "unique_bytes_per_run": unique,

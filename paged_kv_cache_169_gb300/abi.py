@@ -355,6 +355,13 @@ def kv_alloc_build_tables(a: int, seqs, max_blocks: int):
     return [flat[i * max_blocks:(i + 1) * max_blocks] for i in range(n)], list(lens)[:n]
 
 
+def kv_alloc_build_tables_into(a: int, seqs, n: int, tables: int, max_blocks: int, context_lens: int) -> None:
+    """kv_alloc_build_tables writing into caller memory: seqs a ctypes int32 array of n ids,
+    tables / context_lens host addresses of int32 [n][max_blocks] / [n] (e.g. pinned)."""
+    _check("kv_alloc_build_tables", load().kv_alloc_build_tables(a, _i32(seqs), n, C.cast(tables, _I32P), max_blocks,
+                                                                 C.cast(context_lens, _I32P)))
+
+
 def kv_alloc_ref_count(a: int, block: int) -> int:
     r = C.c_int()
     _check("kv_alloc_ref_count", load().kv_alloc_ref_count(a, block, C.byref(r)))
