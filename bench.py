@@ -96,18 +96,27 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel_srcs):
-    """DRAM bytes per launch from the committed ncu summary, only if the kernel sources
-    (device code and its launch code) are unchanged since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "attention_llama13b_traffic.txt")
+KERNEL_SRCS = ("attention_kernel.cuh", "kvp_internal.cuh", "decode_attention.cu", "decode_attention_gqa.cu")
+
+
+def kernel_sources_hash() -> str:
+    """sha256 (16 hex digits) of the decode kernel's device and launch code."""
+    src = [os.path.join(ROOT, "paged_kv_cache_169_gb300", "csrc", f) for f in KERNEL_SRCS]
+    return hashlib.sha256(b"".join(open(f, "rb").read() for f in src)).hexdigest()[:16]
+
+
+def traffic_record(workload: str):
+    """DRAM bytes per launch of the workload's attention kernel from the committed ncu record
+    profiles/traffic_<workload>.txt, only if the kernel sources are unchanged since the
+    counters were taken (else None)."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
     try:
         rec = {}
         for line in open(path):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 rec[k.strip()] = v.strip()
-        h = hashlib.sha256(b"".join(open(f, "rb").read() for f in kernel_srcs)).hexdigest()[:16]
-        if rec.get("source_sha256_16") == h:
+        if rec.get("source_sha256_16") == kernel_sources_hash():
             return float(rec["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -522,9 +531,7 @@ def run_ours(args):
     value = job_throughput(world, step_bytes, args.steps, elapsed_ms)
     peak, peak_src = measured_peak()
     achieved = call_bytes / (attn_ms_mean / 1e3) / 1e9
-    src = [os.path.join(ROOT, "paged_kv_cache_169_gb300", "csrc", f)
-           for f in ("attention_kernel.cuh", "decode_attention.cu")]
-    traffic = traffic_record(src) if (args.workload == "llama13b" and not args.window) else None
+    traffic = traffic_record(args.workload) if not (args.window or args.unfused or args.block_size) else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_rate(w, args.cpu_units)
@@ -829,7 +836,9 @@ def run_decode_steps(args):
         "seq_steps_per_s": w.batch * S / (graph_ms / 1e3),
         "eager": {"ms_per_64_steps": eager_ms, "GB/s": step_bytes / (eager_ms / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_replay": step_bytes},
+                     "frac": achieved / peak, "traffic": traffic_record("decode7b"),
+                     "traffic_note": "DRAM bytes of one launch (one decode step), ncu",
+                     "algorithmic_bytes_per_replay": step_bytes},
         "e2e": {"value": step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "step": "64 decode steps through the C ABI, each: allocator slot reservation, tables into "
@@ -1003,7 +1012,9 @@ def run_parallel(args):
                         "kv_copy_blocks when planned, the fused call, D2H of the outputs"},
         "logical_GB/s": logical / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": uniq_gbs, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": uniq_gbs / peak, "traffic": None, "unique_bytes_per_run": unique,
+                     "frac": uniq_gbs / peak, "traffic": traffic_record("parallel"),
+                     "traffic_note": "DRAM bytes of one launch (one decode step), ncu",
+                     "unique_bytes_per_run": unique,
                      "logical_bytes_per_run": logical},
         "gpu_launches": S + sum(c is not None for c in cows), "clocks": clk,
     }

@@ -55,3 +55,24 @@ def test_default_launch_flags():
     assert bench.LAUNCH_FLAGS[bench.default_launch_flags("llama13b")] == 1 | 2 | 4 | 16
     assert bench.LAUNCH_FLAGS[bench.default_launch_flags("decode7b")] == 1 | 2 | 4 | 16
     assert bench.LAUNCH_FLAGS[bench.default_launch_flags("parallel")] == 1 | 2 | 4 | 16
+
+
+def test_traffic_record_only_for_the_measured_kernel_sources(tmp_path, monkeypatch):
+    """A stored ncu traffic figure is reported only while the kernel sources hash to the
+    version it was measured on."""
+    import shutil
+    src = tmp_path / "paged_kv_cache_169_gb300" / "csrc"
+    src.mkdir(parents=True)
+    for f in bench.KERNEL_SRCS:
+        shutil.copy(os.path.join(bench.ROOT, "paged_kv_cache_169_gb300", "csrc", f), src / f)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_sources_hash()
+    assert len(h) == 16
+    (tmp_path / "profiles" / "traffic_w.txt").write_text(
+        f"# test\nsource_sha256_16: {h}\ndram_bytes_per_launch: 1234\n")
+    assert bench.traffic_record("w") == 1234.0
+    assert bench.traffic_record("other") is None
+    with open(src / bench.KERNEL_SRCS[0], "a") as f:
+        f.write("// changed\n")
+    assert bench.traffic_record("w") is None
