@@ -641,65 +641,73 @@ def abi_workspace_bytes(cache, batch, max_ctx, partition, prefix_groups):
 def host_step_loop(cache, alloc, seqs, q_h, k_h, v_h, max_blocks, max_ctx, scale, stream, groups=None,
                    partition=0):
     """The decode loop as a caller runs it, through the C ABI, every step:
-      1. the host allocator reserves each sequence's next slot (kv_alloc_append_slots), which
-         plans a block copy when the slot lies in a shared block;
-      2. it writes the block tables and lengths into pinned host memory
-         (kv_alloc_build_tables);
-      3. tables, lengths, the planned block pairs and the step's q / new K / new V are
-         copied to the device;
-      4. the planned block copies run (kv_copy_blocks);
-      5. the fused append + attention runs (paged_decode_attention_ex: zeroed workspace and
-         programmatic dependent launch; a host copy precedes every call, so no early flags);
+      1. the host allocator reserves every sequence's next slot in one call
+         (kv_alloc_decode_step), planning a block copy where a slot lies in a shared block;
+      2. it writes the block tables and lengths into a pinned staging buffer
+         (kv_alloc_build_tables), beside the planned block pairs;
+      3. that buffer goes to the device in one copy, and the step's q / new K / new V
+         (packed in pinned memory) in another;
+      4. the planned block copies run (kv_copy_blocks, every layer);
+      5. the fused append + attention runs (paged_decode_attention_ex with an argument block
+         built once: zeroed workspace and programmatic dependent launch; a host copy precedes
+         every call, so no early flags);
       6. the outputs are copied back to pinned host memory.
-    q_h, k_h, v_h: pinned host [steps, batch, H, d].  Returns (ms for all steps, H2D bytes,
-    D2H bytes, block copies, the pinned outputs)."""
+    q_h, k_h, v_h: host [steps, batch, H, d].  Returns (ms for all steps, H2D bytes, D2H
+    bytes, block copies, the pinned outputs)."""
     import ctypes
     import torch
     from paged_kv_cache_169_gb300 import abi
 
     S, n = q_h.shape[0], q_h.shape[1]
     dev = cache.k[0].device
-    pin_bt = torch.empty((S, n, max_blocks), dtype=torch.int32).pin_memory()
-    pin_cl = torch.empty((S, n), dtype=torch.int32).pin_memory()
-    pin_pairs = torch.empty((S, n, 2), dtype=torch.int32).pin_memory()
+    per = q_h[0].numel()
+    # per step: [tables n*max_blocks | lengths n | block pairs 2n] int32, and q | k | v
+    width = n * max_blocks + n + 2 * n
+    pin_meta = torch.empty((S, width), dtype=torch.int32).pin_memory()
+    pin_qkv = torch.empty((S, 3, n) + tuple(q_h.shape[2:]), dtype=q_h.dtype).pin_memory()
+    pin_qkv[:, 0].copy_(q_h)
+    pin_qkv[:, 1].copy_(k_h)
+    pin_qkv[:, 2].copy_(v_h)
     pin_out = torch.empty(q_h.shape, dtype=torch.float32).pin_memory()
-    d_bt = torch.empty((n, max_blocks), dtype=torch.int32, device=dev)
-    d_cl = torch.empty(n, dtype=torch.int32, device=dev)
-    d_pairs = torch.empty((n, 2), dtype=torch.int32, device=dev)
-    d_q, d_k, d_v = (torch.empty(q_h.shape[1:], dtype=q_h.dtype, device=dev) for _ in range(3))
+    d_meta = torch.empty(width, dtype=torch.int32, device=dev)
+    d_bt = d_meta[:n * max_blocks].view(n, max_blocks)
+    d_cl = d_meta[n * max_blocks:n * max_blocks + n]
+    d_pairs = d_meta[n * max_blocks + n:]
+    d_qkv = torch.empty(pin_qkv.shape[1:], dtype=q_h.dtype, device=dev)
     d_out = torch.empty(q_h.shape[1:], dtype=torch.float32, device=dev)
     ws = cache.zeroed_workspace(n, max_ctx, partition, prefix_groups=groups is not None)
     seq_arr = (ctypes.c_int32 * n)(*seqs)
-    flags = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL
+    slots = (ctypes.c_int64 * n)()
+    a = abi.kv_decode_args()                            # every pointer is fixed over the loop
+    a.layer, a.q, a.num_q_heads = 0, d_qkv[0].data_ptr(), 0
+    a.k_new, a.v_new, a.in_dtype = d_qkv[1].data_ptr(), d_qkv[2].data_ptr(), abi.KV_F16
+    a.out, a.block_tables, a.max_blocks_per_seq = d_out.data_ptr(), d_bt.data_ptr(), max_blocks
+    a.context_lens, a.batch, a.max_context = d_cl.data_ptr(), n, max_ctx
+    a.scale, a.partition_tokens = float(scale), partition
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    a.stream = stream.cuda_stream
+    a.flags = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL
+    if groups is not None:
+        a.prefix_groups, a.num_prefix_groups = groups.data_ptr(), groups.shape[0]
+    handle, layers = cache.handle, cache.num_layers
     h2d = d2h = copies = 0
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with torch.cuda.stream(stream):
         ev[0].record(stream)
         for i in range(S):
-            pairs = []
-            for sid in seqs:
-                _, cow = alloc.append_slots(sid, 1)
-                if cow:
-                    pairs.append(cow)
-            abi.kv_alloc_build_tables_into(alloc.handle, seq_arr, n, pin_bt[i].data_ptr(), max_blocks,
-                                           pin_cl[i].data_ptr())
-            d_bt.copy_(pin_bt[i], non_blocking=True)
-            d_cl.copy_(pin_cl[i], non_blocking=True)
-            d_q.copy_(q_h[i], non_blocking=True)
-            d_k.copy_(k_h[i], non_blocking=True)
-            d_v.copy_(v_h[i], non_blocking=True)
-            h2d += (pin_bt[i].numel() + pin_cl[i].numel()) * 4 + 3 * q_h[i].numel() * q_h.element_size()
-            if pairs:
-                pin_pairs[i, :len(pairs)] = torch.tensor(pairs, dtype=torch.int32)
-                d_pairs[:len(pairs)].copy_(pin_pairs[i, :len(pairs)], non_blocking=True)
-                cache.copy_blocks(d_pairs[:len(pairs)], stream=stream)
-                h2d += len(pairs) * 8
-                copies += len(pairs)
-            cache.attention_ex(0, d_q, d_bt, d_cl, max_ctx, scale, k_new=d_k, v_new=d_v, out=d_out,
-                               partition_tokens=partition, workspace=ws, stream=stream, flags=flags,
-                               prefix_groups=groups)
+            row = pin_meta[i]
+            base = row.data_ptr()
+            n_cow = abi.kv_alloc_decode_step(alloc.handle, seq_arr, n, slots, base + 4 * (n * max_blocks + n))
+            abi.kv_alloc_build_tables_into(alloc.handle, seq_arr, n, base, max_blocks, base + 4 * n * max_blocks)
+            d_meta.copy_(row, non_blocking=True)
+            d_qkv.copy_(pin_qkv[i], non_blocking=True)
+            h2d += width * 4 + 3 * per * q_h.element_size()
+            if n_cow:
+                abi.kv_copy_blocks(handle, d_pairs.data_ptr(), n_cow, 0, layers, a.stream)
+                copies += n_cow
+            abi.paged_decode_attention_ex(handle, a)
             pin_out[i].copy_(d_out, non_blocking=True)
-            d2h += d_out.numel() * 4
+            d2h += per * 4
         ev[1].record(stream)
     stream.synchronize()
     return ev[0].elapsed_time(ev[1]), h2d, d2h, copies, pin_out

@@ -461,6 +461,17 @@ KV_API int kv_alloc_seq_fork(kv_alloc* a, int parent, int* child);
 KV_API int kv_alloc_append_slots(kv_alloc* a, int seq, int count, int64_t* slots_out,
                           int32_t* cow_pair_out);
 
+/* One decode step's slots for a batch: reserve the next slot of each of the n sequences
+ * seqs[0..n-1] (host int32), in order, exactly as n calls kv_alloc_append_slots(seq, 1)
+ * would.  slots_out: host int64 [n]; cow_pairs_out: host int32 [n][2] receives the planned
+ * block copies (src, dst) in order, *n_cow their number (the caller runs kv_copy_blocks on
+ * them before the step writes).  The whole step is checked first: an unknown sequence gives
+ * KV_ERR_STATE and a free list too short for every block the step takes gives
+ * KV_ERR_NO_BLOCKS, with the state unchanged in both cases.  The per-step write path of
+ * [PagedAttention] §3.3 (write_to_block) for a batch; one call instead of one per sequence. */
+KV_API int kv_alloc_decode_step(kv_alloc* a, const int32_t* seqs, int n, int64_t* slots_out,
+                                int32_t* cow_pairs_out, int* n_cow);
+
 /* Sliding window: release every block of `seq` that lies wholly before token keep_from
  * (count - 1, back to the free list at 0) and set its table entry to -1; later entries
  * keep their logical positions and the length is unchanged.  *released (may be NULL)

@@ -82,6 +82,7 @@ _SIGS = {
     "kv_alloc_seq_new": (C.c_int, [_VP, C.POINTER(C.c_int)]),
     "kv_alloc_seq_fork": (C.c_int, [_VP, C.c_int, C.POINTER(C.c_int)]),
     "kv_alloc_append_slots": (C.c_int, [_VP, C.c_int, C.c_int, _I64P, _I32P]),
+    "kv_alloc_decode_step": (C.c_int, [_VP, _I32P, C.c_int, _I64P, _I32P, C.POINTER(C.c_int)]),
     "kv_alloc_seq_free": (C.c_int, [_VP, C.c_int]),
     "kv_alloc_seq_trim": (C.c_int, [_VP, C.c_int, C.c_int64, C.POINTER(C.c_int)]),
     "paged_decode_workspace_size_ex": (C.c_size_t, [_VP, _VP]),
@@ -316,6 +317,15 @@ def kv_alloc_append_slots(a: int, seq: int, count: int):
     _check("kv_alloc_append_slots", load().kv_alloc_append_slots(a, seq, count, _i64(slots), _i32(pair)))
     cow = (pair[0], pair[1]) if pair[0] >= 0 else None
     return list(slots), cow
+
+
+def kv_alloc_decode_step(a: int, seqs, n: int, slots_out, pairs_out) -> int:
+    """seqs: ctypes int32 array of n ids; slots_out: ctypes int64 [n]; pairs_out: ctypes int32
+    [2n] (or host addresses).  Returns the number of planned block copies."""
+    ncow = C.c_int(0)
+    _check("kv_alloc_decode_step", load().kv_alloc_decode_step(a, C.cast(seqs, _I32P), n, C.cast(slots_out, _I64P),
+                                                               C.cast(pairs_out, _I32P), C.byref(ncow)))
+    return ncow.value
 
 
 def kv_alloc_seq_trim(a: int, seq: int, keep_from: int) -> int:

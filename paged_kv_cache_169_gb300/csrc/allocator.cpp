@@ -140,6 +140,46 @@ int kv_alloc_append_slots(kv_alloc* a, int seq, int count, int64_t* slots_out,
     return KV_OK;
 }
 
+int kv_alloc_decode_step(kv_alloc* a, const int32_t* seqs, int n, int64_t* slots_out, int32_t* cow_pairs_out,
+                         int* n_cow) {
+    if (!a || n < 0 || (n > 0 && (!seqs || !slots_out || !cow_pairs_out)) || !n_cow) return KV_ERR_INVALID_ARG;
+    *n_cow = 0;
+    // every sequence must exist, and the free list must hold every block the step takes:
+    // a new block where the length is a multiple of B, or a copy where the last block is
+    // still shared (the last of its sharers in this step writes in place)
+    std::unordered_map<int32_t, int> ref_left;
+    int64_t need = 0;
+    const int64_t B = a->block_size;
+    for (int i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seqs[i]);
+        if (it == a->seqs.end()) return KV_ERR_STATE;
+        const kv_alloc::Seq& s = it->second;
+        if (s.len % B == 0) {
+            ++need;
+        } else {
+            const int32_t last = s.table.back();
+            auto r = ref_left.find(last);
+            int& left = r == ref_left.end() ? (ref_left[last] = a->ref[last]) : r->second;
+            if (left > 1) {
+                ++need;
+                --left;
+            }
+        }
+    }
+    if (need > (int64_t)a->free_stack.size()) return KV_ERR_NO_BLOCKS;
+    for (int i = 0; i < n; ++i) {
+        int32_t pair[2];
+        const int rc = kv_alloc_append_slots(a, seqs[i], 1, slots_out + i, pair);
+        if (rc != KV_OK) return rc;                    // not reached: checked above
+        if (pair[0] >= 0) {
+            cow_pairs_out[2 * *n_cow] = pair[0];
+            cow_pairs_out[2 * *n_cow + 1] = pair[1];
+            *n_cow += 1;
+        }
+    }
+    return KV_OK;
+}
+
 int kv_alloc_seq_free(kv_alloc* a, int seq) {
     if (!a) return KV_ERR_INVALID_ARG;
     auto it = a->seqs.find(seq);

@@ -6,6 +6,8 @@ initial free list, same operation sequence): block ids, slots, copy pairs, refer
 counts and free lists must be identical (integer work: bit-exact).
 """
 
+import copy
+import ctypes as C
 import os
 import re
 
@@ -116,6 +118,32 @@ def _run_both(num_blocks, B, order, ops):
                 if ok_a:
                     assert slots_a == slots_m
                     assert ([cow_a] if cow_a else []) == [tuple(c) for c in cows_m]
+            elif kind == "step":                     # one slot for each listed sequence
+                names = op[1]
+                snap = copy.deepcopy(m)
+                slots_m, cows_m, ok_m = [], [], True
+                try:
+                    for nm in names:
+                        sl, cw = m.append_slots(ids[nm][1], 1)
+                        slots_m += sl
+                        cows_m += [tuple(c) for c in cw]
+                except OC.OutOfBlocks:
+                    ok_m = False
+                    m = snap                         # the batch call changes nothing on failure
+                n = len(names)
+                seq_arr = (C.c_int32 * max(n, 1))(*[ids[nm][0] for nm in names])
+                slots = (C.c_int64 * max(n, 1))()
+                pairs = (C.c_int32 * max(2 * n, 2))()
+                try:
+                    n_cow = abi.kv_alloc_decode_step(a, seq_arr, n, slots, pairs)
+                    ok_a = True
+                except abi.KvError as e:
+                    assert e.status == abi.KV_ERR_NO_BLOCKS
+                    ok_a = False
+                assert ok_a == ok_m
+                if ok_a:
+                    assert list(slots)[:n] == slots_m
+                    assert [(pairs[2 * i], pairs[2 * i + 1]) for i in range(n_cow)] == cows_m
             elif kind == "free":
                 ca, cm = ids.pop(op[1])
                 abi.kv_alloc_seq_free(a, ca)
@@ -140,12 +168,15 @@ def _run_both(num_blocks, B, order, ops):
         abi.kv_alloc_destroy(a)
 
 
-def test_allocator_matches_oracle_parallel_sampling(lib):
+@pytest.mark.parametrize("batched", [False, True])
+def test_allocator_matches_oracle_parallel_sampling(lib, batched):
+    """128 decode steps of 8 candidates forked from a 1030-token prompt, one slot per
+    candidate per step: per sequence, or with one kv_alloc_decode_step call per step."""
     ops = [("new", "p"), ("append", "p", 1030)]
     ops += [("fork", "p", f"c{i}") for i in range(1, 8)]
     names = ["p"] + [f"c{i}" for i in range(1, 8)]
     for _ in range(128):
-        ops += [("append", n, 1) for n in names]
+        ops += [("step", names)] if batched else [("append", n, 1) for n in names]
     ops += [("free", n) for n in names]
     _run_both(200, 16, np.random.default_rng(4).permutation(200).tolist(), ops)
 
@@ -167,6 +198,9 @@ def test_allocator_matches_oracle_random_ops(lib):
                 ops.append(("free", live.pop(int(rng.integers(len(live))))))
             elif r < 9:
                 ops.append(("trim", live[int(rng.integers(len(live)))], int(rng.integers(1, 60))))
+            elif rng.integers(2):                    # a decode step over some live sequences
+                pick = rng.permutation(len(live))[:int(rng.integers(1, len(live) + 1))]
+                ops.append(("step", [live[int(i)] for i in pick]))
             else:
                 ops.append(("new", k))
                 live.append(k)
@@ -194,6 +228,12 @@ def test_allocator_errors(lib):
             abi.kv_alloc_build_tables(a, [s], 3)              # table longer than max_blocks
         tabs, lens = abi.kv_alloc_build_tables(a, [s], 6)
         assert lens == [32] and tabs[0][4:] == [-1, -1]
+        # a decode step with an unknown sequence changes nothing
+        before = abi.kv_alloc_free_list(a, 4)
+        with pytest.raises(abi.KvError) as e:
+            abi.kv_alloc_decode_step(a, (C.c_int32 * 2)(s, 999), 2, (C.c_int64 * 2)(), (C.c_int32 * 4)())
+        assert e.value.status == abi.KV_ERR_STATE
+        assert abi.kv_alloc_seq_info(a, s) == (32, 4) and abi.kv_alloc_free_list(a, 4) == before
         abi.kv_alloc_seq_free(a, s)
         assert sorted(abi.kv_alloc_free_list(a, 4)) == [0, 1, 2, 3]
         with pytest.raises(abi.KvError) as e:
@@ -203,3 +243,33 @@ def test_allocator_errors(lib):
         abi.kv_alloc_destroy(a)
     with pytest.raises(abi.KvError):
         abi.kv_alloc_create(4, 8, [0, 1, 1, 2])               # not a permutation
+
+
+def test_decode_step_is_all_or_nothing(lib):
+    """A decode step whose blocks do not all fit changes nothing; one sharer of a block
+    copies and the last sharer writes in place, within one step as across steps."""
+    a = abi.kv_alloc_create(5, 8)
+    try:
+        s0 = abi.kv_alloc_seq_new(a)
+        abi.kv_alloc_append_slots(a, s0, 12)                 # blocks: 2 (the second half full)
+        s1 = abi.kv_alloc_seq_fork(a, s0)                    # shares both
+        s2 = abi.kv_alloc_seq_new(a)
+        abi.kv_alloc_append_slots(a, s2, 16)                 # 2 more blocks, 1 free left
+        free = abi.kv_alloc_free_list(a, 5)
+        seqs = (C.c_int32 * 3)(s0, s1, s2)
+        slots, pairs = (C.c_int64 * 3)(), (C.c_int32 * 6)()
+        # s0 copies the shared half block (1), s1 then writes in place, s2 needs a new
+        # block (1): 2 blocks, 1 free
+        with pytest.raises(abi.KvError) as e:
+            abi.kv_alloc_decode_step(a, seqs, 3, slots, pairs)
+        assert e.value.status == abi.KV_ERR_NO_BLOCKS
+        assert abi.kv_alloc_free_list(a, 5) == free
+        assert [abi.kv_alloc_seq_info(a, s) for s in (s0, s1, s2)] == [(12, 2), (12, 2), (16, 2)]
+        # without s2 it fits: one copy planned, for s0
+        n = abi.kv_alloc_decode_step(a, seqs, 2, slots, pairs)
+        assert n == 1 and pairs[1] == free[0]
+        shared_last = abi.kv_alloc_block_table(a, s1)[-1]
+        assert pairs[0] == shared_last and abi.kv_alloc_ref_count(a, shared_last) == 1
+        assert slots[0] == pairs[1] * 8 + 4 and slots[1] == shared_last * 8 + 4
+    finally:
+        abi.kv_alloc_destroy(a)
