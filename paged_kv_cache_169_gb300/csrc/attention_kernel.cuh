@@ -609,6 +609,57 @@ __device__ __forceinline__ void merge_partials(const AttnArgs& a, int64_t sh0, i
     merge_rows<D, G, FINAL>(a, sh0 + lane / (32 / G), first, count, stride, lane);
 }
 
+// The final merge of one row (partials 0, stride, 2*stride, ... of it; count <= 32) with
+// all 32 lanes (head_dim 128: a float4 of the row per lane).  Lane k loads partial k's
+// (m, l) while the rows of the first eight partials are already in flight, so up to eight
+// partials cost one L2 round trip (merge_rows' first pass over the maxima costs one more).
+// The same operations in the same order as merge_rows with one row: the same bits.
+template <int D>
+__device__ __forceinline__ void merge_row_fast(const AttnArgs& a, int64_t row, int count, int stride, int lane) {
+    static_assert(D == 128, "a float4 of the row per lane");
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + row * a.max_parts;
+    const float4* o = reinterpret_cast<const float4*>(a.part_o + row * a.max_parts * D) + lane;
+    const float2 v = lane < count ? __ldcg(ml + static_cast<int64_t>(lane) * stride) : make_float2(-CUDART_INF_F, 0.f);
+    // the weights and the denominator are summed in partition order, as merge_rows does,
+    // so a row's result does not depend on which of the two merged it
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wk = 0.f, L = 0.f;
+    #pragma unroll 1
+    for (int k0 = 0; k0 < count; k0 += 8) {
+        float4 x[8];
+        #pragma unroll
+        for (int k = 0; k < 8; ++k)
+            x[k] = k0 + k < count ? __ldcg(o + static_cast<int64_t>(k0 + k) * stride * (D / 4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k0 == 0) {
+            const float mx = warp_max(v.x);
+            wk = lane < count ? ex2_approx(v.x - mx) : 0.f;
+        }
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float w = __shfl_sync(FULL, wk, (k0 + k) & 31);
+            const float lk = __shfl_sync(FULL, v.y, (k0 + k) & 31);
+            if (k0 + k < count) L = fmaf(lk, w, L);
+            acc.x = fmaf(w, x[k].x, acc.x);
+            acc.y = fmaf(w, x[k].y, acc.y);
+            acc.z = fmaf(w, x[k].z, acc.z);
+            acc.w = fmaf(w, x[k].w, acc.w);
+        }
+    }
+    const float inv = 1.f / L;
+    if (a.out_f16) {                                   // rounded once, from the float32 result
+        const __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        const __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
+        uint2 wv;
+        wv.x = *reinterpret_cast<const unsigned*>(&lo);
+        wv.y = *reinterpret_cast<const unsigned*>(&hi);
+        reinterpret_cast<uint2*>(static_cast<__half*>(a.out) + row * D)[lane] = wv;
+    } else {
+        reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * D)[lane] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+}
+
 // Partition p of (sequence, KV head) shk has written its partials: publish them and take
 // a ticket.  Up to kMergeFan partitions merge in one step, by the warp that finishes last.
 // Longer splits merge in two levels, which shortens the merge that ends the split: the
@@ -656,6 +707,12 @@ __device__ __forceinline__ void ticket_resolve(const AttnArgs& a, Ticket& tk, in
     if (prev != static_cast<unsigned>(count - 1)) return;
     if (lane == 0) a.arrivals[tk.shk] = 0;                             // left zero for the next call
     __syncwarp();
+    if constexpr (D == 128 && G == 1) {
+        if (count <= 32) {
+            merge_row_fast<D>(a, tk.shk, count, stride, lane);
+            return;
+        }
+    }
     merge_partials<D, G, true>(a, tk.shk * G, 0, count, stride, lane);
 }
 
@@ -668,54 +725,6 @@ struct PfxTicket {
     bool pending;
 };
 
-// One row's merge with all 32 lanes (head_dim 128: a float4 of the row per lane) for at
-// most kPfxMaxParts partials.  Lane k loads partial k's (m, l) while the rows of the first
-// eight partials are already in flight, so up to eight partials cost one L2 round trip.
-template <int D>
-__device__ __forceinline__ void merge_row_fast(const AttnArgs& a, int64_t row, int count, int lane) {
-    static_assert(D == 128, "a float4 of the row per lane");
-    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + row * a.max_parts;
-    const float4* o = reinterpret_cast<const float4*>(a.part_o + row * a.max_parts * D) + lane;
-    const float2 v = lane < count ? __ldcg(ml + lane) : make_float2(-CUDART_INF_F, 0.f);
-    // the weights and the denominator are summed in partition order, as merge_rows does,
-    // so a row's result does not depend on which of the two merged it
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wk = 0.f, L = 0.f;
-    #pragma unroll 1
-    for (int k0 = 0; k0 < count; k0 += 8) {
-        float4 x[8];
-        #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            x[k] = k0 + k < count ? __ldcg(o + (k0 + k) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k0 == 0) {
-            const float mx = warp_max(v.x);
-            wk = lane < count ? ex2_approx(v.x - mx) : 0.f;
-        }
-        #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float w = __shfl_sync(FULL, wk, (k0 + k) & 31);
-            const float lk = __shfl_sync(FULL, v.y, (k0 + k) & 31);
-            if (k0 + k < count) L = fmaf(lk, w, L);
-            acc.x = fmaf(w, x[k].x, acc.x);
-            acc.y = fmaf(w, x[k].y, acc.y);
-            acc.z = fmaf(w, x[k].z, acc.z);
-            acc.w = fmaf(w, x[k].w, acc.w);
-        }
-    }
-    const float inv = 1.f / L;
-    if (a.out_f16) {                                   // rounded once, from the float32 result
-        const __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
-        const __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
-        uint2 wv;
-        wv.x = *reinterpret_cast<const unsigned*>(&lo);
-        wv.y = *reinterpret_cast<const unsigned*>(&hi);
-        reinterpret_cast<uint2*>(static_cast<__half*>(a.out) + row * D)[lane] = wv;
-    } else {
-        reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * D)[lane] =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
-}
-
 template <int D>
 __device__ __forceinline__ void pfx_ticket_resolve(const AttnArgs& a, PfxTicket& tk, int lane) {
     const bool last = tk.pending && tk.prev == static_cast<unsigned>(tk.np - 1);
@@ -726,7 +735,7 @@ __device__ __forceinline__ void pfx_ticket_resolve(const AttnArgs& a, PfxTicket&
     __syncwarp();
     if (__popc(m) == 1) {                          // one row: all 32 lanes on it
         const int r = __ffs(m) - 1;
-        merge_row_fast<D>(a, __shfl_sync(FULL, tk.sq, r), __shfl_sync(FULL, tk.np, r), lane);
+        merge_row_fast<D>(a, __shfl_sync(FULL, tk.sq, r), __shfl_sync(FULL, tk.np, r), 1, lane);
     } else {                                       // rows side by side, 4 lanes each (row r: lanes 4r..4r+3)
         const int r = lane >> 2;
         const int sq = __shfl_sync(FULL, tk.sq, r);
