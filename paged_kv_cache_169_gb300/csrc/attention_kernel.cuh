@@ -219,7 +219,10 @@ struct Cfg {
 #if defined(KVP_PR_RINGS)
     static constexpr int NR_PAIR = KVP_PR_RINGS;   // tuning sweeps only
 #else
-    static constexpr int NR_PAIR = 4;              // head-pair stages: 4 rings, 8 consumer warps
+    // head-pair stages: 4 rings of 2 consumer warps; shared-prefix launches, whose items
+    // are few and short, take 2 rings with deeper stages instead (up to 6 chunks of an
+    // item in flight, most of them fetched before the previous launch ends)
+    static constexpr int NR_PAIR = PFX ? 2 : 4;
 #endif
     static constexpr int NC = PR ? 2 * NR_PAIR
                                  : MMA ? NC_MMA
@@ -234,7 +237,7 @@ struct Cfg {
     static constexpr int NSW_FIT =
         (227 * 1024 - TABLES - RESERVE) /
         (NR * (STAGE + (int)sizeof(Meta) + QR_BYTES));
-    static constexpr int NSW_CAP = (MMA && FP8) ? 6 : 4;   // FP8 stages are half as large
+    static constexpr int NSW_CAP = (MMA && (FP8 || (PR && PFX))) ? 6 : 4;   // FP8 stages are half as large
     static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > NSW_CAP ? NSW_CAP : NSW_FIT);
     static_assert(NSW >= 2, "at least double buffering");
     static constexpr int THREADS = (NC + 1) * 32;

@@ -217,9 +217,12 @@ int plan_attention_prefix(const kv_pool* pool, int batch, int max_context, int p
         P = partition_tokens;
     } else if (partition_tokens == 0) {
         // library choice: short items, so a group's shared prefix (read once for all its
-        // members) spreads over many SMs: about 16 partitions of the longest context,
-        // 64 to 1024 tokens each
-        int64_t p = (static_cast<int64_t>(max_context) + 15) / 16;
+        // members) spreads over many SMs: about 8 partitions of the longest context, 64 to
+        // 1024 tokens each.  With two rings of head pairs per SM, parallel sampling (8
+        // members, 40 heads, 1030-1158 tokens) then fits one round of items: 160-token
+        // partitions measured 0.349 of the copy peak, against 0.29-0.30 at 96 and 128
+        // tokens (more items than rings) and 0.343 at 192.
+        int64_t p = (static_cast<int64_t>(max_context) + 7) / 8;
         p = (p + kPartAlign - 1) / kPartAlign * kPartAlign;
         if (p < 64) p = 64;
         if (p > 1024) p = 1024;
