@@ -362,7 +362,7 @@ KV_API int paged_decode_attention_gqa(kv_pool* pool, int layer, const void* q, i
  *                num_q_heads equal to num_heads and window 0, else KV_ERR_UNSUPPORTED.  The
  *                workspace size depends on whether groups are given (not on their contents):
  *                paged_decode_workspace_size_ex reads num_prefix_groups.  Partitioning with
- *                groups: partition_tokens 0 = about 16 partitions of max_context, 64 to 1024
+ *                groups: partition_tokens 0 = about 8 partitions of max_context, 64 to 1024
  *                tokens; an explicit value must be at least ceil(max_context / 31) rounded up to
  *                a multiple of 32 (a member has at most 32 partitions). */
 #define KV_DECODE_WORKSPACE_ZEROED 1u
