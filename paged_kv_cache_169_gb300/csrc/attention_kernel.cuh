@@ -123,8 +123,8 @@ constexpr int kPfxMaxParts = 32;
 
 constexpr int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
-// Launch shape per storage type: tokens per chunk (CT), consumer warps (NC), ring stages
-// per consumer (NSW).  Compile-time overrides exist only for tuning sweeps
+// Launch shape per storage type: tokens per chunk (CT), consumer warps per SM (NC), ring
+// stages per consumer (NSW).  Compile-time overrides exist only for tuning sweeps
 // (KVP_F16_CT/NC/NSW, KVP_FP8_CT/NC/NSW).
 template <int ESZ> struct Tune { static constexpr int CT = 32, NC = 0, NSW = 0; };   // 0: by stage size
 #if !defined(KVP_F16_CT)
@@ -138,6 +138,9 @@ template <> struct Tune<2> { static constexpr int CT = KVP_F16_CT, NC = KVP_F16_
 #endif
 #if defined(KVP_FP8_CT) && defined(KVP_FP8_NC) && defined(KVP_FP8_NSW)
 template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_NC, NSW = KVP_FP8_NSW; };
+#endif
+#if !defined(KVP_F16_CPS)
+#define KVP_F16_CPS 2              // CTAs per SM of the fp16 single-head launch (override: tuning sweeps)
 #endif
 
 // G_: query heads per KV head (grouped-query attention; 1 = one query per KV head).
@@ -224,9 +227,14 @@ struct Cfg {
     // item in flight, most of them fetched before the previous launch ends)
     static constexpr int NR_PAIR = PFX ? 2 : 4;
 #endif
+    // CTAs resident per SM.  Two (fp16, one head per item) halve the granularity at which
+    // an SM passes from one launch to the next under programmatic dependent launch and at
+    // which a launch's tail frees SMs: each CTA gets half of the SM's 228 KiB (less the
+    // 1 KiB the system keeps per CTA) and half of its consumer warps.
+    static constexpr int CPS = (!MMA && G == 1 && HP == 1 && ESZ == 2) ? KVP_F16_CPS : 1;
     static constexpr int NC = PR ? 2 * NR_PAIR
                                  : MMA ? NC_MMA
-                                       : G == 1 ? (Tune<ESZ>::NC ? Tune<ESZ>::NC : NC_AUTO)
+                                       : G == 1 ? (Tune<ESZ>::NC ? Tune<ESZ>::NC : NC_AUTO) / CPS
                                                 : (G == 2 ? 12 : (G == 4 ? 8 : 6));
     static constexpr int NR = PR ? NR_PAIR : NC;   // rings (one producer lane each)
     // stages that fit beside the prefix table and the barriers
@@ -234,8 +242,9 @@ struct Cfg {
     // beside the stages: the tables and the reserve (alignment slack, barriers, zero line,
     // launch-wide values)
     static constexpr int RESERVE = 1024 + (MMA ? 2048 : 0);
+    static constexpr int SMEM_BUDGET = CPS == 1 ? 227 * 1024 : 228 * 1024 / CPS - 1024;
     static constexpr int NSW_FIT =
-        (227 * 1024 - TABLES - RESERVE) /
+        (SMEM_BUDGET - TABLES - RESERVE) /
         (NR * (STAGE + (int)sizeof(Meta) + QR_BYTES));
     static constexpr int NSW_CAP = (MMA && (FP8 || (PR && PFX))) ? 6 : 4;   // FP8 stages are half as large
     static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > NSW_CAP ? NSW_CAP : NSW_FIT);
@@ -249,7 +258,7 @@ struct Cfg {
     static constexpr int MISC_OFF = ZERO_OFF + 128;             // launch-wide values (the partition size)
     static constexpr int ALIGN_SLACK = MMA ? 1024 : 0;           // to 1024-align the base
     static constexpr int SMEM = MISC_OFF + 16 + ALIGN_SLACK;
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(SMEM <= SMEM_BUDGET, "shared memory budget");
     static_assert(NC <= 32 && (CT == 8 || CT == 16 || CT == 32), "launch shape");
     static_assert(Q_OFF % 16 == 0 && META_R % 16 == 0 && QR_OFF % 16 == 0, "alignment");
 };
@@ -1219,7 +1228,7 @@ __device__ __forceinline__ void consumer_mma(const AttnArgs& a, char* smem, cons
 }
 
 template <typename C>
-__global__ void __launch_bounds__(C::THREADS, 1) attention_partition_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(C::THREADS, C::CPS) attention_partition_kernel(const __grid_constant__ AttnArgs a) {
     constexpr int NC = C::NC, NR = C::NR, NSW = C::NSW, D = C::D, CT = C::CT, TPL = C::TPL, DPL = C::DPL;
     constexpr int CBMAX = C::CBMAX;
     extern __shared__ __align__(128) char smem_raw[];
@@ -1832,6 +1841,11 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
         if (cudaFuncSetAttribute(attention_partition_kernel<C>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
             return KV_ERR_CUDA;
+        // the whole unified L1 / shared array as shared memory, so C::CPS CTAs fit per SM
+        if (C::CPS > 1 && cudaFuncSetAttribute(attention_partition_kernel<C>,
+                                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return KV_ERR_CUDA;
         attr_done |= bit;
     }
     const int total = args.batch;
@@ -1862,7 +1876,7 @@ int launch_typed(const kv_pool* pool, AttnArgs args, const AttnPlan& plan, unsig
         sa.exit_counter = counters + kMaxSub + sub;
         const int64_t upper = static_cast<int64_t>(sa.batch) * (args.H / C::KVH) * args.max_parts;
         int64_t grid = (upper + C::NR - 1) / C::NR;
-        if (grid > pool->num_sms) grid = pool->num_sms;
+        if (grid > static_cast<int64_t>(pool->num_sms) * C::CPS) grid = static_cast<int64_t>(pool->num_sms) * C::CPS;
         if (grid < 1) grid = 1;
         if (plan.flags & KV_DECODE_PDL) {
             // may begin while the previous kernel on the stream finishes (see the kernel)

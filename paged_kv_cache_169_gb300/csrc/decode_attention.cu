@@ -8,10 +8,10 @@ namespace kvp {
 namespace {
 
 template <typename C>
-int consumers_of() { return C::NC; }
+int consumers_of() { return C::NC * C::CPS; }      // per SM
 
 template <typename C>
-int rings_of() { return C::NR; }
+int rings_of() { return C::NR * C::CPS; }
 
 template <int G>
 int consumers_for_g(const kv_pool* pool) {
