@@ -139,8 +139,21 @@ template <> struct Tune<2> { static constexpr int CT = KVP_F16_CT, NC = KVP_F16_
 #if defined(KVP_FP8_CT) && defined(KVP_FP8_NC) && defined(KVP_FP8_NSW)
 template <> struct Tune<1> { static constexpr int CT = KVP_FP8_CT, NC = KVP_FP8_NC, NSW = KVP_FP8_NSW; };
 #endif
+// CTAs per SM by launch shape (overrides: tuning sweeps)
 #if !defined(KVP_F16_CPS)
-#define KVP_F16_CPS 2              // CTAs per SM of the fp16 single-head launch (override: tuning sweeps)
+#define KVP_F16_CPS 2              // fp16, one head per item
+#endif
+#if !defined(KVP_F16P_CPS)
+#define KVP_F16P_CPS 2             // fp16, head pairs (B 8)
+#endif
+#if !defined(KVP_FP8_CPS)
+#define KVP_FP8_CPS 2              // FP8, one head or head pairs per item
+#endif
+#if !defined(KVP_PR_CPS)
+#define KVP_PR_CPS 2               // tensor-core head-pair stages, grouped queries
+#endif
+#if !defined(KVP_PFX_CPS)
+#define KVP_PFX_CPS 2              // tensor-core head-pair stages, shared prefixes
 #endif
 
 // G_: query heads per KV head (grouped-query attention; 1 = one query per KV head).
@@ -213,6 +226,16 @@ struct Cfg {
     static constexpr int QR_BYTES = SWZ_STAGE && !PR ? Q_BYTES : 0;
     static constexpr int STAGE = round_up(Q_OFF + Q_STAGE, (SWZ_STAGE || SWZ_K) ? 1024 : 128);
     static constexpr int NC_AUTO = STAGE <= 9 * 1024 ? 8 : (STAGE <= 17 * 1024 ? 4 : 3);
+    // CTAs resident per SM.  Two halve the granularity at which an SM passes from one
+    // launch to the next under programmatic dependent launch and at which a launch's tail
+    // frees SMs: each CTA gets half of the SM's 228 KiB (less the 1 KiB the system keeps
+    // per CTA) and half of its consumer warps or rings.  Head quads (FP8, B 8) keep one:
+    // half their stages would not double-buffer.
+    static constexpr int CPS = (!MMA && G == 1 && HP == 1 && ESZ == 2) ? KVP_F16_CPS
+                             : (!MMA && G == 1 && ESZ == 2) ? KVP_F16P_CPS
+                             : (!MMA && G == 1 && ESZ == 1 && HP <= 2) ? KVP_FP8_CPS
+                             : (PR && !PFX) ? KVP_PR_CPS
+                             : (PR && PFX) ? KVP_PFX_CPS : 1;
     // more query heads per warp need more registers: fewer consumer warps
 #if defined(KVP_MMA_NC)
     static constexpr int NC_MMA = KVP_MMA_NC;      // tuning sweeps only
@@ -225,13 +248,8 @@ struct Cfg {
     // head-pair stages: 4 rings of 2 consumer warps; shared-prefix launches, whose items
     // are few and short, take 2 rings with deeper stages instead (up to 6 chunks of an
     // item in flight, most of them fetched before the previous launch ends)
-    static constexpr int NR_PAIR = PFX ? 2 : 4;
+    static constexpr int NR_PAIR = (PFX ? 2 : 4) / CPS;
 #endif
-    // CTAs resident per SM.  Two (fp16, one head per item) halve the granularity at which
-    // an SM passes from one launch to the next under programmatic dependent launch and at
-    // which a launch's tail frees SMs: each CTA gets half of the SM's 228 KiB (less the
-    // 1 KiB the system keeps per CTA) and half of its consumer warps.
-    static constexpr int CPS = (!MMA && G == 1 && HP == 1 && ESZ == 2) ? KVP_F16_CPS : 1;
     static constexpr int NC = PR ? 2 * NR_PAIR
                                  : MMA ? NC_MMA
                                        : G == 1 ? (Tune<ESZ>::NC ? Tune<ESZ>::NC : NC_AUTO) / CPS
