@@ -20,6 +20,8 @@ int consumers_for_g(const kv_pool* pool) {
         // head-pair stages (FP8): rings of two warps, each ring's items covering two K/V heads
         if (d.dtype == KV_FP8_E4M3 && d.head_dim == 128 && pool->tmaps && pair_stages(pool, false))
             return rings_of<Cfg<128, uint8_t, __half, G, true, 1, 0, false, true>>();
+        if (d.dtype == KV_F16 && d.head_dim == 128 && pool->tmaps && pair_stages(pool, false))
+            return rings_of<Cfg<128, __half, __half, G, true, 1, 0, false, true>>();
         if (d.dtype == KV_F16 && d.head_dim == 128 && pool->tmaps)
             return consumers_of<Cfg<128, __half, __half, G, true>>();
         if (d.dtype == KV_FP8_E4M3 && d.head_dim == 128 && pool->tmaps)
@@ -64,9 +66,10 @@ bool pair_stages(const kv_pool* pool, bool prefix) {
 #else
     // Measured (GB300): shared-prefix launches +16 % (8 KiB instead of 4 KiB copies lift
     // the per-SM copy rate that bounds them), FP8 grouped-query +4 %; fp16 grouped-query
-    // decode is bound by HBM already and ran 1 % slower, so it keeps one head per stage.
+    // +1.5 % once two CTAs share each SM (1 % slower with one CTA of nine warps per SM).
+    (void)prefix;
     if (!pool->tmaps || !pool->pmaps || pool->desc.num_heads % 2 != 0) return false;
-    return prefix || pool->desc.dtype == KV_FP8_E4M3;
+    return true;
 #endif
 }
 

@@ -13,7 +13,10 @@ int launch_g(const kv_pool* pool, const AttnArgs& a, const AttnPlan& plan, unsig
     const kv_pool_desc& d = pool->desc;
     if (d.dtype == KV_F16) {
         if (d.head_dim == 128) {
-            // tensor cores when the pool has its swizzled tensor maps, else CUDA cores
+            // tensor cores when the pool has its swizzled tensor maps (head-pair stages when
+            // the head count is even), else CUDA cores
+            if (pool->tmaps && plan.pairs)
+                return launch_typed<Cfg<128, __half, __half, G, true, 1, 0, false, true>>(pool, a, plan, counters, stream);
             if (pool->tmaps) return launch_typed<Cfg<128, __half, __half, G, true>>(pool, a, plan, counters, stream);
             return launch_typed<Cfg<128, __half, __half, G>>(pool, a, plan, counters, stream);
         }
