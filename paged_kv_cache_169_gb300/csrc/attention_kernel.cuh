@@ -245,9 +245,10 @@ struct Cfg {
 #if defined(KVP_PR_RINGS)
     static constexpr int NR_PAIR = KVP_PR_RINGS;   // tuning sweeps only
 #else
-    // head-pair stages: 4 rings of 2 consumer warps; shared-prefix launches, whose items
-    // are few and short, take 2 rings with deeper stages instead (up to 6 chunks of an
-    // item in flight, most of them fetched before the previous launch ends)
+    // head-pair stages: 4 rings of 2 consumer warps per SM; shared-prefix launches, whose
+    // items are few and short, take 2 rings per SM with deeper stages instead (up to 6
+    // chunks of an item in flight, most of them fetched before the previous launch ends).
+    // The SM's CTAs share them out.
     static constexpr int NR_PAIR = (PFX ? 2 : 4) / CPS;
 #endif
     static constexpr int NC = PR ? 2 * NR_PAIR
@@ -264,9 +265,11 @@ struct Cfg {
     static constexpr int NSW_FIT =
         (SMEM_BUDGET - TABLES - RESERVE) /
         (NR * (STAGE + (int)sizeof(Meta) + QR_BYTES));
-    static constexpr int NSW_CAP = (MMA && (FP8 || (PR && PFX))) ? 6 : 4;   // FP8 stages are half as large
+    // FP8 stages hold twice the tokens per byte; shared-prefix rings are few and deep
+    static constexpr int NSW_CAP = (MMA && (FP8 || (PR && PFX))) ? 6 : 4;
     static constexpr int NSW = Tune<ESZ>::NSW && !MMA ? Tune<ESZ>::NSW : (NSW_FIT > NSW_CAP ? NSW_CAP : NSW_FIT);
     static_assert(NSW >= 2, "at least double buffering");
+    static_assert(NR >= 1 && NC >= 1, "at least one ring per CTA");
     static constexpr int THREADS = (NC + 1) * 32;
     static constexpr int META_R = NR * NSW * STAGE;                   // one Meta per stage
     static constexpr int QR_OFF = META_R + NR * NSW * (int)sizeof(Meta);   // MMA: one q slot per stage
