@@ -640,9 +640,9 @@ def abi_workspace_bytes(cache, batch, max_ctx, partition, prefix_groups):
 
 def host_step_loop(cache, alloc, seqs, q_h, k_h, v_h, max_blocks, max_ctx, scale, stream, groups=None,
                    partition=0):
-    """The decode loop as a caller runs it, through the C ABI, every step:
-      1. the host allocator reserves every sequence's next slot in one call
-         (kv_alloc_decode_step), planning a block copy where a slot lies in a shared block;
+    """The decode loop as a caller runs it, one kv_decode_step call per step, which does:
+      1. the host allocator reserves every sequence's next slot (kv_alloc_decode_step),
+         planning a block copy where a slot lies in a shared block;
       2. it writes the block tables and lengths into a pinned staging buffer
          (kv_alloc_build_tables), beside the planned block pairs;
       3. that buffer goes to the device in one copy, and the step's q / new K / new V
@@ -672,12 +672,10 @@ def host_step_loop(cache, alloc, seqs, q_h, k_h, v_h, max_blocks, max_ctx, scale
     d_meta = torch.empty(width, dtype=torch.int32, device=dev)
     d_bt = d_meta[:n * max_blocks].view(n, max_blocks)
     d_cl = d_meta[n * max_blocks:n * max_blocks + n]
-    d_pairs = d_meta[n * max_blocks + n:]
     d_qkv = torch.empty(pin_qkv.shape[1:], dtype=q_h.dtype, device=dev)
     d_out = torch.empty(q_h.shape[1:], dtype=torch.float32, device=dev)
     ws = cache.zeroed_workspace(n, max_ctx, partition, prefix_groups=groups is not None)
     seq_arr = (ctypes.c_int32 * n)(*seqs)
-    slots = (ctypes.c_int64 * n)()
     a = abi.kv_decode_args()                            # every pointer is fixed over the loop
     a.layer, a.q, a.num_q_heads = 0, d_qkv[0].data_ptr(), 0
     a.k_new, a.v_new, a.in_dtype = d_qkv[1].data_ptr(), d_qkv[2].data_ptr(), abi.KV_F16
@@ -689,24 +687,17 @@ def host_step_loop(cache, alloc, seqs, q_h, k_h, v_h, max_blocks, max_ctx, scale
     a.flags = abi.KV_DECODE_WORKSPACE_ZEROED | abi.KV_DECODE_PDL
     if groups is not None:
         a.prefix_groups, a.num_prefix_groups = groups.data_ptr(), groups.shape[0]
-    handle, layers = cache.handle, cache.num_layers
+    handle = cache.handle
     h2d = d2h = copies = 0
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with torch.cuda.stream(stream):
         ev[0].record(stream)
+        qkv_bytes = 3 * per * q_h.element_size()
         for i in range(S):
-            row = pin_meta[i]
-            base = row.data_ptr()
-            n_cow = abi.kv_alloc_decode_step(alloc.handle, seq_arr, n, slots, base + 4 * (n * max_blocks + n))
-            abi.kv_alloc_build_tables_into(alloc.handle, seq_arr, n, base, max_blocks, base + 4 * n * max_blocks)
-            d_meta.copy_(row, non_blocking=True)
-            d_qkv.copy_(pin_qkv[i], non_blocking=True)
-            h2d += width * 4 + 3 * per * q_h.element_size()
-            if n_cow:
-                abi.kv_copy_blocks(handle, d_pairs.data_ptr(), n_cow, 0, layers, a.stream)
-                copies += n_cow
-            abi.paged_decode_attention_ex(handle, a)
-            pin_out[i].copy_(d_out, non_blocking=True)
+            copies += abi.kv_decode_step(alloc.handle, handle, seq_arr, n, max_blocks, pin_meta[i].data_ptr(),
+                                         d_meta.data_ptr(), pin_qkv[i].data_ptr(), d_qkv.data_ptr(), qkv_bytes,
+                                         pin_out[i].data_ptr(), per * 4, a)
+            h2d += width * 4 + qkv_bytes
             d2h += per * 4
         ev[1].record(stream)
     stream.synchronize()
@@ -849,9 +840,9 @@ def run_decode_steps(args):
                      "algorithmic_bytes_per_replay": step_bytes},
         "e2e": {"value": step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "step": "64 decode steps through the C ABI, each: allocator slot reservation, tables into "
-                        "pinned memory, H2D of tables, lengths, q and new K/V, the fused call, D2H of the "
-                        "outputs"},
+                "step": "64 decode steps, one kv_decode_step call each: allocator slot reservation, tables "
+                        "into pinned memory, H2D of tables, lengths, q and new K/V, the fused call, D2H of "
+                        "the outputs"},
         "e2e_graph": {"value": step_bytes / (graph_e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                       "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 4,
                       "ms_per_step": graph_e2e_ms,
@@ -1015,9 +1006,9 @@ def run_parallel(args):
         "eager": {"ms_per_128_steps": eager_ms, "unique_GB/s": unique / (eager_ms / 1e3) / 1e9},
         "e2e": {"value": unique / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "step": "128 decode steps through the C ABI, each: allocator slot reservation (copy-on-write "
-                        "plan), tables into pinned memory, H2D of tables, lengths, block pairs, q and new K/V, "
-                        "kv_copy_blocks when planned, the fused call, D2H of the outputs"},
+                "step": "128 decode steps, one kv_decode_step call each: allocator slot reservation "
+                        "(copy-on-write plan), tables into pinned memory, H2D of tables, lengths, block pairs, "
+                        "q and new K/V, kv_copy_blocks when planned, the fused call, D2H of the outputs"},
         "logical_GB/s": logical / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": uniq_gbs, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": uniq_gbs / peak, "traffic": traffic_record("parallel"),

@@ -400,6 +400,35 @@ KV_API size_t paged_decode_workspace_size_ex(const kv_pool* pool, const kv_decod
 /* Decode attention with every option of kv_decode_args; errors as paged_decode_attention. */
 KV_API int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* args);
 
+/* One decode step of a batch, driven from the host in one call: the write-then-read step of
+ * [PagedAttention] §3.3 (allocate or copy-on-write, write the new token, attend) for every
+ * sequence of a batch, through the host allocator and one layer's fused call.
+ *   1. kv_alloc_decode_step(alloc, seqs, n, ...) reserves each sequence's next slot, planning
+ *      a block copy where the slot lies in a shared block (all or nothing);
+ *   2. the block tables, context lengths and planned copy pairs are written into the
+ *      caller's host staging buffer `staging` (int32 [n*max_blocks + n + 2*n]: tables
+ *      [n][max_blocks] padded with -1, lengths [n], pairs [n][2]; page-locked for the copy
+ *      to be asynchronous), which is copied whole to `dev_meta` (device, same layout);
+ *   3. `inputs_bytes` bytes are copied from host `inputs_h` to device `inputs_d` (the caller
+ *      packs the step's q, k_new and v_new there; may be 0);
+ *   4. the planned block copies run over every layer of the pool (kv_copy_blocks);
+ *   5. paged_decode_attention_ex(pool, args) runs the step's fused append + attention;
+ *   6. `out_bytes` bytes of args->out are copied back to host `out_h` (may be 0).
+ * args must describe this batch: batch == n, block_tables == dev_meta (tables part),
+ * context_lens == dev_meta + n*max_blocks, max_blocks_per_seq == max_blocks, k_new and v_new
+ * set (the step appends its token), and neither KV_DECODE_EARLY_TABLES nor
+ * KV_DECODE_EARLY_POOL (the tables are copied just before the call);
+ * otherwise KV_ERR_INVALID_ARG with nothing reserved.  A sequence whose table would exceed
+ * max_blocks after the step is refused the same way.  Every device operation is issued
+ * on args->stream and nothing synchronises, so a caller keeps one staging buffer per step
+ * in flight (a copy reads it later).  Returns the number of planned block copies (>= 0) or
+ * a negative kv_status: KV_ERR_STATE / KV_ERR_NO_BLOCKS from step 1 leave the allocator
+ * unchanged and issue nothing; a failure after step 1 (a CUDA call, the attention's own
+ * argument checks) returns its status with the slots already reserved. */
+KV_API int kv_decode_step(kv_alloc* alloc, kv_pool* pool, const int32_t* seqs, int n, int max_blocks,
+                          int32_t* staging, int32_t* dev_meta, const void* inputs_h, void* inputs_d,
+                          size_t inputs_bytes, void* out_h, size_t out_bytes, const kv_decode_args* args);
+
 /* Size of the library's fixed device scratch array used by paged_decode_attention_static. */
 #define KV_STATIC_SCRATCH_BYTES (16u << 20)
 

@@ -87,6 +87,8 @@ _SIGS = {
     "kv_alloc_seq_trim": (C.c_int, [_VP, C.c_int, C.c_int64, C.POINTER(C.c_int)]),
     "paged_decode_workspace_size_ex": (C.c_size_t, [_VP, _VP]),
     "paged_decode_attention_ex": (C.c_int, [_VP, _VP]),
+    "kv_decode_step": (C.c_int, [_VP, _VP, _I32P, C.c_int, C.c_int, _VP, _VP, _VP, _VP, C.c_size_t, _VP,
+                                 C.c_size_t, _VP]),
     "kv_alloc_seq_info": (C.c_int, [_VP, C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_int)]),
     "kv_alloc_block_table": (C.c_int, [_VP, C.c_int, _I32P, C.c_int, C.POINTER(C.c_int)]),
     "kv_alloc_build_tables": (C.c_int, [_VP, _I32P, C.c_int, _I32P, C.c_int, _I32P]),
@@ -265,6 +267,20 @@ def paged_decode_workspace_size_ex(pool: int, args: "kv_decode_args") -> int:
 
 def paged_decode_attention_ex(pool: int, args: "kv_decode_args") -> None:
     _check("paged_decode_attention_ex", load().paged_decode_attention_ex(pool, C.byref(args)))
+
+
+def kv_decode_step(alloc: int, pool: int, seqs, n: int, max_blocks: int, staging: int, dev_meta: int,
+                   inputs_h: int, inputs_d: int, inputs_bytes: int, out_h: int, out_bytes: int,
+                   args: "kv_decode_args") -> int:
+    """One decode step of a batch through the host allocator and one fused call (see the C
+    header): seqs is a ctypes int32 array of n ids; staging / inputs_h / out_h are host
+    addresses (pinned), dev_meta / inputs_d device addresses.  Returns the number of
+    planned block copies."""
+    rc = load().kv_decode_step(alloc, pool, C.cast(seqs, _I32P), n, max_blocks, staging, dev_meta, inputs_h,
+                               inputs_d, inputs_bytes, out_h, out_bytes, C.byref(args))
+    if rc < 0:
+        _check("kv_decode_step", rc)
+    return rc
 
 
 KV_STATIC_SCRATCH_BYTES = 16 << 20

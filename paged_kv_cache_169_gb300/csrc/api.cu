@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "kvp_internal.cuh"
 
@@ -402,6 +403,54 @@ int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* x) {
                                         x->k_new ? kvp::elem_bytes(x->in_dtype) : 0, x->out, x->block_tables,
                                         x->max_blocks_per_seq, x->context_lens, x->batch, x->max_context,
                                         x->scale, plan, x->workspace, x->stream);
+}
+
+int kv_decode_step(kv_alloc* alloc, kv_pool* pool, const int32_t* seqs, int n, int max_blocks,
+                   int32_t* staging, int32_t* dev_meta, const void* inputs_h, void* inputs_d,
+                   size_t inputs_bytes, void* out_h, size_t out_bytes, const kv_decode_args* args) {
+    if (!alloc || !pool || !args || !seqs || n < 1 || max_blocks < 1 || !staging || !dev_meta)
+        return KV_ERR_INVALID_ARG;
+    if ((inputs_bytes && (!inputs_h || !inputs_d)) || (out_bytes && (!out_h || !args->out)))
+        return KV_ERR_INVALID_ARG;
+    const int64_t tab = static_cast<int64_t>(n) * max_blocks;
+    if (args->batch != n || args->max_blocks_per_seq != max_blocks || args->block_tables != dev_meta ||
+        args->context_lens != dev_meta + tab || !args->k_new || !args->v_new ||
+        (args->flags & (KV_DECODE_EARLY_TABLES | KV_DECODE_EARLY_POOL)))
+        return KV_ERR_INVALID_ARG;
+    // every table must still fit max_blocks once this step's token is in it
+    const int B = pool->desc.block_size;
+    for (int i = 0; i < n; ++i) {
+        int len = 0, nb = 0;
+        const int rc = kv_alloc_seq_info(alloc, seqs[i], &len, &nb);
+        if (rc != KV_OK) return rc;
+        if ((static_cast<int64_t>(len) + 1 + B - 1) / B > max_blocks) return KV_ERR_INVALID_ARG;
+    }
+    int32_t* lens = staging + tab;
+    int32_t* pairs = lens + n;
+    // the slots themselves reach the kernel through the tables and lengths
+    static thread_local std::vector<int64_t> slots;
+    slots.resize(static_cast<size_t>(n));
+    int n_cow = 0;
+    int rc = kv_alloc_decode_step(alloc, seqs, n, slots.data(), pairs, &n_cow);
+    if (rc != KV_OK) return rc;
+    rc = kv_alloc_build_tables(alloc, seqs, n, staging, max_blocks, lens);
+    if (rc != KV_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(args->stream);
+    const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(tab + 3 * static_cast<int64_t>(n));
+    if (cudaMemcpyAsync(dev_meta, staging, meta_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return KV_ERR_CUDA;
+    if (inputs_bytes &&
+        cudaMemcpyAsync(inputs_d, inputs_h, inputs_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return KV_ERR_CUDA;
+    if (n_cow > 0) {
+        rc = kv_copy_blocks(pool, dev_meta + tab + n, n_cow, 0, pool->desc.num_layers, args->stream);
+        if (rc != KV_OK) return rc;
+    }
+    rc = paged_decode_attention_ex(pool, args);
+    if (rc != KV_OK) return rc;
+    if (out_bytes && cudaMemcpyAsync(out_h, args->out, out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KV_ERR_CUDA;
+    return n_cow;
 }
 
 size_t kv_swap_bytes(const kv_pool* pool, int num_blocks, int layer_begin, int layer_end) {

@@ -273,3 +273,25 @@ def test_decode_step_is_all_or_nothing(lib):
         assert slots[0] == pairs[1] * 8 + 4 and slots[1] == shared_last * 8 + 4
     finally:
         abi.kv_alloc_destroy(a)
+
+
+def test_decode_step_entry_refuses_missing_arguments(lib):
+    """kv_decode_step checks its pointers before touching the allocator or the device: with
+    no pool (or no argument block) it returns KV_ERR_INVALID_ARG and reserves nothing."""
+    a = abi.kv_alloc_create(4, 8)
+    try:
+        s0 = abi.kv_alloc_seq_new(a)
+        abi.kv_alloc_append_slots(a, s0, 3)
+        seqs = (C.c_int32 * 1)(s0)
+        staging = (C.c_int32 * 8)()
+        args = abi.kv_decode_args()
+        f = lib.kv_decode_step
+        assert f(a, None, seqs, 1, 2, C.addressof(staging), 1 << 20, None, None, 0, None, 0,
+                 C.byref(args)) == abi.KV_ERR_INVALID_ARG
+        assert f(a, None, seqs, 1, 2, C.addressof(staging), 1 << 20, None, None, 0, None, 0,
+                 None) == abi.KV_ERR_INVALID_ARG                     # no argument block
+        assert f(None, None, seqs, 1, 2, None, None, None, None, 0, None, 0,
+                 C.byref(args)) == abi.KV_ERR_INVALID_ARG            # no allocator, no staging
+        assert abi.kv_alloc_seq_info(a, s0) == (3, 1)                 # nothing reserved
+    finally:
+        abi.kv_alloc_destroy(a)
