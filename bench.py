@@ -661,18 +661,25 @@ def host_step_loop(cache, alloc, seqs, q_h, k_h, v_h, max_blocks, max_ctx, scale
     S, n = q_h.shape[0], q_h.shape[1]
     dev = cache.k[0].device
     per = q_h[0].numel()
-    # per step: [tables n*max_blocks | lengths n | block pairs 2n] int32, and q | k | v
+    # per step, one pinned row: [tables n*max_blocks | lengths n | block pairs 2n] int32,
+    # padding to 256 bytes, then q | k | v; the device copy has the same layout, so the
+    # step's inputs travel with its tables in one copy
     width = n * max_blocks + n + 2 * n
-    pin_meta = torch.empty((S, width), dtype=torch.int32).pin_memory()
-    pin_qkv = torch.empty((S, 3, n) + tuple(q_h.shape[2:]), dtype=q_h.dtype).pin_memory()
-    pin_qkv[:, 0].copy_(q_h)
-    pin_qkv[:, 1].copy_(k_h)
-    pin_qkv[:, 2].copy_(v_h)
+    off = (width * 4 + 255) // 256 * 256
+    qkv_bytes = 3 * per * q_h.element_size()
+    qkv_shape = (3, n) + tuple(q_h.shape[2:])
+    pin_rows = torch.empty((S, off + qkv_bytes), dtype=torch.uint8).pin_memory()
+    for i in range(S):
+        pq = pin_rows[i, off:].view(q_h.dtype).view(qkv_shape)
+        pq[0].copy_(q_h[i])
+        pq[1].copy_(k_h[i])
+        pq[2].copy_(v_h[i])
     pin_out = torch.empty(q_h.shape, dtype=torch.float32).pin_memory()
-    d_meta = torch.empty(width, dtype=torch.int32, device=dev)
+    d_row = torch.empty(off + qkv_bytes, dtype=torch.uint8, device=dev)
+    d_meta = d_row[:width * 4].view(torch.int32)
     d_bt = d_meta[:n * max_blocks].view(n, max_blocks)
     d_cl = d_meta[n * max_blocks:n * max_blocks + n]
-    d_qkv = torch.empty(pin_qkv.shape[1:], dtype=q_h.dtype, device=dev)
+    d_qkv = d_row[off:].view(q_h.dtype).view(qkv_shape)
     d_out = torch.empty(q_h.shape[1:], dtype=torch.float32, device=dev)
     ws = cache.zeroed_workspace(n, max_ctx, partition, prefix_groups=groups is not None)
     seq_arr = (ctypes.c_int32 * n)(*seqs)
@@ -692,12 +699,12 @@ def host_step_loop(cache, alloc, seqs, q_h, k_h, v_h, max_blocks, max_ctx, scale
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with torch.cuda.stream(stream):
         ev[0].record(stream)
-        qkv_bytes = 3 * per * q_h.element_size()
         for i in range(S):
-            copies += abi.kv_decode_step(alloc.handle, handle, seq_arr, n, max_blocks, pin_meta[i].data_ptr(),
-                                         d_meta.data_ptr(), pin_qkv[i].data_ptr(), d_qkv.data_ptr(), qkv_bytes,
+            row = pin_rows[i].data_ptr()
+            copies += abi.kv_decode_step(alloc.handle, handle, seq_arr, n, max_blocks, row, d_row.data_ptr(),
+                                         row + off, d_row.data_ptr() + off, qkv_bytes,
                                          pin_out[i].data_ptr(), per * 4, a)
-            h2d += width * 4 + qkv_bytes
+            h2d += off + qkv_bytes
             d2h += per * 4
         ev[1].record(stream)
     stream.synchronize()
@@ -841,8 +848,8 @@ def run_decode_steps(args):
         "e2e": {"value": step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "step": "64 decode steps, one kv_decode_step call each: allocator slot reservation, tables "
-                        "into pinned memory, H2D of tables, lengths, q and new K/V, the fused call, D2H of "
-                        "the outputs"},
+                        "into pinned memory, one H2D of tables, lengths, q and new K/V, the fused call, D2H "
+                        "of the outputs"},
         "e2e_graph": {"value": step_bytes / (graph_e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                       "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 4,
                       "ms_per_step": graph_e2e_ms,
@@ -1007,8 +1014,8 @@ def run_parallel(args):
         "e2e": {"value": unique / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "step": "128 decode steps, one kv_decode_step call each: allocator slot reservation "
-                        "(copy-on-write plan), tables into pinned memory, H2D of tables, lengths, block pairs, "
-                        "q and new K/V, kv_copy_blocks when planned, the fused call, D2H of the outputs"},
+                        "(copy-on-write plan), tables into pinned memory, one H2D of tables, lengths, block "
+                        "pairs, q and new K/V, kv_copy_blocks when planned, the fused call, D2H of the outputs"},
         "logical_GB/s": logical / (ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": uniq_gbs, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": uniq_gbs / peak, "traffic": traffic_record("parallel"),

@@ -410,7 +410,9 @@ KV_API int paged_decode_attention_ex(kv_pool* pool, const kv_decode_args* args);
  *      [n][max_blocks] padded with -1, lengths [n], pairs [n][2]; page-locked for the copy
  *      to be asynchronous), which is copied whole to `dev_meta` (device, same layout);
  *   3. `inputs_bytes` bytes are copied from host `inputs_h` to device `inputs_d` (the caller
- *      packs the step's q, k_new and v_new there; may be 0);
+ *      packs the step's q, k_new and v_new there; may be 0).  When the inputs lie at the
+ *      same offset after `staging` and after `dev_meta`, at most 256 bytes past the staging
+ *      data, steps 2 and 3 are one copy of both (and of the padding between them);
  *   4. the planned block copies run over every layer of the pool (kv_copy_blocks);
  *   5. paged_decode_attention_ex(pool, args) runs the step's fused append + attention;
  *   6. `out_bytes` bytes of args->out are copied back to host `out_h` (may be 0).

@@ -437,9 +437,16 @@ int kv_decode_step(kv_alloc* alloc, kv_pool* pool, const int32_t* seqs, int n, i
     if (rc != KV_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(args->stream);
     const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(tab + 3 * static_cast<int64_t>(n));
-    if (cudaMemcpyAsync(dev_meta, staging, meta_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    // inputs placed at the same offset after the staging buffer on both sides (at most 256
+    // bytes of padding) travel with it in one copy: each copy has a fixed cost in the stream
+    const ptrdiff_t off_h = static_cast<const char*>(inputs_h) - reinterpret_cast<const char*>(staging);
+    const ptrdiff_t off_d = static_cast<const char*>(inputs_d) - reinterpret_cast<const char*>(dev_meta);
+    const bool one_copy = inputs_bytes && off_h == off_d && off_h >= static_cast<ptrdiff_t>(meta_bytes) &&
+                          off_h <= static_cast<ptrdiff_t>(meta_bytes) + 256;
+    const size_t first = one_copy ? static_cast<size_t>(off_h) + inputs_bytes : meta_bytes;
+    if (cudaMemcpyAsync(dev_meta, staging, first, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return KV_ERR_CUDA;
-    if (inputs_bytes &&
+    if (inputs_bytes && !one_copy &&
         cudaMemcpyAsync(inputs_d, inputs_h, inputs_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return KV_ERR_CUDA;
     if (n_cow > 0) {

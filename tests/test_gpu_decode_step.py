@@ -58,8 +58,9 @@ def _args(cache, ws, d_meta, d_qkv, d_out, n, max_blocks, max_ctx, scale, stream
     return a
 
 
-def _run(one_call: bool, seed: int):
-    """The STEPS decode steps, through kv_decode_step or call by call."""
+def _run(one_call: bool, seed: int, merged: bool = False):
+    """The STEPS decode steps, through kv_decode_step or call by call.  merged: the inputs
+    follow the staging data in one pinned row and one device buffer (a single copy)."""
     w, cache, alloc, seqs, pk, pv, qkv = _setup(seed)
     n, max_blocks = CANDS, -(-(PROMPT + STEPS) // B)
     max_ctx = PROMPT + STEPS
@@ -70,6 +71,15 @@ def _run(one_call: bool, seed: int):
     pin_out = torch.empty((STEPS, n, H, D), dtype=torch.float32).pin_memory()
     d_meta = torch.empty(width, dtype=torch.int32, device="cuda")
     d_qkv = torch.empty((3, n, H, D), dtype=torch.float16, device="cuda")
+    off = (width * 4 + 255) // 256 * 256
+    qkv_bytes = 3 * n * H * D * 2
+    if merged:
+        rows = torch.empty((STEPS, off + qkv_bytes), dtype=torch.uint8).pin_memory()
+        for i in range(STEPS):
+            rows[i, off:].view(torch.float16).view(3, n, H, D).copy_(pin_qkv[i])
+        d_row = torch.empty(off + qkv_bytes, dtype=torch.uint8, device="cuda")
+        d_meta = d_row[:width * 4].view(torch.int32)
+        d_qkv = d_row[off:].view(torch.float16).view(3, n, H, D)
     d_out = torch.empty((n, H, D), dtype=torch.float32, device="cuda")
     ws = cache.zeroed_workspace(n, max_ctx)
     a = _args(cache, ws, d_meta, d_qkv, d_out, n, max_blocks, max_ctx, w.scale, stream)
@@ -79,8 +89,12 @@ def _run(one_call: bool, seed: int):
         for i in range(STEPS):
             row = pin_meta[i]
             base = row.data_ptr()
-            qkv_bytes = pin_qkv[i].numel() * 2
-            if one_call:
+            if one_call and merged:
+                r = rows[i].data_ptr()
+                copies += abi.kv_decode_step(alloc.handle, cache.handle, seq_arr, n, max_blocks, r,
+                                             d_row.data_ptr(), r + off, d_row.data_ptr() + off, qkv_bytes,
+                                             pin_out[i].data_ptr(), d_out.numel() * 4, a)
+            elif one_call:
                 copies += abi.kv_decode_step(alloc.handle, cache.handle, seq_arr, n, max_blocks, base,
                                              d_meta.data_ptr(), pin_qkv[i].data_ptr(), d_qkv.data_ptr(), qkv_bytes,
                                              pin_out[i].data_ptr(), d_out.numel() * 4, a)
@@ -105,9 +119,10 @@ def _run(one_call: bool, seed: int):
     return res
 
 
-def test_decode_step_matches_the_call_by_call_path_and_the_oracle():
+@pytest.mark.parametrize("merged", [False, True])
+def test_decode_step_matches_the_call_by_call_path_and_the_oracle(merged):
     build.build()
-    one = _run(True, 801)
+    one = _run(True, 801, merged)
     ref = _run(False, 801)
     assert one["err"] == 0 and ref["err"] == 0
     assert one["copies"] == ref["copies"] == CANDS - 1        # all but the last sharer copy
