@@ -439,11 +439,12 @@ int kv_decode_step(kv_alloc* alloc, kv_pool* pool, const int32_t* seqs, int n, i
     const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(tab + 3 * static_cast<int64_t>(n));
     // inputs placed at the same offset after the staging buffer on both sides (at most 256
     // bytes of padding) travel with it in one copy: each copy has a fixed cost in the stream
-    const ptrdiff_t off_h = static_cast<const char*>(inputs_h) - reinterpret_cast<const char*>(staging);
-    const ptrdiff_t off_d = static_cast<const char*>(inputs_d) - reinterpret_cast<const char*>(dev_meta);
-    const bool one_copy = inputs_bytes && off_h == off_d && off_h >= static_cast<ptrdiff_t>(meta_bytes) &&
-                          off_h <= static_cast<ptrdiff_t>(meta_bytes) + 256;
-    const size_t first = one_copy ? static_cast<size_t>(off_h) + inputs_bytes : meta_bytes;
+    // (addresses compared as integers: the buffers are separate allocations)
+    const uintptr_t ih = reinterpret_cast<uintptr_t>(inputs_h), sh = reinterpret_cast<uintptr_t>(staging);
+    const uintptr_t id = reinterpret_cast<uintptr_t>(inputs_d), sd = reinterpret_cast<uintptr_t>(dev_meta);
+    const bool one_copy = inputs_bytes && ih >= sh + meta_bytes && ih <= sh + meta_bytes + 256 &&
+                          id >= sd && id - sd == ih - sh;
+    const size_t first = one_copy ? static_cast<size_t>(ih - sh) + inputs_bytes : meta_bytes;
     if (cudaMemcpyAsync(dev_meta, staging, first, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return KV_ERR_CUDA;
     if (inputs_bytes && !one_copy &&
